@@ -1,0 +1,302 @@
+// k_attn.cu — block attention of the drafter:
+//   o = softmax(q [K_ctx || K_blk]^T / sqrt(d)) [V_ctx || V_blk]
+// non-causal (the whole block is drafted in one parallel pass: mlx-dspark
+// v0.0.3 release notes, "Highlights"), GQA, over the sequence's committed
+// context K/V followed by the block's own K/V.
+//
+// One CTA per (context split, kv head, sequence).  The B block rows times the
+// nq/nkv query heads that share a kv head form one query tile (64 rows for
+// B = 16, group 4), so every K/V byte is read once per kv head.  Long contexts
+// are split along the keys (flash-decoding; the pages' long-context verify
+// likewise uses a two-pass attention, dflash-mlx summary, "기술적 도전":
+// JIT SDPA 2-pass for N >= 1024): each split keeps an online softmax and
+// writes its normalised partial output and log-sum-exp; the last split CTA of
+// a (sequence, kv head) to finish (atomic ticket, no spinning) merges the
+// partials in split order.  Q.K^T and P.V run on m16n8k16 tensor-core MMAs
+// with fp32 accumulation; K/V tiles of 64 keys are double-buffered with
+// cp.async into XOR-swizzled shared memory.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dfl {
+
+namespace {
+
+constexpr int kMaxSplits = 32;
+constexpr int kMinChunk = 128;
+constexpr int kKT = 64;  // keys per tile
+
+__device__ __forceinline__ void split_range(int total, int sp, int& ns, int& k0, int& k1) {
+  ns = (total + kMinChunk - 1) / kMinChunk;
+  if (ns > kMaxSplits) ns = kMaxSplits;
+  if (ns < 1) ns = 1;
+  int chunk = (total + ns - 1) / ns;
+  chunk = (chunk + kKT - 1) / kKT * kKT;
+  ns = (total + chunk - 1) / chunk;
+  k0 = sp * chunk;
+  k1 = min(total, k0 + chunk);
+}
+
+template <int D>
+__global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
+  constexpr int RB = D * 2;  // bytes per row
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  const int sp = blockIdx.x, g = blockIdx.y, j = blockIdx.z;
+  const int grp = a.nq / a.nkv;
+  const int rows = a.B * grp;
+  const int nw = blockDim.x >> 5;
+  const int rows_pad = nw * 16;
+  uint8_t* sQ = smem;
+  uint8_t* sK = sQ + rows_pad * RB;        // [2][64][D]
+  uint8_t* sV = sK + 2 * kKT * RB;         // [2][64][D]
+  int* flag = reinterpret_cast<int*>(sV + 2 * kKT * RB);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  pdl_wait();
+  int L = a.len[j];
+  if (L < 0) L = 0;
+  if (L > a.cap) L = a.cap;
+  const int total = L + a.B;
+  int ns, k0, k1;
+  split_range(total, sp, ns, k0, k1);
+  if (sp >= ns) return;
+
+  // ---- Q tile: row rho = tok * grp + hh  ->  q[(j B + tok)][g grp + hh][:]
+  for (int c = threadIdx.x; c < rows_pad * (D / 8); c += blockDim.x) {
+    int rho = c / (D / 8), ch = c % (D / 8);
+    bool ok = rho < rows;
+    const __half* src = a.q;
+    if (ok) {
+      int tok = rho / grp, hh = rho - tok * grp;
+      src = a.q + ((size_t)(j * a.B + tok) * a.nq + (g * grp + hh)) * D + ch * 8;
+    }
+    cp_async16(sQ + rho * RB + ((ch ^ (rho & 7)) << 4), src, ok);
+  }
+  auto load_kv = [&](int buf, int t0) {
+    for (int c = threadIdx.x; c < kKT * (D / 8); c += blockDim.x) {
+      int r = c / (D / 8), ch = c % (D / 8);
+      int t = t0 + r;
+      bool ok = t < k1;
+      const __half* ks = a.kc;
+      const __half* vs = a.vc;
+      if (ok) {
+        if (t < L) {
+          size_t off = (((size_t)j * a.nkv + g) * a.cap + t) * D + ch * 8;
+          ks = a.kc + off;
+          vs = a.vc + off;
+        } else {
+          size_t off = ((size_t)(j * a.B + (t - L)) * a.nkv + g) * D + ch * 8;
+          ks = a.kblk + off;
+          vs = a.vblk + off;
+        }
+      }
+      int so = buf * kKT * RB + r * RB + ((ch ^ (r & 7)) << 4);
+      cp_async16(sK + so, ks, ok);
+      cp_async16(sV + so, vs, ok);
+    }
+  };
+  const int ntile = (k1 - k0 + kKT - 1) / kKT;
+  load_kv(0, k0);
+  cp_async_commit();
+
+  const float sl2 = rsqrtf((float)D) * 1.4426950408889634f;
+  const int g8 = lane >> 2, t4 = lane & 3;
+  float o[D / 8][4];
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
+  float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
+  uint32_t qf[D / 16][4];
+
+  for (int it = 0; it < ntile; ++it) {
+    if (it + 1 < ntile) load_kv((it + 1) & 1, k0 + (it + 1) * kKT);
+    cp_async_commit();
+    cp_async_wait<1>();
+    __syncthreads();
+    if (it == 0) {
+      const uint32_t qb = smem_u32(sQ);
+#pragma unroll
+      for (int ks = 0; ks < D / 16; ++ks) {
+        int row = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        int ch = 2 * ks + (lane >> 4);
+        ldsm_x4(qb + row * RB + ((ch ^ (row & 7)) << 4), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+      }
+    }
+    const int buf = it & 1;
+    const uint32_t kb = smem_u32(sK + buf * kKT * RB);
+    const uint32_t vb = smem_u32(sV + buf * kKT * RB);
+    // S = Q K^T : 16 rows x 64 keys per warp
+    float s[8][4];
+#pragma unroll
+    for (int n = 0; n < 8; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[n][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+#pragma unroll
+      for (int n16 = 0; n16 < 4; ++n16) {
+        int key = n16 * 16 + (lane & 7) + ((lane >> 4) << 3);
+        int ch = 2 * ks + ((lane >> 3) & 1);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kb + key * RB + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+        mma_f16(s[2 * n16], qf[ks], b0, b1);
+        mma_f16(s[2 * n16 + 1], qf[ks], b2, b3);
+      }
+    }
+    // scale, mask, online softmax (rows g8 and g8 + 8 of this warp)
+    const int kbase = k0 + it * kKT;
+    float mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int n = 0; n < 8; ++n)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        int key = kbase + n * 8 + 2 * t4 + (e & 1);
+        float v = key < k1 ? s[n][e] * sl2 : -INFINITY;
+        s[n][e] = v;
+        mx[e >> 1] = fmaxf(mx[e >> 1], v);
+      }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+    }
+    float corr[2], mnew[2], rs[2] = {0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      mnew[r] = fmaxf(mrow[r], mx[r]);
+      corr[r] = exp2f(mrow[r] - mnew[r]);
+      mrow[r] = mnew[r];
+    }
+    uint32_t pf[4][4];  // P as the A operand of P.V, 4 k16 steps over 64 keys
+#pragma unroll
+    for (int n = 0; n < 8; ++n) {
+      float p0 = exp2f(s[n][0] - mnew[0]);
+      float p1 = exp2f(s[n][1] - mnew[0]);
+      float p2 = exp2f(s[n][2] - mnew[1]);
+      float p3 = exp2f(s[n][3] - mnew[1]);
+      rs[0] += p0 + p1;
+      rs[1] += p2 + p3;
+      __half2 h01 = __floats2half2_rn(p0, p1);
+      __half2 h23 = __floats2half2_rn(p2, p3);
+      pf[n >> 1][(n & 1) * 2 + 0] = *reinterpret_cast<uint32_t*>(&h01);
+      pf[n >> 1][(n & 1) * 2 + 1] = *reinterpret_cast<uint32_t*>(&h23);
+    }
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      rs[r] += __shfl_xor_sync(0xffffffffu, rs[r], 1);
+      rs[r] += __shfl_xor_sync(0xffffffffu, rs[r], 2);
+      lrow[r] = lrow[r] * corr[r] + rs[r];
+    }
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+      o[i][0] *= corr[0];
+      o[i][1] *= corr[0];
+      o[i][2] *= corr[1];
+      o[i][3] *= corr[1];
+    }
+    // O += P V
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+#pragma unroll
+      for (int dp = 0; dp < D / 16; ++dp) {
+        int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+        int ch = 2 * dp + (lane >> 4);
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(vb + key * RB + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+        mma_f16(o[2 * dp], pf[kk], b0, b1);
+        mma_f16(o[2 * dp + 1], pf[kk], b2, b3);
+      }
+    }
+    __syncthreads();
+  }
+  pdl_trigger();
+
+  // normalise this split's rows; log2-domain log-sum-exp
+  float inv[2], lse[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    inv[r] = lrow[r] > 0.f ? 1.f / lrow[r] : 0.f;
+    lse[r] = mrow[r] + log2f(lrow[r]);
+  }
+  const int grp_rows = rows;
+  if (ns == 1) {
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        int rho = warp * 16 + g8 + ((e >> 1) << 3);
+        if (rho >= grp_rows) continue;
+        int tok = rho / grp, hh = rho - tok * grp;
+        int dim = i * 8 + 2 * t4 + (e & 1);
+        a.out[((size_t)(j * a.B + tok) * a.nq + g * grp + hh) * D + dim] = __float2half_rn(o[i][e] * inv[e >> 1]);
+      }
+    return;
+  }
+  const size_t base = ((size_t)(j * a.nkv + g) * kMaxSplits);
+  float* op = a.opart + (base + sp) * (size_t)rows_pad * D;
+  float* ml = a.mlpart + (base + sp) * (size_t)rows_pad;
+#pragma unroll
+  for (int i = 0; i < D / 8; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      int rho = warp * 16 + g8 + ((e >> 1) << 3);
+      int dim = i * 8 + 2 * t4 + (e & 1);
+      op[(size_t)rho * D + dim] = o[i][e] * inv[e >> 1];
+    }
+  if (t4 == 0) {
+    ml[warp * 16 + g8] = lse[0];
+    ml[warp * 16 + g8 + 8] = lse[1];
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int old = atomicAdd(&a.tickets[j * a.nkv + g], 1);
+    *flag = (old == ns - 1);
+  }
+  __syncthreads();
+  if (!*flag) return;
+  __threadfence();
+  const float* op0 = a.opart + base * (size_t)rows_pad * D;
+  const float* ml0 = a.mlpart + base * (size_t)rows_pad;
+  for (int c = threadIdx.x; c < grp_rows * D; c += blockDim.x) {
+    int rho = c / D, dim = c - rho * D;
+    float mmax = -INFINITY;
+    for (int s2 = 0; s2 < ns; ++s2) mmax = fmaxf(mmax, __ldcg(ml0 + (size_t)s2 * rows_pad + rho));
+    float num = 0.f, den = 0.f;
+    for (int s2 = 0; s2 < ns; ++s2) {
+      float w = exp2f(__ldcg(ml0 + (size_t)s2 * rows_pad + rho) - mmax);
+      num += w * __ldcg(op0 + ((size_t)s2 * rows_pad + rho) * D + dim);
+      den += w;
+    }
+    int tok = rho / grp, hh = rho - tok * grp;
+    a.out[((size_t)(j * a.B + tok) * a.nq + g * grp + hh) * D + dim] = __float2half_rn(num / den);
+  }
+  if (threadIdx.x == 0) a.tickets[j * a.nkv + g] = 0;
+}
+
+}  // namespace
+
+size_t attn_ws_bytes(int b, int B, int nq, int nkv, int d) {
+  int rows = B * (nq / nkv);
+  int rows_pad = (rows + 15) / 16 * 16;
+  size_t n = (size_t)b * nkv * kMaxSplits;
+  return n * rows_pad * d * sizeof(float) + n * rows_pad * sizeof(float);
+}
+
+cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
+  AttnArgs a = a0;
+  a.max_splits = kMaxSplits;
+  const int rows = a.B * (a.nq / a.nkv);
+  const int nw = (rows + 15) / 16;
+  const int rows_pad = nw * 16;
+  const size_t smem = 128 + (size_t)rows_pad * a.d * 2 + 4 * kKT * a.d * 2 + 16;
+  dim3 grid(kMaxSplits, a.nkv, a.b);
+  void* args[] = {&a};
+  const void* fn = a.d == 128 ? (const void*)attn_kernel<128> : (const void*)attn_kernel<64>;
+  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return launch_k(fn, grid, dim3(nw * 32), smem, st, pdl, args);
+}
+
+}  // namespace dfl

@@ -1,0 +1,478 @@
+// k_gemm_w8.cu — skinny W8A16 GEMM  Y[M x N] = s[N] . (X[M x K] Q[N x K]^T)
+// with fused epilogues, and the packer that produces its weight layout.
+//
+// Method: int8 projection weights with one fp16 scale per output channel,
+// dequantised as q * s (mirror-sd README, "The Story", Phase 3; "How It Works":
+// int8 constants dequantised affinely).  At M = 16..32 activation rows the
+// contraction streams every weight byte once and does 2M flops per byte, far
+// below GB300's ridge, so the kernel is built to keep HBM busy:
+//  * swap-AB: weights are the 16-row MMA operand, activations the 8-column
+//    one, so the thin M side never pads a 128-row tile;
+//  * a producer warp streams 16 KB packed weight tiles with 1-D bulk copies
+//    (the packer lays each tile out in MMA-fragment order, so a copy needs no
+//    tensor map and every consumer lane reads 16 contiguous bytes), and the
+//    matching 128-column activation slice with a 2-D TMA load (128-byte
+//    swizzle, rows past M zero-filled), into a 4-stage mbarrier ring;
+//  * consumer warps turn biased int8 into fp16 exactly in registers and issue
+//    m16n8k16 MMAs with fp32 accumulation; the scale is applied after the
+//    K reduction;
+//  * split-K over CTAs with a deterministic reduction: every split writes its
+//    partial tile, the last CTA to arrive (atomic ticket, no spinning) sums
+//    the partials in split order and runs the epilogue;
+//  * programmatic dependent launch: the weight copies of the first stages are
+//    issued before griddepcontrol.wait, overlapping the previous kernel's tail.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dfl {
+
+namespace {
+
+constexpr int kStages = 4;
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+
+template <int MT>
+struct Geo {
+  static constexpr int MCH = MT * 8;          // activation rows per chunk
+  static constexpr int ABYTES = 2 * MCH * 128;  // two [MCH][64] fp16 halves
+  static constexpr int STAGE = kTileBytes + ABYTES;
+  static constexpr int TSTRIDE = 132;  // epilogue tile row stride (floats)
+  static constexpr size_t SMEM = 1024 + kStages * (size_t)STAGE + 2 * kStages * 8 + 64;
+};
+
+// packed row -> logical row
+__device__ __forceinline__ int logical_row(int prow, int layout, int N) {
+  if (layout == 1) {
+    int tile = prow >> 7, r = prow & 127;
+    return r < 64 ? tile * 64 + r : (N >> 1) + tile * 64 + (r - 64);
+  }
+  return prow;
+}
+
+__device__ __forceinline__ void rope_pair(float& x1, float& x2, int pos, int p, int d, float theta) {
+  // angle = pos * theta^(-2p/d), formed and range-reduced in double, then
+  // evaluated with the single-precision sincosf.
+  double inv = exp2(-(2.0 * p / d) * log2((double)theta));
+  double ang = (double)pos * inv;
+  const double two_pi = 6.283185307179586476925286766559;
+  ang -= two_pi * rint(ang / two_pi);
+  float sn, cs;
+  sincosf((float)ang, &sn, &cs);
+  float a = x1, b = x2;
+  x1 = a * cs - b * sn;
+  x2 = b * cs + a * sn;
+}
+
+template <int MT>
+__device__ void epilogue(const W8Args& a, const float* T, int nt, int z, int warp, int lane) {
+  using G = Geo<MT>;
+  const int tid = threadIdx.x;
+  const int nthr = blockDim.x;
+  const int prow0 = a.row0 + nt * kTile;  // first packed row of this tile
+  if (a.epi == EPI_STORE_F32 || a.epi == EPI_RESID_F32) {
+    for (int i = tid; i < G::MCH * kTile; i += nthr) {
+      int tok = i >> 7, r = i & 127;
+      int m = z * G::MCH + tok;
+      if (m >= a.M) continue;
+      int n = logical_row(prow0 + r, a.layout, a.N);
+      float v = T[tok * G::TSTRIDE + r] * __half2float(a.s[n]);
+      float* o = a.out_f32 + (size_t)m * a.ldo + (n - a.row0);
+      if (a.epi == EPI_RESID_F32) *o += v; else *o = v;
+    }
+    return;
+  }
+  if (a.epi == EPI_SWIGLU) {
+    const int F = a.N >> 1;
+    for (int i = tid; i < G::MCH * 64; i += nthr) {
+      int tok = i >> 6, r = i & 63;
+      int m = z * G::MCH + tok;
+      if (m >= a.M) continue;
+      int j = nt * 64 + r;
+      float gate = T[tok * G::TSTRIDE + r] * __half2float(a.s[j]);
+      float up = T[tok * G::TSTRIDE + r + 64] * __half2float(a.s[F + j]);
+      float g = gate / (1.0f + expf(-gate)) * up;
+      a.out_h[(size_t)m * F + j] = __float2half_rn(g);
+    }
+    return;
+  }
+  // per-head epilogues: one warp per activation row, lane holds rows lane+32i
+  const int qd = a.nq * a.d, kd = a.nkv * a.d;
+  const int kind = prow0 < qd ? 0 : (prow0 < qd + kd ? 1 : 2);  // q, k, v
+  for (int tok = warp; tok < G::MCH; tok += kConsumerWarps + 1) {
+    int m = z * G::MCH + tok;
+    if (m >= a.M) continue;
+    int seq = m / a.rows_per_seq, slot = m - seq * a.rows_per_seq;
+    int L0 = a.len[seq];
+    int ccount = 0;
+    if (a.epi == EPI_KVCOMMIT) {
+      int nn = a.nacc[seq];
+      ccount = min(nn + 1, a.rows_per_seq);
+      if (nn < -1 || nn > a.rows_per_seq || L0 < 0 || L0 + max(ccount, 0) > a.cap || slot >= ccount) continue;
+    } else if (L0 < 0) {
+      L0 = 0;
+    }
+    const int pos = L0 + slot;
+    float v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      int r = lane + 32 * i;
+      v[i] = T[tok * G::TSTRIDE + r] * __half2float(a.s[prow0 + r]);
+    }
+    if (kind != 2) {
+      const float* gam = kind == 0 ? a.gq : a.gk;
+      if (a.d == 128) {
+        float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        float inv = rsqrtf(ss / 128.0f + a.eps);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] *= inv * gam[lane + 32 * i];
+        rope_pair(v[0], v[2], pos, lane, 128, a.theta);
+        rope_pair(v[1], v[3], pos, lane + 32, 128, a.theta);
+      } else {  // d == 64: rows 0..63 head A, 64..127 head B
+        float sa = v[0] * v[0] + v[1] * v[1];
+        float sb = v[2] * v[2] + v[3] * v[3];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          sa += __shfl_xor_sync(0xffffffffu, sa, o);
+          sb += __shfl_xor_sync(0xffffffffu, sb, o);
+        }
+        float ia = rsqrtf(sa / 64.0f + a.eps), ib = rsqrtf(sb / 64.0f + a.eps);
+        v[0] *= ia * gam[lane];
+        v[1] *= ia * gam[lane + 32];
+        v[2] *= ib * gam[lane];
+        v[3] *= ib * gam[lane + 32];
+        rope_pair(v[0], v[1], pos, lane, 64, a.theta);
+        rope_pair(v[2], v[3], pos, lane, 64, a.theta);
+      }
+    }
+    if (a.epi == EPI_QKV) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        int row = prow0 + lane + 32 * i;
+        __half hv = __float2half_rn(v[i]);
+        if (kind == 0) a.out_h[(size_t)m * qd + row] = hv;
+        else if (kind == 1) a.kout[(size_t)m * kd + (row - qd)] = hv;
+        else a.vout[(size_t)m * kd + (row - qd - kd)] = hv;
+      }
+    } else {  // EPI_KVCOMMIT: cache [b][nkv][cap][d]
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        int row = prow0 + lane + 32 * i - qd;  // within k|v rows
+        int isv = row >= kd;
+        int rr = isv ? row - kd : row;
+        int h = rr / a.d, e = rr - h * a.d;
+        size_t off = (((size_t)seq * a.nkv + h) * a.cap + pos) * a.d + e;
+        (isv ? a.vout : a.kout)[off] = __float2half_rn(v[i]);
+      }
+    }
+  }
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                               const W8Args a) {
+  using G = Geo<MT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * G::STAGE);
+  uint64_t* empty = full + kStages;
+  int* flag = reinterpret_cast<int*>(empty + kStages);
+
+  const int nt = blockIdx.x, sp = blockIdx.y, z = blockIdx.z;
+  const int ntiles = gridDim.x;
+  const int KT = a.K / kTile;
+  const int kt0 = (int)(((long long)sp * KT) / a.splits);
+  const int kt1 = (int)(((long long)(sp + 1) * KT) / a.splits);
+  const int nk = kt1 - kt0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  float acc[2][MT][4];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int j = 0; j < MT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[i][j][e] = 0.f;
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&xmap);
+      const uint8_t* wsrc = a.q + ((size_t)((a.row0 >> 7) + nt) * KT + kt0) * kTileBytes;
+      const uint64_t pol = policy_evict_first();
+      const int pre = nk < kStages ? nk : kStages;
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], G::STAGE);
+        bulk_g2s_hint(smem + i * G::STAGE, wsrc + (size_t)i * kTileBytes, kTileBytes, &full[i], pol);
+      }
+      pdl_wait();
+      for (int i = 0; i < pre; ++i) {
+        uint8_t* sa = smem + i * G::STAGE + kTileBytes;
+        tma_load_2d(sa, &xmap, (kt0 + i) * kTile, z * G::MCH, &full[i]);
+        tma_load_2d(sa + G::MCH * 128, &xmap, (kt0 + i) * kTile + 64, z * G::MCH, &full[i]);
+      }
+      for (int i = pre; i < nk; ++i) {
+        const int slot = i % kStages;
+        if (!mbar_wait(&empty[slot], ((i / kStages) - 1) & 1, a.status)) break;
+        mbar_arrive_expect_tx(&full[slot], G::STAGE);
+        uint8_t* st = smem + slot * G::STAGE;
+        bulk_g2s_hint(st, wsrc + (size_t)i * kTileBytes, kTileBytes, &full[slot], pol);
+        tma_load_2d(st + kTileBytes, &xmap, (kt0 + i) * kTile, z * G::MCH, &full[slot]);
+        tma_load_2d(st + kTileBytes + G::MCH * 128, &xmap, (kt0 + i) * kTile + 64, z * G::MCH, &full[slot]);
+      }
+    }
+    pdl_trigger();
+  } else {
+    // ---------------- consumers ----------------
+    pdl_wait();
+    const int g_tok_lo = (lane & 7) + ((lane >> 4) << 3);
+    const int ch_hi = (lane >> 3) & 1;
+    for (int i = 0; i < nk; ++i) {
+      const int slot = i % kStages;
+      if (!mbar_wait(&full[slot], (i / kStages) & 1, a.status)) break;
+      const uint8_t* wl = smem + slot * G::STAGE + (warp * 8 * 32 + lane) * 16;
+      const uint32_t abase = smem_u32(smem + slot * G::STAGE + kTileBytes);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        uint4 wq = *reinterpret_cast<const uint4*>(wl + ks * 32 * 16);
+        uint32_t af[2][4];
+        biased_u8x4_to_half2x2(wq.x, af[0][0], af[0][1]);
+        biased_u8x4_to_half2x2(wq.y, af[0][2], af[0][3]);
+        biased_u8x4_to_half2x2(wq.z, af[1][0], af[1][1]);
+        biased_u8x4_to_half2x2(wq.w, af[1][2], af[1][3]);
+        const uint32_t hbase = abase + (ks >> 2) * (G::MCH * 128);
+        const int ch = ((ks & 3) << 1) + ch_hi;
+#pragma unroll
+        for (int p = 0; p < MT / 2; ++p) {
+          const int tok = p * 16 + g_tok_lo;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(hbase + tok * 128 + ((ch ^ (tok & 7)) << 4), b0, b1, b2, b3);
+          mma_f16(acc[0][2 * p], af[0], b0, b1);
+          mma_f16(acc[1][2 * p], af[1], b0, b1);
+          mma_f16(acc[0][2 * p + 1], af[0], b2, b3);
+          mma_f16(acc[1][2 * p + 1], af[1], b2, b3);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    pdl_trigger();
+  }
+  __syncthreads();  // all stages consumed: the ring can be reused as scratch
+
+  float* T = reinterpret_cast<float*>(smem);  // [MCH][TSTRIDE]
+  const int g = lane >> 2, t = lane & 3;
+  const size_t part_tile = (size_t)G::MCH * kTile;
+  const int tix = z * ntiles + nt;
+  if (warp < kConsumerWarps) {
+    if (a.splits == 1) {
+#pragma unroll
+      for (int mg = 0; mg < 2; ++mg)
+#pragma unroll
+        for (int j = 0; j < MT; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            int r = warp * 32 + mg * 16 + g + ((e >> 1) << 3);
+            int tok = j * 8 + 2 * t + (e & 1);
+            T[tok * G::TSTRIDE + r] = acc[mg][j][e];
+          }
+    } else {
+      float* P = a.part + ((size_t)tix * a.splits + sp) * part_tile;
+#pragma unroll
+      for (int mg = 0; mg < 2; ++mg)
+#pragma unroll
+        for (int j = 0; j < MT; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            int r = warp * 32 + mg * 16 + g + ((e >> 1) << 3);
+            int tok = j * 8 + 2 * t + (e & 1);
+            P[tok * kTile + r] = acc[mg][j][e];
+          }
+    }
+  }
+  if (a.splits > 1) {
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int old = atomicAdd(&a.tickets[tix], 1);
+      *flag = (old == a.splits - 1);
+    }
+    __syncthreads();
+    if (!*flag) return;
+    __threadfence();
+    const float* P0 = a.part + (size_t)tix * a.splits * part_tile;
+    for (int i = threadIdx.x; i < G::MCH * kTile; i += blockDim.x) {
+      float s = 0.f;
+      for (int sp2 = 0; sp2 < a.splits; ++sp2) s += __ldcg(P0 + sp2 * part_tile + i);
+      T[(i >> 7) * G::TSTRIDE + (i & 127)] = s;
+    }
+    if (threadIdx.x == 0) a.tickets[tix] = 0;
+  }
+  __syncthreads();
+  epilogue<MT>(a, T, nt, z, warp, lane);
+}
+
+// ------------------------------------------------------------- packing ----
+template <typename T>
+__device__ __forceinline__ float ld_w(const void* w, size_t i);
+template <>
+__device__ __forceinline__ float ld_w<float>(const void* w, size_t i) {
+  return static_cast<const float*>(w)[i];
+}
+template <>
+__device__ __forceinline__ float ld_w<__half>(const void* w, size_t i) {
+  return __half2float(static_cast<const __half*>(w)[i]);
+}
+template <>
+__device__ __forceinline__ float ld_w<__nv_bfloat16>(const void* w, size_t i) {
+  return __bfloat162float(static_cast<const __nv_bfloat16*>(w)[i]);
+}
+
+// s[n] = fp16(absmax_n / 127): one warp per logical row
+template <typename T>
+__global__ void pack_scale_kernel(const void* w, int64_t N, int64_t K, __half* s) {
+  int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (row >= N) return;
+  int lane = threadIdx.x & 31;
+  float m = 0.f;
+  for (int64_t k = lane; k < K; k += 32) m = fmaxf(m, fabsf(ld_w<T>(w, row * K + k)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) s[row] = __float2half_rn(m / 127.0f);
+}
+
+// one thread per 16-byte lane chunk of the packed layout:
+// tile (nt, kt) -> [warp 4][kstep 8][lane 32][frag(2w) 8 B | frag(2w+1) 8 B]
+template <typename T>
+__global__ void pack_q_kernel(const void* w, int64_t N, int64_t K, int layout, const __half* s, uint8_t* q) {
+  int64_t chunk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  int64_t nchunks = N * K / 16;
+  if (chunk >= nchunks) return;
+  const int64_t KT = K / kTile;
+  int64_t tile = chunk >> 10;
+  int within = (int)(chunk & 1023);
+  int wq = within >> 8, ks = (within >> 5) & 7, ln = within & 31;
+  int64_t nt = tile / KT, kt = tile - nt * KT;
+  int g = ln >> 2, t = ln & 3;
+  uint32_t out[4];
+#pragma unroll
+  for (int f = 0; f < 2; ++f) {
+    int mg = 2 * wq + f;
+    uint32_t word[2] = {0u, 0u};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      // byte order of one m16k16 fragment for lane (g, t)
+      int r = g + ((e >> 1) & 1) * 8;
+      int c = 2 * t + (e & 1) + ((e >> 2) & 1) * 8;
+      int64_t prow = nt * kTile + mg * 16 + r;
+      int64_t lrow = prow;
+      if (layout == 1) {
+        int64_t tl = prow >> 7, rr = prow & 127;
+        lrow = rr < 64 ? tl * 64 + rr : (N >> 1) + tl * 64 + (rr - 64);
+      }
+      int64_t col = kt * kTile + ks * 16 + c;
+      float sc = __half2float(s[lrow]);
+      int qv = 0;
+      if (sc != 0.f) {
+        float r_ = rintf(ld_w<T>(w, lrow * K + col) / sc);
+        r_ = fminf(fmaxf(r_, -127.f), 127.f);
+        qv = (int)r_;
+      }
+      uint32_t byte = (uint32_t)((qv + 128) & 0xFF);
+      word[e >> 2] |= byte << (8 * (e & 3));
+    }
+    out[2 * f] = word[0];
+    out[2 * f + 1] = word[1];
+  }
+  reinterpret_cast<uint4*>(q)[chunk] = make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+}  // namespace
+
+int w8_pick_splits(int units, int KT) {
+  int target = 2 * kNumSMs;
+  int s = (target + units - 1) / units;
+  int smax = KT >= 4 ? KT / 2 : 1;
+  if (s > smax) s = smax;
+  if (s < 1) s = 1;
+  return s;
+}
+
+static int pick_mt(int M) { return M <= 16 ? 2 : 4; }
+
+size_t w8_partial_bytes(int M, int nrows, int K) {
+  int mt = pick_mt(M), mch = mt * 8;
+  int chunks = (M + mch - 1) / mch;
+  int units = chunks * (nrows / kTile);
+  int s = w8_pick_splits(units, K / kTile);
+  if (s == 1) return 0;
+  return (size_t)units * s * mch * kTile * sizeof(float);
+}
+
+size_t w8_ticket_count(int M, int nrows) {
+  int mt = pick_mt(M), mch = mt * 8;
+  return (size_t)((M + mch - 1) / mch) * (nrows / kTile);
+}
+
+cudaError_t w8_gemm(const W8Args& a0, const __half* x, cudaStream_t st, bool pdl) {
+  W8Args a = a0;
+  const int mt = pick_mt(a.M);
+  const int mch = mt * 8;
+  const int chunks = (a.M + mch - 1) / mch;
+  const int ntiles = a.nrows / kTile;
+  a.splits = w8_pick_splits(chunks * ntiles, a.K / kTile);
+  CUtensorMap map;
+  if (!encode_tmap_2d(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, (uint64_t)a.K, (uint64_t)a.M,
+                      (uint64_t)a.K * 2, 64, (uint32_t)mch, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  void* args[] = {&map, &a};
+  dim3 grid(ntiles, a.splits, chunks);
+  if (mt == 2) {
+    static bool attr = false;
+    if (!attr) {
+      cudaFuncSetAttribute((const void*)w8_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)Geo<2>::SMEM);
+      attr = true;
+    }
+    return launch_k((const void*)w8_gemm_kernel<2>, grid, dim3(kThreads), Geo<2>::SMEM, st, pdl, args);
+  }
+  static bool attr4 = false;
+  if (!attr4) {
+    cudaFuncSetAttribute((const void*)w8_gemm_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)Geo<4>::SMEM);
+    attr4 = true;
+  }
+  return launch_k((const void*)w8_gemm_kernel<4>, grid, dim3(kThreads), Geo<4>::SMEM, st, pdl, args);
+}
+
+cudaError_t w8_pack(const void* w, int w_dtype, int64_t N, int64_t K, int layout, uint8_t* q_out, __half* s_out,
+                    cudaStream_t st) {
+  dim3 b1(256);
+  dim3 g1((unsigned)((N + 7) / 8));
+  int64_t nchunks = N * K / 16;
+  dim3 g2((unsigned)((nchunks + 255) / 256));
+  if (w_dtype == 0) {
+    pack_scale_kernel<float><<<g1, b1, 0, st>>>(w, N, K, s_out);
+    pack_q_kernel<float><<<g2, 256, 0, st>>>(w, N, K, layout, s_out, q_out);
+  } else if (w_dtype == 1) {
+    pack_scale_kernel<__half><<<g1, b1, 0, st>>>(w, N, K, s_out);
+    pack_q_kernel<__half><<<g2, 256, 0, st>>>(w, N, K, layout, s_out, q_out);
+  } else {
+    pack_scale_kernel<__nv_bfloat16><<<g1, b1, 0, st>>>(w, N, K, s_out);
+    pack_q_kernel<__nv_bfloat16><<<g2, 256, 0, st>>>(w, N, K, layout, s_out, q_out);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace dfl

@@ -1,0 +1,104 @@
+// kernels.h — host-side launchers shared between the C-ABI translation unit
+// and the kernel translation units.  Plain C++ declarations, no device code.
+#pragma once
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dfl {
+
+constexpr int kTile = 128;         // packed W8 tile edge (rows x k-columns)
+constexpr int kTileBytes = 16384;  // one packed int8 tile
+constexpr int kNumSMs = 152;
+
+enum Epi : int {
+  EPI_STORE_F32 = 0,  // out[m][n] = y
+  EPI_RESID_F32 = 1,  // out[m][n] += y
+  EPI_SWIGLU = 2,     // g[m][j] = silu(gate_j) * up_j  (fp16)
+  EPI_QKV = 3,        // per-head Q/K RMSNorm + RoPE; q, block k, block v (fp16)
+  EPI_KVCOMMIT = 4,   // per-head K RMSNorm + RoPE; K, V appended to the cache
+};
+
+struct W8Args {
+  const uint8_t* q;  // packed tiles
+  const __half* s;   // logical-order scales
+  int N, K, layout;
+  int row0;   // first packed row used (multiple of 128)
+  int nrows;  // packed rows used (multiple of 128)
+  int M;      // activation rows
+  int splits;
+  float* part;   // split-K partials
+  int* tickets;  // per (chunk, tile) arrival counters, zero between calls
+  int epi;
+  float* out_f32;
+  int ldo;
+  __half* out_h;  // EPI_SWIGLU: g [M][F]; EPI_QKV: q [M][nq d]
+  __half* kout;   // EPI_QKV: block k [M][nkv d]; EPI_KVCOMMIT: layer's K cache
+  __half* vout;
+  const float* gq;
+  const float* gk;
+  int nq, nkv, d, F;
+  float theta, eps;
+  const int* len;    // [b] committed lengths
+  const int* nacc;   // EPI_KVCOMMIT: accept lengths
+  int rows_per_seq;  // activation rows per sequence
+  int b, cap;
+  int* status;
+};
+
+// Tensor-map encoder from the driver (resolved once through the runtime).
+bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);
+
+// Launch helper: PDL attribute on when `pdl`.
+cudaError_t launch_k(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, void** args);
+
+// --- W8A16 GEMM (k_gemm_w8.cu) ---
+int w8_pick_splits(int units, int KT);
+size_t w8_partial_bytes(int M, int nrows, int K);
+size_t w8_ticket_count(int M, int nrows);
+cudaError_t w8_gemm(const W8Args& a, const __half* x, cudaStream_t st, bool pdl);
+cudaError_t w8_pack(const void* w, int w_dtype, int64_t N, int64_t K, int layout, uint8_t* q_out, __half* s_out,
+                    cudaStream_t st);
+
+// --- lm-head GEMM + argmax (k_lmhead.cu) ---
+size_t lmhead_ws_bytes(int64_t M);
+cudaError_t lmhead_argmax(const __nv_bfloat16* h, const __nv_bfloat16* w, int M, int V, int H, int* idx_out,
+                          float* maxlogit, float* logits, void* ws, cudaStream_t st, bool pdl, int* status);
+
+// --- block attention (k_attn.cu) ---
+struct AttnArgs {
+  const __half* q;     // [M][nq][d]
+  const __half* kblk;  // [M][nkv][d]
+  const __half* vblk;
+  const __half* kc;  // layer's K cache [b][nkv][cap][d]
+  const __half* vc;
+  const int* len;
+  __half* out;  // [M][nq][d]
+  float* opart;
+  float* mlpart;
+  int* tickets;  // [b][nkv]
+  int b, B, nq, nkv, d, cap;
+  int max_splits;
+  int* status;
+};
+size_t attn_ws_bytes(int b, int B, int nq, int nkv, int d);
+cudaError_t attention(const AttnArgs& a, cudaStream_t st, bool pdl);
+
+// --- small kernels (k_small.cu) ---
+cudaError_t embed_rmsnorm(const __nv_bfloat16* E, const int* last_tok, int mask_id, int V, int b, int B, int H,
+                          const float* gamma, float eps, float* x, __half* u, cudaStream_t st, bool pdl,
+                          int* status);
+cudaError_t rmsnorm_f16(const float* x, int M, int H, const float* gamma, float eps, __half* u, cudaStream_t st,
+                        bool pdl);
+cudaError_t final_norm(const float* x, int b, int B, int H, const float* gamma, float eps, __nv_bfloat16* h,
+                       float* hidden_out, cudaStream_t st, bool pdl);
+cudaError_t commit_len_update(int* len, const int* nacc, int b, int rows_per_seq, int cap, cudaStream_t st,
+                              bool pdl, int* status);
+size_t verify_ws_bytes(int b, int R, int64_t V);
+cudaError_t verify_accept(const float* logits, const int* draft, int b, int R, int D, int64_t V, int* n_out,
+                          int* corr_out, int* emitted, int* next_tok, void* ws, cudaStream_t st, bool pdl);
+
+}  // namespace dfl

@@ -1,0 +1,48 @@
+"""Helpers for the GPU parity tests (test infrastructure)."""
+import numpy as np
+
+try:
+    import torch
+except Exception:  # pragma: no cover
+    torch = None
+
+
+def gpu_available() -> bool:
+    return torch is not None and torch.cuda.is_available()
+
+
+def unpack_tiled_q(qbytes: np.ndarray, N: int, K: int, layout: int = 0) -> np.ndarray:
+    """Restates the packed W8 layout of include/dflash.h's packer to recover
+    the logical int8 q[N][K]: 128x128 tiles in (row-tile, k-tile) order, each
+    [warp 4][k16 step 8][lane 32][16 bytes = two 8-byte m16k16 fragments],
+    bytes stored as q + 128."""
+    KT = K // 128
+    t = qbytes.reshape(N // 128, KT, 4, 8, 32, 2, 8).astype(np.int16) - 128
+    q = np.empty((N, K), np.int8)
+    lane = np.arange(32)
+    g, tt = lane // 4, lane % 4
+    e = np.arange(8)
+    r_off = ((e >> 1) & 1) * 8
+    c_off = (e & 1) + ((e >> 2) & 1) * 8
+    rows = g[:, None] + r_off[None, :]          # [32][8]
+    cols = 2 * tt[:, None] + c_off[None, :]     # [32][8]
+    for nt in range(N // 128):
+        for w in range(4):
+            for f in range(2):
+                mg = 2 * w + f
+                for ks in range(8):
+                    blk = t[nt, :, w, ks, :, f, :]  # [KT][32][8]
+                    pr = nt * 128 + mg * 16 + rows      # packed rows
+                    if layout == 1:
+                        tl, rr = pr >> 7, pr & 127
+                        lr = np.where(rr < 64, tl * 64 + rr, N // 2 + tl * 64 + (rr - 64))
+                    else:
+                        lr = pr
+                    for kt in range(KT):
+                        q[lr, kt * 128 + ks * 16 + cols] = blk[kt]
+    return q
+
+
+def rel_err(got, ref) -> float:
+    ref = np.asarray(ref, np.float64)
+    return float(np.abs(np.asarray(got, np.float64) - ref).max() / max(np.abs(ref).max(), 1e-30))
