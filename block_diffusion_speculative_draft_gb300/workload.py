@@ -1,15 +1,16 @@
-"""Shared set-up for whole-step GPU parity tests and bench.py: builds the
-synthetic drafter on the device, commits each sequence's context through
-dflash_kv_commit, and computes the oracle's view of the same inputs.
-(Test and measurement infrastructure; the oracle parts run on the CPU.)"""
+"""Synthetic workload set-up shared by bench.py and the GPU tests: per-sequence
+context lengths, the target hidden rows of each context, and the prefill of
+the draft KV cache through dflash_kv_commit."""
 from __future__ import annotations
 
 import numpy as np
 
-from block_diffusion_speculative_draft_gb300 import synth
+from . import synth
 
 
 def contexts(cfg) -> np.ndarray:
+    """Committed context length per sequence: the workload's fixed lengths or
+    a seeded uniform draw for ragged batches."""
     if cfg.ctx_range is not None:
         return synth.ragged_contexts(cfg.seed, "ctx", cfg.b, *cfg.ctx_range)
     c = list(cfg.ctx) * cfg.b if len(cfg.ctx) == 1 else list(cfg.ctx)
@@ -21,8 +22,9 @@ def context_hidden(cfg, j: int, C: int) -> np.ndarray:
 
 
 def commit_contexts(api, torch, cfg, model, kv, ws, ctx, rows_per_seq: int, dev):
-    """Prefill each sequence's committed context in chunks of rows_per_seq
-    hidden rows (n = rows - 1 per chunk, -1 once a sequence is done)."""
+    """Prefill each sequence's context in chunks of rows_per_seq target hidden
+    rows (n = rows - 1 per chunk, -1 once a sequence is complete).  Returns the
+    host hidden rows of every sequence."""
     b = cfg.b
     W = cfg.k * cfg.H
     hids = [context_hidden(cfg, j, int(ctx[j])) for j in range(b)]

@@ -12,7 +12,7 @@ import pytest
 from oracle import dflash_oracle as O
 from block_diffusion_speculative_draft_gb300 import synth
 from block_diffusion_speculative_draft_gb300.configs import TINY
-from tests.drafter_harness import commit_contexts, contexts
+from block_diffusion_speculative_draft_gb300.workload import commit_contexts, contexts
 from tests.gpu_util import gpu_available, rel_err
 
 pytestmark = [pytest.mark.gpu, pytest.mark.skipif(not gpu_available(), reason="needs a GPU")]

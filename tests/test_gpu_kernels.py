@@ -76,7 +76,7 @@ def test_lmhead_argmax(M, V, H):
     torch.cuda.synchronize()
     ridx, rmax, margin, rlg = O.lmhead_argmax(hb, wb)
     ok = margin > 1e-2
-    assert ok.mean() > 0.5
+    assert ok.sum() >= M // 2
     assert np.array_equal(idx.cpu().numpy()[ok], ridx[ok])
     assert rel_err(lg.cpu().numpy(), rlg) <= 1e-4
     assert np.allclose(mx.cpu().numpy(), rmax, rtol=1e-4, atol=1e-4)
