@@ -2,6 +2,7 @@
 // argument validation, workspace carving and the kernel sequence of one
 // draft step, one verify-accept and one draft-KV commit.  No allocation ever
 // happens here: every byte of scratch comes from the caller's workspace.
+#include <math.h>
 #include <string.h>
 
 #include "../../include/dflash.h"
@@ -39,7 +40,7 @@ int check_cfg(const dflash_config* c) {
   if (c->H % 128 || (c->nq * c->d) % 128 || (c->nkv * c->d) % 128 || c->F % 128 || (c->k * c->H) % 128)
     return DFLASH_EUNSUPPORTED;
   if (c->nq % c->nkv) return DFLASH_EUNSUPPORTED;
-  if (c->B > 32) return DFLASH_EUNSUPPORTED;
+  if (c->B > 32 || c->H > 8192) return DFLASH_EUNSUPPORTED;
   if (c->B * (c->nq / c->nkv) > 160) return DFLASH_EUNSUPPORTED;  // one attention query tile
   return DFLASH_OK;
 }
@@ -61,41 +62,11 @@ struct WS {
   __half* g;
   __nv_bfloat16* h;
   float* y;
-  float* part;
-  int* tickets;
-  float* opart;
-  float* mlpart;
-  int* atickets;
   void* lm;
   size_t total;
 };
 
-size_t max_partial(const dflash_config& c, int M, int Mc) {
-  size_t p = 0;
-  auto upd = [&](size_t v) { p = v > p ? v : p; };
-  const int nqkv = (c.nq + 2 * c.nkv) * c.d;
-  upd(w8_partial_bytes(M, nqkv, c.H));
-  upd(w8_partial_bytes(M, c.H, c.nq * c.d));
-  upd(w8_partial_bytes(M, 2 * c.F, c.H));
-  upd(w8_partial_bytes(M, c.H, c.F));
-  upd(w8_partial_bytes(Mc, c.H, c.k * c.H));
-  upd(w8_partial_bytes(Mc, 2 * c.nkv * c.d, c.H));
-  return p;
-}
-
-size_t max_tickets(const dflash_config& c, int M, int Mc) {
-  size_t p = 0;
-  auto upd = [&](size_t v) { p = v > p ? v : p; };
-  const int nqkv = (c.nq + 2 * c.nkv) * c.d;
-  upd(w8_ticket_count(M, nqkv));
-  upd(w8_ticket_count(M, c.H));
-  upd(w8_ticket_count(M, 2 * c.F));
-  upd(w8_ticket_count(Mc, c.H));
-  upd(w8_ticket_count(Mc, 2 * c.nkv * c.d));
-  return p;
-}
-
-// Carves the workspace; counters (tickets, argmax keys) come first so a
+// Carves the workspace; the lm-head's argmax keys and ticket come first so a
 // single zero-fill of the whole buffer initialises them.
 WS carve(const dflash_config& c, int b, int rps, uint8_t* base) {
   WS w;
@@ -106,8 +77,6 @@ WS carve(const dflash_config& c, int b, int rps, uint8_t* base) {
     off += al256(bytes);
     return p;
   };
-  w.tickets = (int*)take(max_tickets(c, M, Mc) * sizeof(int));
-  w.atickets = (int*)take((size_t)b * c.nkv * sizeof(int));
   w.lm = take(lmhead_ws_bytes(b * (c.B - 1)));
   w.x = (float*)take((size_t)M * c.H * 4);
   w.u = (__half*)take((size_t)Mx * c.H * 2);
@@ -118,23 +87,13 @@ WS carve(const dflash_config& c, int b, int rps, uint8_t* base) {
   w.g = (__half*)take((size_t)M * c.F * 2);
   w.h = (__nv_bfloat16*)take((size_t)b * (c.B - 1) * c.H * 2);
   w.y = (float*)take((size_t)Mc * c.H * 4);
-  w.part = (float*)take(max_partial(c, M, Mc));
-  size_t ab = attn_ws_bytes(b, c.B, c.nq, c.nkv, c.d);
-  uint8_t* ap = take(ab);
-  w.opart = (float*)ap;
-  {
-    int rows = c.B * (c.nq / c.nkv);
-    int rows_pad = (rows + 15) / 16 * 16;
-    size_t n = (size_t)b * c.nkv * 32;
-    w.mlpart = ap ? (float*)(ap + n * rows_pad * c.d * sizeof(float)) : nullptr;
-  }
   w.total = off;
   return w;
 }
 
 int map_err(cudaError_t e) { return e == cudaSuccess ? DFLASH_OK : DFLASH_ECUDA; }
 
-W8Args base_args(const dflash_w8& w, int M, WS& ws, int epi) {
+W8Args base_args(const dflash_w8& w, int M, int epi) {
   W8Args a;
   memset(&a, 0, sizeof(a));
   a.q = static_cast<const uint8_t*>(w.q);
@@ -145,11 +104,14 @@ W8Args base_args(const dflash_w8& w, int M, WS& ws, int epi) {
   a.row0 = 0;
   a.nrows = (int)w.N;
   a.M = M;
-  a.part = ws.part;
-  a.tickets = ws.tickets;
   a.epi = epi;
   a.status = status_ptr();
   return a;
+}
+
+// RoPE frequencies theta^(-2p/d) for the per-head epilogues, in double
+void fill_inv_freq(W8Args& a, float theta, int d) {
+  for (int p = 0; p < 64; ++p) a.inv_freq[p] = p < d / 2 ? pow((double)theta, -2.0 * p / d) : 0.0;
 }
 
 }  // namespace
@@ -194,18 +156,14 @@ int32_t dflash_pack_w8a16(const void* w, int32_t w_dtype, int64_t N, int64_t K, 
 
 int32_t dflash_w8a16_linear(const dflash_w8* w, const uint16_t* x, int64_t M, float* y, void* ws, size_t ws_bytes,
                             void* stream) {
+  (void)ws;
+  (void)ws_bytes;  // split-K reduces through cluster shared memory: no scratch
   if (!w || !x || !y) return DFLASH_EINVAL;
   if (M < 1 || M > 4096) return DFLASH_EINVAL;
   if (w->N % 128 || w->K % 128 || w->N < 128) return DFLASH_EUNSUPPORTED;
   if (int r = check_w8(*w, w->N, w->K, w->layout)) return r;
   if (!aligned16(x)) return DFLASH_EINVAL;
-  size_t need = al256(w8_ticket_count((int)M, (int)w->N) * sizeof(int)) + w8_partial_bytes((int)M, (int)w->N, (int)w->K);
-  if (!ws || ws_bytes < need) return DFLASH_EWORKSPACE;
-  WS wsv;
-  memset(&wsv, 0, sizeof(wsv));
-  wsv.tickets = static_cast<int*>(ws);
-  wsv.part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + al256(w8_ticket_count((int)M, (int)w->N) * sizeof(int)));
-  W8Args a = base_args(*w, (int)M, wsv, EPI_STORE_F32);
+  W8Args a = base_args(*w, (int)M, EPI_STORE_F32);
   a.out_f32 = y;
   a.ldo = (int)w->N;
   return map_err(w8_gemm(a, reinterpret_cast<const __half*>(x), static_cast<cudaStream_t>(stream), false));
@@ -213,7 +171,7 @@ int32_t dflash_w8a16_linear(const dflash_w8* w, const uint16_t* x, int64_t M, fl
 
 int32_t dflash_w8a16_linear_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes) {
   if (!bytes || M < 1 || M > 4096 || N < 128 || K < 128 || N % 128 || K % 128) return DFLASH_EINVAL;
-  *bytes = al256(w8_ticket_count((int)M, (int)N) * sizeof(int)) + w8_partial_bytes((int)M, (int)N, (int)K);
+  *bytes = 0;
   return DFLASH_OK;
 }
 
@@ -225,7 +183,9 @@ static int check_weights(const dflash_weights* w) {
   if (!w->gamma_hid || !w->gamma_in || !w->gamma_post || !w->gamma_q || !w->gamma_k || !w->gamma_final ||
       !w->embed || !w->lm_head)
     return DFLASH_EINVAL;
-  if (!aligned16(w->lm_head)) return DFLASH_EINVAL;
+  if (!aligned16(w->lm_head) || !aligned16(w->embed) || !aligned16(w->gamma_hid) || !aligned16(w->gamma_in) ||
+      !aligned16(w->gamma_post) || !aligned16(w->gamma_final))
+    return DFLASH_EINVAL;
   if (int r = check_w8(w->fc, c.H, (int64_t)c.k * c.H, DFLASH_LAYOUT_PLAIN)) return r;
   const int64_t nqkv = (int64_t)(c.nq + 2 * c.nkv) * c.d;
   for (int l = 0; l < c.L; ++l) {
@@ -249,6 +209,7 @@ int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const i
   if (int r = check_weights(w)) return r;
   if (int r = check_kv(kv)) return r;
   if (!last_tok || !draft_out) return DFLASH_EINVAL;
+  if (!aligned16(hidden_out)) return DFLASH_EINVAL;
   const dflash_config& c = w->cfg;
   const int b = kv->b;
   if ((int64_t)b * c.B > 4096) return DFLASH_EUNSUPPORTED;
@@ -267,7 +228,8 @@ int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const i
   if (e != cudaSuccess) return DFLASH_ECUDA;
   for (int l = 0; l < c.L; ++l) {
     // [q|k|v] = W8(qkv) u ; per-head QK-RMSNorm + neox RoPE in the epilogue
-    W8Args a = base_args(w->qkv[l], M, s, EPI_QKV);
+    W8Args a = base_args(w->qkv[l], M, EPI_QKV);
+    fill_inv_freq(a, c.rope_theta, c.d);
     a.out_h = s.q;
     a.kout = s.kb;
     a.vout = s.vb;
@@ -292,9 +254,6 @@ int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const i
     at.vc = reinterpret_cast<const __half*>(kv->v) + l * layer_kv;
     at.len = kv->len;
     at.out = s.ao;
-    at.opart = s.opart;
-    at.mlpart = s.mlpart;
-    at.tickets = s.atickets;
     at.b = b;
     at.B = c.B;
     at.nq = c.nq;
@@ -304,18 +263,18 @@ int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const i
     at.status = status;
     if ((e = attention(at, st, true)) != cudaSuccess) return DFLASH_ECUDA;
     // x += W8(o) attn
-    W8Args ao = base_args(w->o[l], M, s, EPI_RESID_F32);
+    W8Args ao = base_args(w->o[l], M, EPI_RESID_F32);
     ao.out_f32 = s.x;
     ao.ldo = c.H;
     if ((e = w8_gemm(ao, s.ao, st, true)) != cudaSuccess) return DFLASH_ECUDA;
     if ((e = rmsnorm_f16(s.x, M, c.H, w->gamma_post + (size_t)l * c.H, c.eps, s.u, st, true)) != cudaSuccess)
       return DFLASH_ECUDA;
     // g = silu(gate) * up
-    W8Args ag = base_args(w->gu[l], M, s, EPI_SWIGLU);
+    W8Args ag = base_args(w->gu[l], M, EPI_SWIGLU);
     ag.out_h = s.g;
     if ((e = w8_gemm(ag, s.u, st, true)) != cudaSuccess) return DFLASH_ECUDA;
     // x += W8(down) g
-    W8Args ad = base_args(w->down[l], M, s, EPI_RESID_F32);
+    W8Args ad = base_args(w->down[l], M, EPI_RESID_F32);
     ad.out_f32 = s.x;
     ad.ldo = c.H;
     if ((e = w8_gemm(ad, s.g, st, true)) != cudaSuccess) return DFLASH_ECUDA;
@@ -390,13 +349,14 @@ int32_t dflash_kv_commit(const dflash_weights* w, const dflash_kv* kv, const uin
   const size_t layer_kv = (size_t)b * c.nkv * kv->cap * c.d;
   cudaError_t e;
   // c = RMSNorm(W8(fc) h; gamma_hid)
-  W8Args af = base_args(w->fc, Mc, s, EPI_STORE_F32);
+  W8Args af = base_args(w->fc, Mc, EPI_STORE_F32);
   af.out_f32 = s.y;
   af.ldo = c.H;
   if ((e = w8_gemm(af, reinterpret_cast<const __half*>(hid), st, false)) != cudaSuccess) return DFLASH_ECUDA;
   if ((e = rmsnorm_f16(s.y, Mc, c.H, w->gamma_hid, c.eps, s.u, st, true)) != cudaSuccess) return DFLASH_ECUDA;
   for (int l = 0; l < c.L; ++l) {
-    W8Args a = base_args(w->qkv[l], Mc, s, EPI_KVCOMMIT);
+    W8Args a = base_args(w->qkv[l], Mc, EPI_KVCOMMIT);
+    fill_inv_freq(a, c.rope_theta, c.d);
     a.row0 = c.nq * c.d;
     a.nrows = 2 * c.nkv * c.d;
     a.kout = reinterpret_cast<__half*>(kv->k) + l * layer_kv;

@@ -9,12 +9,13 @@
 // B = 16, group 4), so every K/V byte is read once per kv head.  Long contexts
 // are split along the keys (flash-decoding; the pages' long-context verify
 // likewise uses a two-pass attention, dflash-mlx summary, "기술적 도전":
-// JIT SDPA 2-pass for N >= 1024): each split keeps an online softmax and
-// writes its normalised partial output and log-sum-exp; the last split CTA of
-// a (sequence, kv head) to finish (atomic ticket, no spinning) merges the
-// partials in split order.  Q.K^T and P.V run on m16n8k16 tensor-core MMAs
-// with fp32 accumulation; K/V tiles of 64 keys are double-buffered with
-// cp.async into XOR-swizzled shared memory.
+// JIT SDPA 2-pass for N >= 1024): the splits of one (sequence, kv head) form
+// a thread-block cluster; each keeps an online softmax, leaves its normalised
+// partial output and log-sum-exp in shared memory, and after a cluster
+// barrier every CTA merges one slice of query rows over all splits through
+// distributed shared memory, in split order.  Q.K^T and P.V run on m16n8k16
+// tensor-core MMAs with fp32 accumulation; K/V tiles of 64 keys are
+// double-buffered with cp.async into XOR-swizzled shared memory.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -22,18 +23,14 @@ namespace dfl {
 
 namespace {
 
-constexpr int kMaxSplits = 32;
-constexpr int kMinChunk = 128;
-constexpr int kKT = 64;  // keys per tile
+constexpr int kMaxSplits = 8;  // one portable cluster
+constexpr int kKT = 64;        // keys per tile
 
-__device__ __forceinline__ void split_range(int total, int sp, int& ns, int& k0, int& k1) {
-  ns = (total + kMinChunk - 1) / kMinChunk;
-  if (ns > kMaxSplits) ns = kMaxSplits;
-  if (ns < 1) ns = 1;
+// keys [k0, k1) of split sp out of ns equal, 64-aligned chunks of `total`
+__device__ __forceinline__ void split_range(int total, int sp, int ns, int& k0, int& k1) {
   int chunk = (total + ns - 1) / ns;
   chunk = (chunk + kKT - 1) / kKT * kKT;
-  ns = (total + chunk - 1) / chunk;
-  k0 = sp * chunk;
+  k0 = min(total, sp * chunk);
   k1 = min(total, k0 + chunk);
 }
 
@@ -43,6 +40,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   const int sp = blockIdx.x, g = blockIdx.y, j = blockIdx.z;
+  const int ns = gridDim.x;
   const int grp = a.nq / a.nkv;
   const int rows = a.B * grp;
   const int nw = blockDim.x >> 5;
@@ -50,7 +48,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + rows_pad * RB;        // [2][64][D]
   uint8_t* sV = sK + 2 * kKT * RB;         // [2][64][D]
-  int* flag = reinterpret_cast<int*>(sV + 2 * kKT * RB);
+  float* sLse = reinterpret_cast<float*>(sV + 2 * kKT * RB);  // [rows_pad]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   pdl_wait();
@@ -58,9 +56,8 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
   if (L < 0) L = 0;
   if (L > a.cap) L = a.cap;
   const int total = L + a.B;
-  int ns, k0, k1;
+  int k0, k1;
   split_range(total, sp, ns, k0, k1);
-  if (sp >= ns) return;
 
   // ---- Q tile: row rho = tok * grp + hh  ->  q[(j B + tok)][g grp + hh][:]
   for (int c = threadIdx.x; c < rows_pad * (D / 8); c += blockDim.x) {
@@ -213,90 +210,100 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
   }
   pdl_trigger();
 
-  // normalise this split's rows; log2-domain log-sum-exp
+  // normalise this split's rows; log2-domain log-sum-exp (-inf when empty)
   float inv[2], lse[2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     inv[r] = lrow[r] > 0.f ? 1.f / lrow[r] : 0.f;
-    lse[r] = mrow[r] + log2f(lrow[r]);
+    lse[r] = lrow[r] > 0.f ? mrow[r] + log2f(lrow[r]) : -INFINITY;
   }
-  const int grp_rows = rows;
   if (ns == 1) {
 #pragma unroll
     for (int i = 0; i < D / 8; ++i)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         int rho = warp * 16 + g8 + ((e >> 1) << 3);
-        if (rho >= grp_rows) continue;
+        if (rho >= rows) continue;
         int tok = rho / grp, hh = rho - tok * grp;
         int dim = i * 8 + 2 * t4 + (e & 1);
         a.out[((size_t)(j * a.B + tok) * a.nq + g * grp + hh) * D + dim] = __float2half_rn(o[i][e] * inv[e >> 1]);
       }
     return;
   }
-  const size_t base = ((size_t)(j * a.nkv + g) * kMaxSplits);
-  float* op = a.opart + (base + sp) * (size_t)rows_pad * D;
-  float* ml = a.mlpart + (base + sp) * (size_t)rows_pad;
+  // partial O [rows_pad][D] fp32 over the (now idle) Q/K/V buffers; an empty
+  // split may still have zero-fill copies in flight
+  cp_async_wait<0>();
+  __syncthreads();
+  float* sO = reinterpret_cast<float*>(sQ);
 #pragma unroll
   for (int i = 0; i < D / 8; ++i)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       int rho = warp * 16 + g8 + ((e >> 1) << 3);
       int dim = i * 8 + 2 * t4 + (e & 1);
-      op[(size_t)rho * D + dim] = o[i][e] * inv[e >> 1];
+      sO[rho * D + dim] = o[i][e] * inv[e >> 1];
     }
   if (t4 == 0) {
-    ml[warp * 16 + g8] = lse[0];
-    ml[warp * 16 + g8 + 8] = lse[1];
+    sLse[warp * 16 + g8] = lse[0];
+    sLse[warp * 16 + g8 + 8] = lse[1];
   }
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int old = atomicAdd(&a.tickets[j * a.nkv + g], 1);
-    *flag = (old == ns - 1);
-  }
-  __syncthreads();
-  if (!*flag) return;
-  __threadfence();
-  const float* op0 = a.opart + base * (size_t)rows_pad * D;
-  const float* ml0 = a.mlpart + base * (size_t)rows_pad;
-  for (int c = threadIdx.x; c < grp_rows * D; c += blockDim.x) {
-    int rho = c / D, dim = c - rho * D;
+  cluster_sync();
+  // merge rows [r0, r1) over the ns splits, in split order
+  const int r0 = (sp * rows) / ns, r1 = ((sp + 1) * rows) / ns;
+  const uint32_t obase = smem_u32(sO), lbase = smem_u32(sLse);
+  for (int it = threadIdx.x; it < (r1 - r0) * (D / 4); it += blockDim.x) {
+    const int rho = r0 + it / (D / 4), c4 = it % (D / 4);
+    float ls[kMaxSplits];
     float mmax = -INFINITY;
-    for (int s2 = 0; s2 < ns; ++s2) mmax = fmaxf(mmax, __ldcg(ml0 + (size_t)s2 * rows_pad + rho));
-    float num = 0.f, den = 0.f;
-    for (int s2 = 0; s2 < ns; ++s2) {
-      float w = exp2f(__ldcg(ml0 + (size_t)s2 * rows_pad + rho) - mmax);
-      num += w * __ldcg(op0 + ((size_t)s2 * rows_pad + rho) * D + dim);
-      den += w;
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxSplits; ++s2) {
+      ls[s2] = s2 < ns ? ld_dsmem_f32(dsmem_addr(lbase + rho * 4u, (uint32_t)s2)) : -INFINITY;
+      mmax = fmaxf(mmax, ls[s2]);
     }
+    float4 ov[kMaxSplits];
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxSplits; ++s2)
+      if (s2 < ns) ov[s2] = ld_dsmem_f4(dsmem_addr(obase + (uint32_t)(rho * D + 4 * c4) * 4u, (uint32_t)s2));
+    float den = 0.f;
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxSplits; ++s2)
+      if (s2 < ns) {
+        float w = exp2f(ls[s2] - mmax);
+        den += w;
+        num.x += w * ov[s2].x;
+        num.y += w * ov[s2].y;
+        num.z += w * ov[s2].z;
+        num.w += w * ov[s2].w;
+      }
+    const float id = 1.f / den;
     int tok = rho / grp, hh = rho - tok * grp;
-    a.out[((size_t)(j * a.B + tok) * a.nq + g * grp + hh) * D + dim] = __float2half_rn(num / den);
+    __half2* dst = reinterpret_cast<__half2*>(a.out + ((size_t)(j * a.B + tok) * a.nq + g * grp + hh) * D + 4 * c4);
+    dst[0] = __floats2half2_rn(num.x * id, num.y * id);
+    dst[1] = __floats2half2_rn(num.z * id, num.w * id);
   }
-  if (threadIdx.x == 0) a.tickets[j * a.nkv + g] = 0;
+  cluster_sync();  // peers are done reading this CTA's partial
 }
 
 }  // namespace
 
-size_t attn_ws_bytes(int b, int B, int nq, int nkv, int d) {
-  int rows = B * (nq / nkv);
-  int rows_pad = (rows + 15) / 16 * 16;
-  size_t n = (size_t)b * nkv * kMaxSplits;
-  return n * rows_pad * d * sizeof(float) + n * rows_pad * sizeof(float);
-}
-
 cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
   AttnArgs a = a0;
-  a.max_splits = kMaxSplits;
   const int rows = a.B * (a.nq / a.nkv);
   const int nw = (rows + 15) / 16;
   const int rows_pad = nw * 16;
-  const size_t smem = 128 + (size_t)rows_pad * a.d * 2 + 4 * kKT * a.d * 2 + 16;
-  dim3 grid(kMaxSplits, a.nkv, a.b);
+  int ns = (a.cap + a.B + 127) / 128;  // splits sized for the longest possible context
+  if (ns > kMaxSplits) ns = kMaxSplits;
+  if (ns < 1) ns = 1;
+  a.max_splits = ns;
+  size_t smem = 128 + (size_t)rows_pad * a.d * 2 + 4 * kKT * a.d * 2 + rows_pad * 4;
+  const size_t need_o = 128 + (size_t)rows_pad * a.d * 4 + rows_pad * 4;  // partial O over Q/K/V
+  if (need_o > smem) smem = need_o;
+  dim3 grid(ns, a.nkv, a.b);
   void* args[] = {&a};
   const void* fn = a.d == 128 ? (const void*)attn_kernel<128> : (const void*)attn_kernel<64>;
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  return launch_k(fn, grid, dim3(nw * 32), smem, st, pdl, args);
+  return launch_kc(fn, grid, dim3(nw * 32), smem, st, pdl, dim3(ns, 1, 1), args);
 }
 
 }  // namespace dfl

@@ -16,9 +16,11 @@
 //  * consumer warps turn biased int8 into fp16 exactly in registers and issue
 //    m16n8k16 MMAs with fp32 accumulation; the scale is applied after the
 //    K reduction;
-//  * split-K over CTAs with a deterministic reduction: every split writes its
-//    partial tile, the last CTA to arrive (atomic ticket, no spinning) sums
-//    the partials in split order and runs the epilogue;
+//  * split-K over the CTAs of a thread-block cluster: each split keeps its
+//    fp32 partial tile in shared memory, and after a cluster barrier every
+//    CTA sums one slice of activation rows over all splits through
+//    distributed shared memory, in split order (deterministic), then runs the
+//    epilogue for that slice; no partial ever touches global memory;
 //  * programmatic dependent launch: the weight copies of the first stages are
 //    issued before griddepcontrol.wait, overlapping the previous kernel's tail.
 #include "kernels.h"
@@ -38,6 +40,8 @@ struct Geo {
   static constexpr int ABYTES = 2 * MCH * 128;  // two [MCH][64] fp16 halves
   static constexpr int STAGE = kTileBytes + ABYTES;
   static constexpr int TSTRIDE = 132;  // epilogue tile row stride (floats)
+  static constexpr int TBYTES = (MCH * TSTRIDE * 4 + 1023) / 1024 * 1024;
+  static_assert(2 * TBYTES <= kStages * STAGE, "epilogue tiles must fit in the ring");
   static constexpr size_t SMEM = 1024 + kStages * (size_t)STAGE + 2 * kStages * 8 + 64;
 };
 
@@ -50,10 +54,10 @@ __device__ __forceinline__ int logical_row(int prow, int layout, int N) {
   return prow;
 }
 
-__device__ __forceinline__ void rope_pair(float& x1, float& x2, int pos, int p, int d, float theta) {
-  // angle = pos * theta^(-2p/d), formed and range-reduced in double, then
-  // evaluated with the single-precision sincosf.
-  double inv = exp2(-(2.0 * p / d) * log2((double)theta));
+__device__ __forceinline__ void rope_pair(float& x1, float& x2, int pos, double inv) {
+  // angle = pos * theta^(-2p/d) (inv = theta^(-2p/d) from the host, in
+  // double), formed and range-reduced in double, then evaluated with the
+  // single-precision sincosf.
   double ang = (double)pos * inv;
   const double two_pi = 6.283185307179586476925286766559;
   ang -= two_pi * rint(ang / two_pi);
@@ -64,15 +68,18 @@ __device__ __forceinline__ void rope_pair(float& x1, float& x2, int pos, int p, 
   x2 = b * cs + a * sn;
 }
 
+// Epilogue for the chunk's activation rows [tlo, thi); T holds the reduced,
+// unscaled fp32 tile as [row][TSTRIDE].
 template <int MT>
-__device__ void epilogue(const W8Args& a, const float* T, int nt, int z, int warp, int lane) {
+__device__ void epilogue(const W8Args& a, const float* T, int nt, int z, int tlo, int thi, int warp, int lane) {
   using G = Geo<MT>;
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
+  const int ntok = thi - tlo;
   const int prow0 = a.row0 + nt * kTile;  // first packed row of this tile
   if (a.epi == EPI_STORE_F32 || a.epi == EPI_RESID_F32) {
-    for (int i = tid; i < G::MCH * kTile; i += nthr) {
-      int tok = i >> 7, r = i & 127;
+    for (int i = tid; i < ntok * kTile; i += nthr) {
+      int tok = tlo + (i >> 7), r = i & 127;
       int m = z * G::MCH + tok;
       if (m >= a.M) continue;
       int n = logical_row(prow0 + r, a.layout, a.N);
@@ -84,8 +91,8 @@ __device__ void epilogue(const W8Args& a, const float* T, int nt, int z, int war
   }
   if (a.epi == EPI_SWIGLU) {
     const int F = a.N >> 1;
-    for (int i = tid; i < G::MCH * 64; i += nthr) {
-      int tok = i >> 6, r = i & 63;
+    for (int i = tid; i < ntok * 64; i += nthr) {
+      int tok = tlo + (i >> 6), r = i & 63;
       int m = z * G::MCH + tok;
       if (m >= a.M) continue;
       int j = nt * 64 + r;
@@ -99,7 +106,7 @@ __device__ void epilogue(const W8Args& a, const float* T, int nt, int z, int war
   // per-head epilogues: one warp per activation row, lane holds rows lane+32i
   const int qd = a.nq * a.d, kd = a.nkv * a.d;
   const int kind = prow0 < qd ? 0 : (prow0 < qd + kd ? 1 : 2);  // q, k, v
-  for (int tok = warp; tok < G::MCH; tok += kConsumerWarps + 1) {
+  for (int tok = tlo + warp; tok < thi; tok += kConsumerWarps + 1) {
     int m = z * G::MCH + tok;
     if (m >= a.M) continue;
     int seq = m / a.rows_per_seq, slot = m - seq * a.rows_per_seq;
@@ -128,8 +135,8 @@ __device__ void epilogue(const W8Args& a, const float* T, int nt, int z, int war
         float inv = rsqrtf(ss / 128.0f + a.eps);
 #pragma unroll
         for (int i = 0; i < 4; ++i) v[i] *= inv * gam[lane + 32 * i];
-        rope_pair(v[0], v[2], pos, lane, 128, a.theta);
-        rope_pair(v[1], v[3], pos, lane + 32, 128, a.theta);
+        rope_pair(v[0], v[2], pos, a.inv_freq[lane]);
+        rope_pair(v[1], v[3], pos, a.inv_freq[lane + 32]);
       } else {  // d == 64: rows 0..63 head A, 64..127 head B
         float sa = v[0] * v[0] + v[1] * v[1];
         float sb = v[2] * v[2] + v[3] * v[3];
@@ -143,8 +150,8 @@ __device__ void epilogue(const W8Args& a, const float* T, int nt, int z, int war
         v[1] *= ia * gam[lane + 32];
         v[2] *= ib * gam[lane];
         v[3] *= ib * gam[lane + 32];
-        rope_pair(v[0], v[1], pos, lane, 64, a.theta);
-        rope_pair(v[2], v[3], pos, lane, 64, a.theta);
+        rope_pair(v[0], v[1], pos, a.inv_freq[lane]);
+        rope_pair(v[2], v[3], pos, a.inv_freq[lane]);
       }
     }
     if (a.epi == EPI_QKV) {
@@ -178,10 +185,8 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * G::STAGE);
   uint64_t* empty = full + kStages;
-  int* flag = reinterpret_cast<int*>(empty + kStages);
 
   const int nt = blockIdx.x, sp = blockIdx.y, z = blockIdx.z;
-  const int ntiles = gridDim.x;
   const int KT = a.K / kTile;
   const int kt0 = (int)(((long long)sp * KT) / a.splits);
   const int kt1 = (int)(((long long)(sp + 1) * KT) / a.splits);
@@ -271,56 +276,56 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
   }
   __syncthreads();  // all stages consumed: the ring can be reused as scratch
 
-  float* T = reinterpret_cast<float*>(smem);  // [MCH][TSTRIDE]
+  // own partial tile P[tok][TSTRIDE] at the ring's start; the reduced slice
+  // goes to a second buffer so peers can keep reading P meanwhile
+  float* P = reinterpret_cast<float*>(smem);
+  float* T = reinterpret_cast<float*>(smem + G::TBYTES);
   const int g = lane >> 2, t = lane & 3;
-  const size_t part_tile = (size_t)G::MCH * kTile;
-  const int tix = z * ntiles + nt;
   if (warp < kConsumerWarps) {
-    if (a.splits == 1) {
 #pragma unroll
-      for (int mg = 0; mg < 2; ++mg)
+    for (int mg = 0; mg < 2; ++mg)
 #pragma unroll
-        for (int j = 0; j < MT; ++j)
+      for (int j = 0; j < MT; ++j)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            int r = warp * 32 + mg * 16 + g + ((e >> 1) << 3);
-            int tok = j * 8 + 2 * t + (e & 1);
-            T[tok * G::TSTRIDE + r] = acc[mg][j][e];
-          }
-    } else {
-      float* P = a.part + ((size_t)tix * a.splits + sp) * part_tile;
-#pragma unroll
-      for (int mg = 0; mg < 2; ++mg)
-#pragma unroll
-        for (int j = 0; j < MT; ++j)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            int r = warp * 32 + mg * 16 + g + ((e >> 1) << 3);
-            int tok = j * 8 + 2 * t + (e & 1);
-            P[tok * kTile + r] = acc[mg][j][e];
-          }
-    }
+        for (int e = 0; e < 4; ++e) {
+          int r = warp * 32 + mg * 16 + g + ((e >> 1) << 3);
+          int tok = j * 8 + 2 * t + (e & 1);
+          P[tok * G::TSTRIDE + r] = acc[mg][j][e];
+        }
   }
-  if (a.splits > 1) {
-    __threadfence();
+  if (a.splits == 1) {
     __syncthreads();
-    if (threadIdx.x == 0) {
-      int old = atomicAdd(&a.tickets[tix], 1);
-      *flag = (old == a.splits - 1);
-    }
-    __syncthreads();
-    if (!*flag) return;
-    __threadfence();
-    const float* P0 = a.part + (size_t)tix * a.splits * part_tile;
-    for (int i = threadIdx.x; i < G::MCH * kTile; i += blockDim.x) {
-      float s = 0.f;
-      for (int sp2 = 0; sp2 < a.splits; ++sp2) s += __ldcg(P0 + sp2 * part_tile + i);
-      T[(i >> 7) * G::TSTRIDE + (i & 127)] = s;
-    }
-    if (threadIdx.x == 0) a.tickets[tix] = 0;
+    epilogue<MT>(a, P, nt, z, 0, G::MCH, warp, lane);
+    return;
   }
-  __syncthreads();
-  epilogue<MT>(a, T, nt, z, warp, lane);
+  // ---- split-K reduction across the cluster through distributed smem ----
+  cluster_sync();
+  const int S = a.splits;
+  const int tlo = (sp * G::MCH) / S, thi = ((sp + 1) * G::MCH) / S;
+  const int items = (thi - tlo) * (kTile / 4);  // float4 items of this slice
+  const uint32_t pbase = smem_u32(P);
+  for (int it = threadIdx.x; it < items; it += blockDim.x) {
+    const int tok = tlo + it / (kTile / 4), c4 = it % (kTile / 4);
+    const uint32_t off = pbase + (uint32_t)(tok * G::TSTRIDE + 4 * c4) * 4u;
+    float4 v[8];
+    float4 accv = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < S; s0 += 8) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (s0 + q < S) v[q] = ld_dsmem_f4(dsmem_addr(off, (uint32_t)(s0 + q)));
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (s0 + q < S) {
+          accv.x += v[q].x;
+          accv.y += v[q].y;
+          accv.z += v[q].z;
+          accv.w += v[q].w;
+        }
+    }
+    *reinterpret_cast<float4*>(T + tok * G::TSTRIDE + 4 * c4) = accv;
+  }
+  cluster_sync();  // every peer has finished reading this CTA's partial
+  epilogue<MT>(a, T, nt, z, tlo, thi, warp, lane);
 }
 
 // ------------------------------------------------------------- packing ----
@@ -401,29 +406,18 @@ __global__ void pack_q_kernel(const void* w, int64_t N, int64_t K, int layout, c
 }  // namespace
 
 int w8_pick_splits(int units, int KT) {
+  // enough CTAs for two per SM, at most one cluster of 8 splits, and at
+  // least two 128-column k-tiles per split
   int target = 2 * kNumSMs;
   int s = (target + units - 1) / units;
   int smax = KT >= 4 ? KT / 2 : 1;
   if (s > smax) s = smax;
+  if (s > 8) s = 8;
   if (s < 1) s = 1;
   return s;
 }
 
 static int pick_mt(int M) { return M <= 16 ? 2 : 4; }
-
-size_t w8_partial_bytes(int M, int nrows, int K) {
-  int mt = pick_mt(M), mch = mt * 8;
-  int chunks = (M + mch - 1) / mch;
-  int units = chunks * (nrows / kTile);
-  int s = w8_pick_splits(units, K / kTile);
-  if (s == 1) return 0;
-  return (size_t)units * s * mch * kTile * sizeof(float);
-}
-
-size_t w8_ticket_count(int M, int nrows) {
-  int mt = pick_mt(M), mch = mt * 8;
-  return (size_t)((M + mch - 1) / mch) * (nrows / kTile);
-}
 
 cudaError_t w8_gemm(const W8Args& a0, const __half* x, cudaStream_t st, bool pdl) {
   W8Args a = a0;
@@ -438,22 +432,10 @@ cudaError_t w8_gemm(const W8Args& a0, const __half* x, cudaStream_t st, bool pdl
     return cudaErrorInvalidValue;
   void* args[] = {&map, &a};
   dim3 grid(ntiles, a.splits, chunks);
-  if (mt == 2) {
-    static bool attr = false;
-    if (!attr) {
-      cudaFuncSetAttribute((const void*)w8_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)Geo<2>::SMEM);
-      attr = true;
-    }
-    return launch_k((const void*)w8_gemm_kernel<2>, grid, dim3(kThreads), Geo<2>::SMEM, st, pdl, args);
-  }
-  static bool attr4 = false;
-  if (!attr4) {
-    cudaFuncSetAttribute((const void*)w8_gemm_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)Geo<4>::SMEM);
-    attr4 = true;
-  }
-  return launch_k((const void*)w8_gemm_kernel<4>, grid, dim3(kThreads), Geo<4>::SMEM, st, pdl, args);
+  const void* fn = mt == 2 ? (const void*)w8_gemm_kernel<2> : (const void*)w8_gemm_kernel<4>;
+  const size_t smem = mt == 2 ? Geo<2>::SMEM : Geo<4>::SMEM;
+  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  return launch_kc(fn, grid, dim3(kThreads), smem, st, pdl, dim3(1, a.splits, 1), args);
 }
 
 cudaError_t w8_pack(const void* w, int w_dtype, int64_t N, int64_t K, int layout, uint8_t* q_out, __half* s_out,

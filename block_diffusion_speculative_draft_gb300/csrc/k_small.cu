@@ -22,6 +22,32 @@ cudaError_t launch_k(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStr
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+cudaError_t launch_kc(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, dim3 cluster,
+                      void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster.x * cluster.y * cluster.z > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster.x;
+    attr[n].val.clusterDim.y = cluster.y;
+    attr[n].val.clusterDim.z = cluster.z;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -65,11 +91,51 @@ __device__ __forceinline__ float block_sum(float v, float* sh) {
   return s;
 }
 
+constexpr int kNormThreads = 256;
+constexpr int kNormVec = 8;  // float4 per thread: rows up to 8192 wide
+
+// Loads a fp32 row into registers (all loads issued before any use) and
+// returns its sum of squares over the block.
+__device__ __forceinline__ float load_row(const float* xr, int H, float4 (&v)[kNormVec], float* sh) {
+  const int n4 = H >> 2;
+  const float4* x4 = reinterpret_cast<const float4*>(xr);
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) {
+    int c = threadIdx.x + i * kNormThreads;
+    v[i] = c < n4 ? x4[c] : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+  return block_sum(ss, sh);
+}
+
+__device__ __forceinline__ void store_f16_row(__half* ur, int H, const float4 (&v)[kNormVec], float inv,
+                                              const float* gamma) {
+  const int n4 = H >> 2;
+  const float4* g4 = reinterpret_cast<const float4*>(gamma);
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) {
+    int c = threadIdx.x + i * kNormThreads;
+    if (c < n4) {
+      float4 g = g4[c];
+      __half2 a = __floats2half2_rn(v[i].x * inv * g.x, v[i].y * inv * g.y);
+      __half2 b = __floats2half2_rn(v[i].z * inv * g.z, v[i].w * inv * g.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&a);
+      pk.y = *reinterpret_cast<uint32_t*>(&b);
+      reinterpret_cast<uint2*>(ur)[c] = pk;
+    }
+  }
+}
+
 // x[m] = E[tok(m)] (fp32), u[m] = RMSNorm(x[m]; gamma) (fp16).
 // Slot 0 of each sequence is its last accepted token, slots 1..B-1 the mask
 // token (mlx-dspark v0.0.3, "Highlights"; mirror-sd "How It Works").
-__global__ void embed_rmsnorm_kernel(const __nv_bfloat16* E, const int* last_tok, int mask_id, int V, int B, int H,
-                                     const float* gamma, float eps, float* x, __half* u, int* status) {
+__global__ void __launch_bounds__(kNormThreads) embed_rmsnorm_kernel(const __nv_bfloat16* E, const int* last_tok,
+                                                                    int mask_id, int V, int B, int H,
+                                                                    const float* gamma, float eps, float* x,
+                                                                    __half* u, int* status) {
   __shared__ float sh[32];
   pdl_wait();
   const int m = blockIdx.x;
@@ -77,54 +143,69 @@ __global__ void embed_rmsnorm_kernel(const __nv_bfloat16* E, const int* last_tok
   int tok = slot == 0 ? last_tok[j] : mask_id;
   bool ok = tok >= 0 && tok < V;
   if (!ok && threadIdx.x == 0) atomicOr(status, kDevBadToken);
-  const __nv_bfloat16* e = E + (size_t)(ok ? tok : 0) * H;
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) {
-    float v = ok ? __bfloat162float(e[i]) : 0.f;
-    x[(size_t)m * H + i] = v;
-    ss += v * v;
+  const uint2* e4 = reinterpret_cast<const uint2*>(E + (size_t)(ok ? tok : 0) * H);  // 4 bf16 per uint2
+  const int n4 = H >> 2;
+  float4 v[kNormVec];
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) {
+    int c = threadIdx.x + i * kNormThreads;
+    uint2 w = (ok && c < n4) ? e4[c] : make_uint2(0u, 0u);
+    v[i].x = __uint_as_float(w.x << 16);
+    v[i].y = __uint_as_float(w.x & 0xFFFF0000u);
+    v[i].z = __uint_as_float(w.y << 16);
+    v[i].w = __uint_as_float(w.y & 0xFFFF0000u);
   }
-  float tot = block_sum(ss, sh);
-  float inv = rsqrtf(tot / H + eps);
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+  float inv = rsqrtf(block_sum(ss, sh) / H + eps);
   pdl_trigger();
-  for (int i = threadIdx.x; i < H; i += blockDim.x)
-    u[(size_t)m * H + i] = __float2half_rn(x[(size_t)m * H + i] * inv * gamma[i]);
+  float4* xr = reinterpret_cast<float4*>(x + (size_t)m * H);
+#pragma unroll
+  for (int i = 0; i < kNormVec; ++i) {
+    int c = threadIdx.x + i * kNormThreads;
+    if (c < n4) xr[c] = v[i];
+  }
+  store_f16_row(u + (size_t)m * H, H, v, inv, gamma);
 }
 
-__global__ void rmsnorm_f16_kernel(const float* x, int H, const float* gamma, float eps, __half* u) {
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_f16_kernel(const float* x, int H, const float* gamma,
+                                                                  float eps, __half* u) {
   __shared__ float sh[32];
   pdl_wait();
   const int m = blockIdx.x;
-  const float* xr = x + (size_t)m * H;
-  float ss = 0.f;
-  for (int i = threadIdx.x; i < H; i += blockDim.x) {
-    float v = xr[i];
-    ss += v * v;
-  }
-  float inv = rsqrtf(block_sum(ss, sh) / H + eps);
+  float4 v[kNormVec];
+  float inv = rsqrtf(load_row(x + (size_t)m * H, H, v, sh) / H + eps);
   pdl_trigger();
-  for (int i = threadIdx.x; i < H; i += blockDim.x) u[(size_t)m * H + i] = __float2half_rn(xr[i] * inv * gamma[i]);
+  store_f16_row(u + (size_t)m * H, H, v, inv, gamma);
 }
 
 // rows 1..B-1 of every sequence: h = RMSNorm(x; gamma_final) as bf16
-__global__ void final_norm_kernel(const float* x, int B, int H, const float* gamma, float eps, __nv_bfloat16* h,
-                                  float* hidden_out) {
+__global__ void __launch_bounds__(kNormThreads) final_norm_kernel(const float* x, int B, int H, const float* gamma,
+                                                                 float eps, __nv_bfloat16* h, float* hidden_out) {
   __shared__ float sh[32];
   pdl_wait();
   const int o = blockIdx.x;  // output row j (B-1) + i
   const int j = o / (B - 1), i = o - j * (B - 1);
-  const float* xr = x + ((size_t)j * B + i + 1) * H;
-  float ss = 0.f;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    float v = xr[c];
-    ss += v * v;
-  }
-  float inv = rsqrtf(block_sum(ss, sh) / H + eps);
+  float4 v[kNormVec];
+  float inv = rsqrtf(load_row(x + ((size_t)j * B + i + 1) * H, H, v, sh) / H + eps);
   pdl_trigger();
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    float v = xr[c] * inv * gamma[c];
-    h[(size_t)o * H + c] = __float2bfloat16_rn(v);
-    if (hidden_out) hidden_out[(size_t)o * H + c] = v;
+  const int n4 = H >> 2;
+  const float4* g4 = reinterpret_cast<const float4*>(gamma);
+#pragma unroll
+  for (int q = 0; q < kNormVec; ++q) {
+    int c = threadIdx.x + q * kNormThreads;
+    if (c < n4) {
+      float4 g = g4[c];
+      float4 y = make_float4(v[q].x * inv * g.x, v[q].y * inv * g.y, v[q].z * inv * g.z, v[q].w * inv * g.w);
+      __nv_bfloat162 a = __floats2bfloat162_rn(y.x, y.y);
+      __nv_bfloat162 b = __floats2bfloat162_rn(y.z, y.w);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&a);
+      pk.y = *reinterpret_cast<uint32_t*>(&b);
+      reinterpret_cast<uint2*>(h + (size_t)o * H)[c] = pk;
+      if (hidden_out) reinterpret_cast<float4*>(hidden_out + (size_t)o * H)[c] = y;
+    }
   }
 }
 
@@ -180,13 +261,25 @@ __global__ void __launch_bounds__(256) verify_kernel(const VerifyArgs a) {
   unsigned long long best = 0ull;
   if ((a.V & 3) == 0) {
     const float4* l4 = reinterpret_cast<const float4*>(lr);
-    for (int64_t i = c0 / 4 + threadIdx.x; i < c1 / 4; i += blockDim.x) {
-      float4 v = __ldcs(l4 + i);
-      uint32_t b0 = (uint32_t)(4 * i);
-      best = umax64(best, argmax_key(v.x, b0));
-      best = umax64(best, argmax_key(v.y, b0 + 1));
-      best = umax64(best, argmax_key(v.z, b0 + 2));
-      best = umax64(best, argmax_key(v.w, b0 + 3));
+    const int64_t e4 = c1 / 4;
+    for (int64_t i0 = c0 / 4 + threadIdx.x; i0 < e4; i0 += 4 * (int64_t)blockDim.x) {
+      float4 v[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        int64_t i = i0 + q * (int64_t)blockDim.x;
+        v[q] = i < e4 ? __ldcs(l4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        int64_t i = i0 + q * (int64_t)blockDim.x;
+        if (i < e4) {
+          uint32_t b0 = (uint32_t)(4 * i);
+          best = umax64(best, argmax_key(v[q].x, b0));
+          best = umax64(best, argmax_key(v[q].y, b0 + 1));
+          best = umax64(best, argmax_key(v[q].z, b0 + 2));
+          best = umax64(best, argmax_key(v[q].w, b0 + 3));
+        }
+      }
     }
   } else {
     for (int64_t i = c0 + threadIdx.x; i < c1; i += blockDim.x) best = umax64(best, argmax_key(lr[i], (uint32_t)i));
@@ -251,19 +344,19 @@ cudaError_t embed_rmsnorm(const __nv_bfloat16* E, const int* last_tok, int mask_
                           const float* gamma, float eps, float* x, __half* u, cudaStream_t st, bool pdl,
                           int* status) {
   void* args[] = {&E, &last_tok, &mask_id, &V, &B, &H, &gamma, &eps, &x, &u, &status};
-  return launch_k((const void*)embed_rmsnorm_kernel, dim3(b * B), dim3(256), 0, st, pdl, args);
+  return launch_k((const void*)embed_rmsnorm_kernel, dim3(b * B), dim3(kNormThreads), 0, st, pdl, args);
 }
 
 cudaError_t rmsnorm_f16(const float* x, int M, int H, const float* gamma, float eps, __half* u, cudaStream_t st,
                         bool pdl) {
   void* args[] = {&x, &H, &gamma, &eps, &u};
-  return launch_k((const void*)rmsnorm_f16_kernel, dim3(M), dim3(256), 0, st, pdl, args);
+  return launch_k((const void*)rmsnorm_f16_kernel, dim3(M), dim3(kNormThreads), 0, st, pdl, args);
 }
 
 cudaError_t final_norm(const float* x, int b, int B, int H, const float* gamma, float eps, __nv_bfloat16* h,
                        float* hidden_out, cudaStream_t st, bool pdl) {
   void* args[] = {&x, &B, &H, &gamma, &eps, &h, &hidden_out};
-  return launch_k((const void*)final_norm_kernel, dim3(b * (B - 1)), dim3(256), 0, st, pdl, args);
+  return launch_k((const void*)final_norm_kernel, dim3(b * (B - 1)), dim3(kNormThreads), 0, st, pdl, args);
 }
 
 cudaError_t commit_len_update(int* len, const int* nacc, int b, int rows_per_seq, int cap, cudaStream_t st,

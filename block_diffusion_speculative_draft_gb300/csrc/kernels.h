@@ -28,9 +28,7 @@ struct W8Args {
   int row0;   // first packed row used (multiple of 128)
   int nrows;  // packed rows used (multiple of 128)
   int M;      // activation rows
-  int splits;
-  float* part;   // split-K partials
-  int* tickets;  // per (chunk, tile) arrival counters, zero between calls
+  int splits;  // k-splits = cluster size along y
   int epi;
   float* out_f32;
   int ldo;
@@ -46,19 +44,21 @@ struct W8Args {
   int rows_per_seq;  // activation rows per sequence
   int b, cap;
   int* status;
+  double inv_freq[64];  // RoPE theta^(-2p/d), p < d/2 (per-head epilogues)
 };
 
 // Tensor-map encoder from the driver (resolved once through the runtime).
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);
 
-// Launch helper: PDL attribute on when `pdl`.
+// Launch helpers: PDL attribute on when `pdl`; launch_kc also groups blocks
+// into thread-block clusters of shape `cluster` (no cluster when 1x1x1).
 cudaError_t launch_k(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, void** args);
+cudaError_t launch_kc(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, dim3 cluster,
+                      void** args);
 
 // --- W8A16 GEMM (k_gemm_w8.cu) ---
 int w8_pick_splits(int units, int KT);
-size_t w8_partial_bytes(int M, int nrows, int K);
-size_t w8_ticket_count(int M, int nrows);
 cudaError_t w8_gemm(const W8Args& a, const __half* x, cudaStream_t st, bool pdl);
 cudaError_t w8_pack(const void* w, int w_dtype, int64_t N, int64_t K, int layout, uint8_t* q_out, __half* s_out,
                     cudaStream_t st);
@@ -77,14 +77,10 @@ struct AttnArgs {
   const __half* vc;
   const int* len;
   __half* out;  // [M][nq][d]
-  float* opart;
-  float* mlpart;
-  int* tickets;  // [b][nkv]
   int b, B, nq, nkv, d, cap;
   int max_splits;
   int* status;
 };
-size_t attn_ws_bytes(int b, int B, int nq, int nkv, int d);
 cudaError_t attention(const AttnArgs& a, cudaStream_t st, bool pdl);
 
 // --- small kernels (k_small.cu) ---
