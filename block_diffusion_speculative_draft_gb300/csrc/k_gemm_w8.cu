@@ -42,7 +42,9 @@ struct Geo {
   static constexpr int TSTRIDE = 132;  // epilogue tile row stride (floats)
   static constexpr int TBYTES = (MCH * TSTRIDE * 4 + 1023) / 1024 * 1024;
   static_assert(2 * TBYTES <= kStages * STAGE, "epilogue tiles must fit in the ring");
-  static constexpr size_t SMEM = 1024 + kStages * (size_t)STAGE + 2 * kStages * 8 + 64;
+  // side data after the barriers: row scales, gamma, per-row positions
+  static constexpr int SIDE = 128 * 4 + 128 * 4 + MCH * 4;
+  static constexpr size_t SMEM = 1024 + kStages * (size_t)STAGE + 2 * kStages * 8 + 64 + SIDE;
 };
 
 // packed row -> logical row
@@ -60,7 +62,8 @@ __device__ __forceinline__ void rope_pair(float& x1, float& x2, int pos, double 
   // single-precision sincosf.
   double ang = (double)pos * inv;
   const double two_pi = 6.283185307179586476925286766559;
-  ang -= two_pi * rint(ang / two_pi);
+  const double inv_two_pi = 0.15915494309189533576888376337251;
+  ang -= two_pi * rint(ang * inv_two_pi);
   float sn, cs;
   sincosf((float)ang, &sn, &cs);
   float a = x1, b = x2;
@@ -68,38 +71,72 @@ __device__ __forceinline__ void rope_pair(float& x1, float& x2, int pos, double 
   x2 = b * cs + a * sn;
 }
 
-// Epilogue for the chunk's activation rows [tlo, thi); T holds the reduced,
-// unscaled fp32 tile as [row][TSTRIDE].
+// Epilogue for the chunk's activation rows [tlo, thi).  T holds the reduced,
+// unscaled fp32 tile as [row][TSTRIDE]; sc[r] is packed row r's scale, gam
+// the per-head gamma and pos[t] the position of row t (-1: not written), all
+// staged in shared memory before the main loop so that no global load sits on
+// the epilogue's critical path except the residual read, issued in batches.
 template <int MT>
-__device__ void epilogue(const W8Args& a, const float* T, int nt, int z, int tlo, int thi, int warp, int lane) {
+__device__ void epilogue(const W8Args& a, const float* T, const float* sc, const float* gam, const int* pos,
+                         int nt, int z, int tlo, int thi, int warp, int lane) {
   using G = Geo<MT>;
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
   const int ntok = thi - tlo;
   const int prow0 = a.row0 + nt * kTile;  // first packed row of this tile
   if (a.epi == EPI_STORE_F32 || a.epi == EPI_RESID_F32) {
-    for (int i = tid; i < ntok * kTile; i += nthr) {
-      int tok = tlo + (i >> 7), r = i & 127;
-      int m = z * G::MCH + tok;
-      if (m >= a.M) continue;
-      int n = logical_row(prow0 + r, a.layout, a.N);
-      float v = T[tok * G::TSTRIDE + r] * __half2float(a.s[n]);
-      float* o = a.out_f32 + (size_t)m * a.ldo + (n - a.row0);
-      if (a.epi == EPI_RESID_F32) *o += v; else *o = v;
+    const int items = ntok * (kTile / 4);  // groups of 4 consecutive rows
+    for (int base = tid; base < items; base += 4 * nthr) {
+      float4 xo[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int it = base + u * nthr;
+        xo[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (it < items && a.epi == EPI_RESID_F32) {
+          const int tok = tlo + it / (kTile / 4), r = 4 * (it % (kTile / 4));
+          const int m = z * G::MCH + tok;
+          if (m < a.M) {
+            const int n = logical_row(prow0 + r, a.layout, a.N);
+            xo[u] = *reinterpret_cast<const float4*>(a.out_f32 + (size_t)m * a.ldo + (n - a.row0));
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int it = base + u * nthr;
+        if (it >= items) continue;
+        const int tok = tlo + it / (kTile / 4), r = 4 * (it % (kTile / 4));
+        const int m = z * G::MCH + tok;
+        if (m >= a.M) continue;
+        const int n = logical_row(prow0 + r, a.layout, a.N);
+        const float* t = T + tok * G::TSTRIDE + r;
+        float4 v = make_float4(t[0] * sc[r] + xo[u].x, t[1] * sc[r + 1] + xo[u].y, t[2] * sc[r + 2] + xo[u].z,
+                               t[3] * sc[r + 3] + xo[u].w);
+        *reinterpret_cast<float4*>(a.out_f32 + (size_t)m * a.ldo + (n - a.row0)) = v;
+      }
     }
     return;
   }
   if (a.epi == EPI_SWIGLU) {
     const int F = a.N >> 1;
-    for (int i = tid; i < ntok * 64; i += nthr) {
-      int tok = tlo + (i >> 6), r = i & 63;
-      int m = z * G::MCH + tok;
+    const int items = ntok * 16;  // groups of 4 output columns
+    for (int it = tid; it < items; it += nthr) {
+      const int tok = tlo + it / 16, r = 4 * (it % 16);
+      const int m = z * G::MCH + tok;
       if (m >= a.M) continue;
-      int j = nt * 64 + r;
-      float gate = T[tok * G::TSTRIDE + r] * __half2float(a.s[j]);
-      float up = T[tok * G::TSTRIDE + r + 64] * __half2float(a.s[F + j]);
-      float g = gate / (1.0f + expf(-gate)) * up;
-      a.out_h[(size_t)m * F + j] = __float2half_rn(g);
+      const float* t = T + tok * G::TSTRIDE;
+      float g[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float gate = t[r + e] * sc[r + e];
+        float up = t[r + e + 64] * sc[r + e + 64];
+        g[e] = gate / (1.0f + expf(-gate)) * up;
+      }
+      __half2 h0 = __floats2half2_rn(g[0], g[1]), h1 = __floats2half2_rn(g[2], g[3]);
+      uint2 pk;
+      pk.x = *reinterpret_cast<uint32_t*>(&h0);
+      pk.y = *reinterpret_cast<uint32_t*>(&h1);
+      *reinterpret_cast<uint2*>(a.out_h + (size_t)m * F + nt * 64 + r) = pk;
     }
     return;
   }
@@ -107,27 +144,17 @@ __device__ void epilogue(const W8Args& a, const float* T, int nt, int z, int tlo
   const int qd = a.nq * a.d, kd = a.nkv * a.d;
   const int kind = prow0 < qd ? 0 : (prow0 < qd + kd ? 1 : 2);  // q, k, v
   for (int tok = tlo + warp; tok < thi; tok += kConsumerWarps + 1) {
-    int m = z * G::MCH + tok;
-    if (m >= a.M) continue;
-    int seq = m / a.rows_per_seq, slot = m - seq * a.rows_per_seq;
-    int L0 = a.len[seq];
-    int ccount = 0;
-    if (a.epi == EPI_KVCOMMIT) {
-      int nn = a.nacc[seq];
-      ccount = min(nn + 1, a.rows_per_seq);
-      if (nn < -1 || nn > a.rows_per_seq || L0 < 0 || L0 + max(ccount, 0) > a.cap || slot >= ccount) continue;
-    } else if (L0 < 0) {
-      L0 = 0;
-    }
-    const int pos = L0 + slot;
+    const int m = z * G::MCH + tok;
+    const int p = pos[tok];
+    if (m >= a.M || p < 0) continue;
+    const int seq = m / a.rows_per_seq;
     float v[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       int r = lane + 32 * i;
-      v[i] = T[tok * G::TSTRIDE + r] * __half2float(a.s[prow0 + r]);
+      v[i] = T[tok * G::TSTRIDE + r] * sc[r];
     }
     if (kind != 2) {
-      const float* gam = kind == 0 ? a.gq : a.gk;
       if (a.d == 128) {
         float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
 #pragma unroll
@@ -135,8 +162,8 @@ __device__ void epilogue(const W8Args& a, const float* T, int nt, int z, int tlo
         float inv = rsqrtf(ss / 128.0f + a.eps);
 #pragma unroll
         for (int i = 0; i < 4; ++i) v[i] *= inv * gam[lane + 32 * i];
-        rope_pair(v[0], v[2], pos, a.inv_freq[lane]);
-        rope_pair(v[1], v[3], pos, a.inv_freq[lane + 32]);
+        rope_pair(v[0], v[2], p, a.inv_freq[lane]);
+        rope_pair(v[1], v[3], p, a.inv_freq[lane + 32]);
       } else {  // d == 64: rows 0..63 head A, 64..127 head B
         float sa = v[0] * v[0] + v[1] * v[1];
         float sb = v[2] * v[2] + v[3] * v[3];
@@ -150,8 +177,8 @@ __device__ void epilogue(const W8Args& a, const float* T, int nt, int z, int tlo
         v[1] *= ia * gam[lane + 32];
         v[2] *= ib * gam[lane];
         v[3] *= ib * gam[lane + 32];
-        rope_pair(v[0], v[1], pos, a.inv_freq[lane]);
-        rope_pair(v[2], v[3], pos, a.inv_freq[lane]);
+        rope_pair(v[0], v[1], p, a.inv_freq[lane]);
+        rope_pair(v[2], v[3], p, a.inv_freq[lane]);
       }
     }
     if (a.epi == EPI_QKV) {
@@ -170,7 +197,7 @@ __device__ void epilogue(const W8Args& a, const float* T, int nt, int z, int tlo
         int isv = row >= kd;
         int rr = isv ? row - kd : row;
         int h = rr / a.d, e = rr - h * a.d;
-        size_t off = (((size_t)seq * a.nkv + h) * a.cap + pos) * a.d + e;
+        size_t off = (((size_t)seq * a.nkv + h) * a.cap + p) * a.d + e;
         (isv ? a.vout : a.kout)[off] = __float2half_rn(v[i]);
       }
     }
@@ -185,6 +212,9 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * G::STAGE);
   uint64_t* empty = full + kStages;
+  float* s_sc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(empty + kStages) + 64);  // [128]
+  float* s_gam = s_sc + 128;                                                                 // [128]
+  int* s_pos = reinterpret_cast<int*>(s_gam + 128);                                          // [MCH]
 
   const int nt = blockIdx.x, sp = blockIdx.y, z = blockIdx.z;
   const int KT = a.K / kTile;
@@ -240,7 +270,35 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
     pdl_trigger();
   } else {
     // ---------------- consumers ----------------
+    {  // weights-side data first (independent of the preceding kernel)
+      const int r = threadIdx.x;  // 0..127
+      const int prow = a.row0 + nt * kTile + r;
+      s_sc[r] = __half2float(a.s[logical_row(prow, a.layout, a.N)]);
+      if (a.epi == EPI_QKV || a.epi == EPI_KVCOMMIT) {
+        const int qd = a.nq * a.d;
+        const float* gsrc = (a.row0 + nt * kTile) < qd ? a.gq : a.gk;
+        s_gam[r] = (gsrc && r < a.d) ? gsrc[r] : 1.f;
+      }
+    }
     pdl_wait();
+    if ((a.epi == EPI_QKV || a.epi == EPI_KVCOMMIT) && threadIdx.x < G::MCH) {
+      // position of each activation row of this chunk, -1 when not written
+      const int t = threadIdx.x, m = z * G::MCH + t;
+      int p = -1;
+      if (m < a.M) {
+        const int seq = m / a.rows_per_seq, slot = m - seq * a.rows_per_seq;
+        int L0 = a.len[seq];
+        if (a.epi == EPI_KVCOMMIT) {
+          const int nn = a.nacc[seq];
+          const int cnt = min(nn + 1, a.rows_per_seq);
+          const bool ok = nn >= -1 && nn <= a.rows_per_seq && L0 >= 0 && L0 + max(cnt, 0) <= a.cap;
+          p = (ok && slot < cnt) ? L0 + slot : -1;
+        } else {
+          p = (L0 < 0 ? 0 : L0) + slot;
+        }
+      }
+      s_pos[t] = p;
+    }
     const int g_tok_lo = (lane & 7) + ((lane >> 4) << 3);
     const int ch_hi = (lane >> 3) & 1;
     for (int i = 0; i < nk; ++i) {
@@ -295,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
   }
   if (a.splits == 1) {
     __syncthreads();
-    epilogue<MT>(a, P, nt, z, 0, G::MCH, warp, lane);
+    epilogue<MT>(a, P, s_sc, s_gam, s_pos, nt, z, 0, G::MCH, warp, lane);
     return;
   }
   // ---- split-K reduction across the cluster through distributed smem ----
@@ -325,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
     *reinterpret_cast<float4*>(T + tok * G::TSTRIDE + 4 * c4) = accv;
   }
   cluster_sync();  // every peer has finished reading this CTA's partial
-  epilogue<MT>(a, T, nt, z, tlo, thi, warp, lane);
+  epilogue<MT>(a, T, s_sc, s_gam, s_pos, nt, z, tlo, thi, warp, lane);
 }
 
 // ------------------------------------------------------------- packing ----
@@ -408,8 +466,8 @@ __global__ void pack_q_kernel(const void* w, int64_t N, int64_t K, int layout, c
 int w8_pick_splits(int units, int KT) {
   // enough CTAs for two per SM, at most one cluster of 8 splits, and at
   // least two 128-column k-tiles per split
-  int target = 2 * kNumSMs;
-  int s = (target + units - 1) / units;
+  int target = 2 * kNumSMs;  // one wave at two CTAs per SM
+  int s = target / units;
   int smax = KT >= 4 ? KT / 2 : 1;
   if (s > smax) s = smax;
   if (s > 8) s = 8;

@@ -299,11 +299,13 @@ __global__ void __launch_bounds__(256) verify_kernel(const VerifyArgs a) {
   pdl_trigger();
   if (!flag) return;
   __threadfence();
-  for (int r = threadIdx.x; r < a.R; r += blockDim.x) {
-    unsigned long long k = 0ull;
+  // merge the P slices of every row: one warp per row, lanes over slices
+  for (int r = threadIdx.x >> 5; r < a.R; r += blockDim.x >> 5) {
     const unsigned long long* pr = a.part + ((size_t)j * a.R + r) * a.P;
-    for (int q = 0; q < a.P; ++q) k = umax64(k, __ldcg(pr + q));
-    amax[r] = (int)key_index(k);
+    unsigned long long k = 0ull;
+    for (int q = (threadIdx.x & 31); q < a.P; q += 32) k = umax64(k, __ldcg(pr + q));
+    k = warp_max64(k);
+    if ((threadIdx.x & 31) == 0) amax[r] = (int)key_index(k);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
