@@ -27,7 +27,7 @@ EXPORTS = [
     "dflash_version", "dflash_status_string", "dflash_workspace_size", "dflash_pack_w8a16",
     "dflash_w8a16_linear_workspace_size", "dflash_w8a16_linear", "dflash_draft_block",
     "dflash_lmhead_workspace_size", "dflash_lmhead_argmax", "dflash_verify_workspace_size",
-    "dflash_verify_accept", "dflash_kv_commit", "dflash_get_status",
+    "dflash_verify_accept", "dflash_verify_accept_noalloc", "dflash_kv_commit", "dflash_get_status",
 ]
 
 
@@ -88,6 +88,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dflash_lmhead_argmax": ([P, P, I64, I64, I64, P, P, P, P, SZ, P], I32),
         "dflash_verify_workspace_size": ([I32, I32, I64, PSZ], I32),
         "dflash_verify_accept": ([P, P, I32, I32, I32, I64, P, P, P, P, P, SZ, P], I32),
+        "dflash_verify_accept_noalloc": ([P, P, I32, I32, I32, I64, P, P, P, P, P], I32),
         "dflash_kv_commit": ([ctypes.POINTER(Weights), ctypes.POINTER(KV), P, I32, P, P, SZ, P], I32),
         "dflash_get_status": ([ctypes.POINTER(ctypes.c_int32), I32], I32),
     }
@@ -201,6 +202,17 @@ def dflash_verify_accept(logits, draft, n_out, corr_out, emitted=None, next_tok=
     _check("dflash_verify_accept", load_library().dflash_verify_accept(
         logits.data_ptr(), draft.data_ptr(), b, R, D, V, n_out.data_ptr(), corr_out.data_ptr(), _ptr(emitted),
         _ptr(next_tok), ws.data_ptr(), ws.numel(), _stream(stream)))
+
+
+def dflash_verify_accept_noalloc(logits, draft, n_out, corr_out, emitted=None, next_tok=None, stream=None):
+    """Same result as dflash_verify_accept without a workspace: for callers
+    that cannot allocate device memory, the library's own fixed device scratch
+    is used (one shared array per GPU; serialise overlapping calls)."""
+    b, R, V = logits.shape
+    D = draft.shape[1]
+    _check("dflash_verify_accept_noalloc", load_library().dflash_verify_accept_noalloc(
+        logits.data_ptr(), draft.data_ptr(), b, R, D, V, n_out.data_ptr(), corr_out.data_ptr(), _ptr(emitted),
+        _ptr(next_tok), _stream(stream)))
 
 
 def dflash_draft_block(model: "DeviceDrafter", kv: "KVCache", last_tok, draft_out, ws, hidden=None, logits=None,

@@ -330,6 +330,19 @@ int32_t dflash_verify_accept(const float* logits, const int32_t* draft, int32_t 
                                static_cast<cudaStream_t>(stream), false));
 }
 
+int32_t dflash_verify_accept_noalloc(const float* logits, const int32_t* draft, int32_t b, int32_t R, int32_t D,
+                                     int64_t V, int32_t* n_out, int32_t* corr_out, int32_t* emitted_out,
+                                     int32_t* next_tok_out, void* stream) {
+  if (!logits || !draft || !n_out || !corr_out) return DFLASH_EINVAL;
+  if (b < 1 || R < 1 || R > 64 || D < 1 || D > R || V < 1 || V > ((int64_t)1 << 31) - 1) return DFLASH_EINVAL;
+  if ((int64_t)b * R > 65535) return DFLASH_EUNSUPPORTED;
+  if ((V & 3) == 0 && !aligned16(logits)) return DFLASH_EINVAL;
+  const size_t need = verify_noalloc_need(b, R, V);
+  if (need == (size_t)-1 || need > kNoAllocScratchBytes) return DFLASH_EWORKSPACE;
+  return map_err(verify_accept_noalloc(logits, draft, b, R, D, V, n_out, corr_out, emitted_out, next_tok_out,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
 int32_t dflash_kv_commit(const dflash_weights* w, const dflash_kv* kv, const uint16_t* hid, int32_t rows_per_seq,
                          const int32_t* n, void* ws, size_t ws_bytes, void* stream) {
   if (int r = check_weights(w)) return r;

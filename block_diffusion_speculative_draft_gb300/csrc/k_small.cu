@@ -2,6 +2,8 @@
 // RMSNorm, RMSNorm, final norm, commit-length update and the greedy
 // verify-accept; plus the launch and tensor-map helpers shared by all
 // kernels.
+#include <mutex>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -392,6 +394,67 @@ cudaError_t verify_accept(const float* logits, const int* draft, int b, int R, i
   a.tickets = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ws) + (size_t)b * R * a.P * 8);
   void* args[] = {&a};
   return launch_k((const void*)verify_kernel, dim3(a.P, b * R), dim3(256), 0, st, pdl, args);
+}
+
+// ------------------------------------------- allocation-free verify ----
+// Scratch for callers that cannot allocate device memory: a fixed array in
+// this library's device image, present on every GPU that loads the library
+// until the process exits.  Layout: per-sequence tickets at offset 0, the
+// per-slice argmax keys from offset kNoAllocTicketBytes.
+constexpr size_t kNoAllocTicketBytes = 4096;
+static __device__ __align__(256) unsigned char g_verify_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {nullptr};
+}  // namespace
+
+size_t verify_noalloc_need(int b, int R, int64_t V) {
+  int P = verify_parts(b, R, V);
+  if ((size_t)b * sizeof(int) > kNoAllocTicketBytes) return (size_t)-1;
+  return kNoAllocTicketBytes + (size_t)b * R * P * sizeof(unsigned long long);
+}
+
+cudaError_t verify_accept_noalloc(const float* logits, const int* draft, int b, int R, int D, int64_t V, int* n_out,
+                                  int* corr_out, int* emitted, int* next_tok, cudaStream_t st) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  void* base = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+      // device-side address of the scratch array on the current device
+      e = cudaGetSymbolAddress(&g_scratch_ptr[dev], g_verify_scratch);
+      if (e != cudaSuccess) {
+        g_scratch_ptr[dev] = nullptr;
+        return e;
+      }
+    }
+    base = g_scratch_ptr[dev];
+  }
+  VerifyArgs a;
+  a.logits = logits;
+  a.draft = draft;
+  a.b = b;
+  a.R = R;
+  a.D = D;
+  a.V = V;
+  a.P = verify_parts(b, R, V);
+  a.chunk = (V + a.P - 1) / a.P;
+  a.chunk = (a.chunk + 3) / 4 * 4;
+  a.n_out = n_out;
+  a.corr_out = corr_out;
+  a.emitted = emitted;
+  a.next_tok = next_tok;
+  a.tickets = static_cast<int*>(base);
+  a.part = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(base) + kNoAllocTicketBytes);
+  // tickets must start at zero whatever an earlier (possibly failed) call left
+  e = cudaMemsetAsync(a.tickets, 0, (size_t)b * sizeof(int), st);
+  if (e != cudaSuccess) return e;
+  void* args[] = {&a};
+  return launch_k((const void*)verify_kernel, dim3(a.P, b * R), dim3(256), 0, st, false, args);
 }
 
 }  // namespace dfl

@@ -97,4 +97,11 @@ size_t verify_ws_bytes(int b, int R, int64_t V);
 cudaError_t verify_accept(const float* logits, const int* draft, int b, int R, int D, int64_t V, int* n_out,
                           int* corr_out, int* emitted, int* next_tok, void* ws, cudaStream_t st, bool pdl);
 
+// Allocation-free variant of verify_accept: scratch lives in a fixed device
+// array of kNoAllocScratchBytes inside the library (k_small.cu).
+constexpr size_t kNoAllocScratchBytes = 64 * 1024;
+size_t verify_noalloc_need(int b, int R, int64_t V);
+cudaError_t verify_accept_noalloc(const float* logits, const int* draft, int b, int R, int D, int64_t V, int* n_out,
+                                  int* corr_out, int* emitted, int* next_tok, cudaStream_t st);
+
 }  // namespace dfl

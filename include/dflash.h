@@ -231,6 +231,33 @@ DFLASH_API int32_t dflash_verify_accept(const float* logits, const int32_t* draf
                              int32_t* emitted_out, int32_t* next_tok_out,
                              void* ws, size_t ws_bytes, void* stream);
 
+/* Allocation-free verify-accept.  The paper has no counterpart to this call;
+ * it exists for callers that cannot allocate device memory themselves (for
+ * example code running inside a stream capture that forbids allocation,
+ * embedders whose memory is fully pre-reserved by another allocator, or
+ * plain C hosts without a CUDA allocator wrapper).  It computes exactly what
+ * dflash_verify_accept computes, with the same arguments minus the
+ * workspace: its scratch is a fixed 64 KiB array inside the library's device
+ * image, resident on every GPU that loads the library until the process
+ * exits.  Shapes whose scratch would exceed that (more than 1024 sequences,
+ * or b*R*slices keys beyond the array) return DFLASH_EWORKSPACE.  The first
+ * call on a device resolves the array's device address (cudaGetSymbolAddress
+ * with that device current); make that first call before any stream
+ * capture.  Each call clears the per-sequence counters it needs with
+ * cudaMemsetAsync on the stream.  All calls share the one array, which keeps
+ * the last call's contents, so calls that can overlap on the GPU (different
+ * streams without ordering) race: serialise them.  No cudaMalloc, cudaFree
+ * or other allocating routine is ever called. */
+DFLASH_API int32_t dflash_verify_accept_noalloc(const float* logits,
+                                                const int32_t* draft,
+                                                int32_t b, int32_t R,
+                                                int32_t D, int64_t V,
+                                                int32_t* n_out,
+                                                int32_t* corr_out,
+                                                int32_t* emitted_out,
+                                                int32_t* next_tok_out,
+                                                void* stream);
+
 /* Draft-KV commit with rollback of the rejected suffix (mlx-dspark v0.0.3,
  * "Notes": KV rollback; dflash-mlx "What It Does": conditioning on target
  * hidden states).  hid: [b][rows_per_seq][k*H] fp16 target hidden rows of the
