@@ -38,7 +38,10 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture
 # of the named kernel on the named workload, keyed by a hash of the kernel's
 # source file; ignored (reported null) once that source has changed.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    "lmhead_kernel": {"workload": "qwen3-4b-shaped-5L-h2560-b16-ctx512", "bytes": 780937216,
+                      "src": "44ee09dfad9f58df"},
+}
 
 
 def src_hash(name: str) -> str:
