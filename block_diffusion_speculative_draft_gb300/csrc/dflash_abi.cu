@@ -26,6 +26,20 @@ int* status_ptr() {
   return ptrs[dev];
 }
 
+struct DevInfo {
+  int sms = 0, smem_optin = 0;
+};
+DevInfo dev_info() {
+  static DevInfo cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DevInfo();
+  if (!cache[dev].sms) {
+    cudaDeviceGetAttribute(&cache[dev].sms, cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&cache[dev].smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  }
+  return cache[dev];
+}
+
 inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -63,8 +77,41 @@ struct WS {
   __nv_bfloat16* h;
   float* y;
   void* lm;
+  // fused-step kernel
+  int* stick;
+  unsigned long long* skeys;
+  unsigned* sbar;
+  float* spart;
+  size_t spart_bytes;
+  float* sattn_o;
+  float* sattn_lse;
   size_t total;
 };
+
+constexpr int kStepMaxSplits = 8;
+
+int step_rows_pad(const dflash_config& c) {
+  const int rows = c.B * (c.nq / c.nkv);
+  return (rows + 127) / 128 * 128;
+}
+
+int step_ntiles_max(const dflash_config& c) {
+  int n = (c.nq + 2 * c.nkv) * c.d;
+  n = n > c.H ? n : c.H;
+  n = n > 2 * c.F ? n : 2 * c.F;
+  return n / 128;
+}
+
+int step_nslots_for(const dflash_config& c, int G) {
+  const int nqkv = (c.nq + 2 * c.nkv) * c.d;
+  int s = step_nslots(nqkv / 128, c.H / 128, G);
+  int t = step_nslots(c.H / 128, c.nq * c.d / 128, G);
+  s = s > t ? s : t;
+  t = step_nslots(2 * c.F / 128, c.H / 128, G);
+  s = s > t ? s : t;
+  t = step_nslots(c.H / 128, c.F / 128, G);
+  return s > t ? s : t;
+}
 
 // Carves the workspace; the lm-head's argmax keys and ticket come first so a
 // single zero-fill of the whole buffer initialises them.
@@ -78,6 +125,10 @@ WS carve(const dflash_config& c, int b, int rps, uint8_t* base) {
     return p;
   };
   w.lm = take(lmhead_ws_bytes(b * (c.B - 1)));
+  const bool step = M <= 32;
+  w.stick = (int*)take(step ? (size_t)step_ntiles_max(c) * sizeof(int) : 0);
+  w.skeys = (unsigned long long*)take(step ? 32 * sizeof(unsigned long long) : 0);
+  w.sbar = (unsigned*)take(step ? 2 * sizeof(unsigned) : 0);
   w.x = (float*)take((size_t)M * c.H * 4);
   w.u = (__half*)take((size_t)Mx * c.H * 2);
   w.q = (__half*)take((size_t)M * c.nq * c.d * 2);
@@ -87,6 +138,11 @@ WS carve(const dflash_config& c, int b, int rps, uint8_t* base) {
   w.g = (__half*)take((size_t)M * c.F * 2);
   w.h = (__nv_bfloat16*)take((size_t)b * (c.B - 1) * c.H * 2);
   w.y = (float*)take((size_t)Mc * c.H * 4);
+  w.spart_bytes = step ? (size_t)step_ntiles_max(c) * step_nslots_for(c, kNumSMs) * 32 * 128 * sizeof(float) : 0;
+  w.spart = (float*)take(w.spart_bytes);
+  const size_t na = step ? (size_t)b * c.nkv * kStepMaxSplits * step_rows_pad(c) : 0;
+  w.sattn_o = (float*)take(na * c.d * sizeof(float));
+  w.sattn_lse = (float*)take(na * sizeof(float));
   w.total = off;
   return w;
 }
@@ -223,6 +279,92 @@ int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const i
   const int qd = c.nq * c.d, kd = c.nkv * c.d;
   const size_t layer_kv = (size_t)b * c.nkv * kv->cap * c.d;
   cudaError_t e;
+  if (M <= step_max_mch() && c.L <= 8) {
+    // the whole step as one persistent kernel when it fits
+    const DevInfo di = dev_info();
+    const int mt = M <= 16 ? 2 : 4;
+    const size_t xb = step_x_bytes(mt, c.d, c.H);
+    int ring = 0;
+    if (di.smem_optin > 0) {
+      const size_t fixed = step_smem_bytes(mt, 0, xb);
+      ring = fixed < (size_t)di.smem_optin ? (int)(((size_t)di.smem_optin - fixed) / (kTileBytes + 16)) : 0;
+      ring = ring > 8 ? 8 : ring;
+    }
+    const int G = di.sms;
+    const int nslots = G > 0 ? step_nslots_for(c, G) : 0;
+    const size_t need_part = (size_t)step_ntiles_max(c) * nslots * 32 * 128 * sizeof(float);
+    if (ring >= 3 && G > 0 && need_part <= s.spart_bytes) {
+      StepArgs a;
+      memset(&a, 0, sizeof(a));
+      a.L = c.L;
+      a.H = c.H;
+      a.nq = c.nq;
+      a.nkv = c.nkv;
+      a.d = c.d;
+      a.F = c.F;
+      a.V = c.V;
+      a.B = c.B;
+      a.b = b;
+      a.M = M;
+      a.mask_id = c.mask_id;
+      a.cap = kv->cap;
+      const int nrc = step_rows_pad(c) / 128;
+      int nsa = (G + 2 * b * c.nkv * nrc - 1) / (2 * b * c.nkv * nrc);
+      const int maxk = (kv->cap + c.B + 127) / 128;
+      nsa = nsa > maxk ? maxk : nsa;
+      nsa = nsa > kStepMaxSplits ? kStepMaxSplits : nsa;
+      a.nsa = nsa < 1 ? 1 : nsa;
+      a.ring_stages = ring;
+      a.nslots = nslots;
+      a.xbytes = (int)xb;
+      a.eps = c.eps;
+      for (int p = 0; p < 64; ++p) a.inv_freq[p] = p < c.d / 2 ? pow((double)c.rope_theta, -2.0 * p / c.d) : 0.0;
+      auto sw = [](const dflash_w8& x) {
+        StepW8 r;
+        r.q = static_cast<const uint8_t*>(x.q);
+        r.s = reinterpret_cast<const __half*>(x.s);
+        r.N = (int)x.N;
+        r.K = (int)x.K;
+        r.layout = x.layout;
+        return r;
+      };
+      for (int l = 0; l < c.L; ++l) {
+        a.qkv[l] = sw(w->qkv[l]);
+        a.o[l] = sw(w->o[l]);
+        a.gu[l] = sw(w->gu[l]);
+        a.down[l] = sw(w->down[l]);
+      }
+      a.gamma_in = w->gamma_in;
+      a.gamma_post = w->gamma_post;
+      a.gamma_q = w->gamma_q;
+      a.gamma_k = w->gamma_k;
+      a.gamma_final = w->gamma_final;
+      a.embed = reinterpret_cast<const __nv_bfloat16*>(w->embed);
+      a.kc = reinterpret_cast<const __half*>(kv->k);
+      a.vc = reinterpret_cast<const __half*>(kv->v);
+      a.len = kv->len;
+      a.last_tok = last_tok;
+      a.draft_out = draft_out;
+      a.hidden_out = hidden_out;
+      a.logits_out = logits_out;
+      a.x = s.x;
+      a.u = s.u;
+      a.q = s.q;
+      a.kb = s.kb;
+      a.vb = s.vb;
+      a.ao = s.ao;
+      a.g = s.g;
+      a.h = s.h;
+      a.part = s.spart;
+      a.tickets = s.stick;
+      a.attn_o = s.sattn_o;
+      a.attn_lse = s.sattn_lse;
+      a.keys = s.skeys;
+      a.bar = s.sbar;
+      a.status = status;
+      return map_err(draft_step(a, reinterpret_cast<const __nv_bfloat16*>(w->lm_head), st, G));
+    }
+  }
   e = embed_rmsnorm(reinterpret_cast<const __nv_bfloat16*>(w->embed), last_tok, c.mask_id, c.V, b, c.B, c.H,
                     w->gamma_in, c.eps, s.x, s.u, st, false, status);
   if (e != cudaSuccess) return DFLASH_ECUDA;

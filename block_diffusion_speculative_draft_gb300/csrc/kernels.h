@@ -97,6 +97,56 @@ size_t verify_ws_bytes(int b, int R, int64_t V);
 cudaError_t verify_accept(const float* logits, const int* draft, int b, int R, int D, int64_t V, int* n_out,
                           int* corr_out, int* emitted, int* next_tok, void* ws, cudaStream_t st, bool pdl);
 
+// --- whole draft step as one persistent cooperative kernel (k_step.cu) ---
+struct StepW8 {
+  const uint8_t* q;
+  const __half* s;
+  int N, K, layout;
+};
+struct StepArgs {
+  int L, H, nq, nkv, d, F, V, B, b, M, mask_id, cap;
+  int nsa;          // attention key splits
+  int ring_stages;  // weight ring depth
+  int nslots;       // partial slots per row tile
+  int xbytes;       // shared union region bytes
+  float eps;
+  double inv_freq[64];
+  StepW8 qkv[8], o[8], gu[8], down[8];
+  const float* gamma_in;
+  const float* gamma_post;
+  const float* gamma_q;
+  const float* gamma_k;
+  const float* gamma_final;
+  const __nv_bfloat16* embed;
+  const __half* kc;
+  const __half* vc;
+  const int* len;
+  const int* last_tok;
+  int* draft_out;
+  float* hidden_out;
+  float* logits_out;
+  float* x;
+  __half* u;
+  __half* q;
+  __half* kb;
+  __half* vb;
+  __half* ao;
+  __half* g;
+  __nv_bfloat16* h;
+  float* part;
+  int* tickets;
+  float* attn_o;
+  float* attn_lse;
+  unsigned long long* keys;
+  unsigned* bar;
+  int* status;
+};
+int step_max_mch();
+size_t step_smem_bytes(int mt, int ring_stages, size_t xbytes);
+size_t step_x_bytes(int mt, int d, int H);
+int step_nslots(int ntiles, int KT, int G);
+cudaError_t draft_step(const StepArgs& a, const __nv_bfloat16* lm_head, cudaStream_t st, int G);
+
 // Allocation-free variant of verify_accept: scratch lives in a fixed device
 // array of kNoAllocScratchBytes inside the library (k_small.cu).
 constexpr size_t kNoAllocScratchBytes = 64 * 1024;

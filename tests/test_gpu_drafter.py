@@ -153,3 +153,14 @@ def test_bad_token_flag():
     draft = torch.empty((1, cfg.B - 1), dtype=torch.int32, device=DEV)
     api.dflash_draft_block(model, kv, torch.tensor([cfg.V + 5], dtype=torch.int32, device=DEV), draft, ws)
     assert api.dflash_get_status() & api.DEV_BAD_TOKEN
+
+
+@pytest.mark.parametrize("b,lo,hi", [(2, 20, 70), (4, 16, 90)])
+def test_tiny_batched_ragged(b, lo, hi):
+    """Ragged batches: b = 2 (32 block rows) and b = 4 (64 block rows) cover
+    both launch shapes of the draft step; every sequence matches the oracle."""
+    import dataclasses
+    cfg = dataclasses.replace(TINY, b=b, ctx=(), ctx_range=(lo, hi), seed=1100 + b)
+    W, model, ctx, kv, ws, hids = _setup(cfg, cfg.B)
+    _check_cache(cfg, W, kv, hids, ctx, range(b))
+    _check_draft(cfg, W, model, kv, ws, hids, ctx)
