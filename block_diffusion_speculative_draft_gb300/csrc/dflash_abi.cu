@@ -287,7 +287,7 @@ int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const i
     int ring = 0;
     if (di.smem_optin > 0) {
       const size_t fixed = step_smem_bytes(mt, 0, xb);
-      ring = fixed < (size_t)di.smem_optin ? (int)(((size_t)di.smem_optin - fixed) / (kTileBytes + 16)) : 0;
+      ring = fixed < (size_t)di.smem_optin ? (int)(((size_t)di.smem_optin - fixed) / (step_stage_bytes(mt) + 16)) : 0;
       ring = ring > 8 ? 8 : ring;
     }
     const int G = di.sms;

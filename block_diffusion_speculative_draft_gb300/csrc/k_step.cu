@@ -7,20 +7,24 @@
 // one CTA per SM runs the whole step (embedding, L x {QKV + QK-norm + RoPE,
 // block attention, o + residual, RMSNorm, gate|up + SwiGLU, down +
 // residual, RMSNorm}, final norm, lm-head + argmax):
-//  * a producer warp walks the CTA's weight schedule for the WHOLE step and
-//    streams 16 KB tiles (1-D bulk copies of packed int8 tiles, 2-D TMA boxes
-//    of the bf16 lm-head) into an mbarrier ring; weights never depend on
-//    activations, so the stream runs straight through phase boundaries;
-//  * eight consumer warps follow the same schedule, stage each tile's
-//    activation slice with cp.async (prefetch distance 2), convert int8 to
-//    fp16 exactly in registers and issue m16n8k16 MMAs (fp32 accumulate);
+//  * a prefetch warp walks the CTA's weight schedule for the WHOLE step and
+//    pulls each 16 KB tile into L2 (bulk / tensor prefetch) a fixed distance
+//    ahead; weights never depend on activations, so HBM keeps streaming
+//    straight through phase boundaries, with L2 as the deep buffer;
+//  * a loader warp follows the same schedule into an mbarrier ring in shared
+//    memory: per stage one weight tile (1-D bulk copy of a packed int8 tile,
+//    or a 2-D TMA box of the bf16 lm-head, now an L2 hit) plus the matching
+//    activation slice (2-D TMA, 128-byte swizzle, rows past M zero-filled),
+//    issued once the phase's inputs are complete;
+//  * eight consumer warps convert int8 to fp16 exactly in registers and issue
+//    m16n8k16 MMAs (fp32 accumulate);
 //  * the GEMM work of a phase is split stream-K style: CTA c owns a
 //    contiguous range of (row tile, k-tile) units; a row tile spanning several
 //    CTAs is finished by the last to arrive (atomic ticket), which sums the
 //    partials in CTA order (deterministic) and runs the fused epilogue;
-//  * phases are separated by a grid barrier among consumer warps (counter +
-//    generation, bounded spin); the launch is cooperative, so all CTAs are
-//    co-resident.
+//  * phases are separated by a grid barrier among consumer warps (one atomic
+//    per CTA on a self-resetting word whose top bit flips once per barrier,
+//    bounded spin); the launch is cooperative, so all CTAs are co-resident.
 // Data written by other CTAs inside the kernel is read with L1-bypassing
 // loads (cp.async.cg, ld.global.cg) after the grid barrier's acquire.
 // Only the activation rows M = b * B <= 32 path uses this kernel.
@@ -33,8 +37,11 @@ namespace {
 
 constexpr int kNC = 8;             // consumer warps
 constexpr int kCT = kNC * 32;      // consumer threads
-constexpr int kThr = kCT + 32;     // + producer warp
-constexpr int kStage = 16384;      // one ring stage
+constexpr int kThr = kCT + 64;     // + loader warp + L2-prefetch warp
+constexpr int kStage = 16384;      // weight bytes of one ring stage
+constexpr int kPrefetchAhead = 24; // L2 prefetch distance, in weight tiles
+constexpr int kMiscPhase = 2;      // misc[] slot: grid barriers completed
+constexpr int kMiscLoaded = 3;     // misc[] slot: stages issued by the loader
 constexpr int kTS = 132;           // epilogue tile stride (floats)
 
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory"); }
@@ -45,30 +52,36 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   return v;
 }
 
-// Grid barrier among the consumer warps of every CTA: arrival counter and
-// generation word in global memory, reset by the last arrival, so the words
-// are back at their start state after every barrier.  Bounded spin.
-__device__ void grid_sync(unsigned* bar, int* status) {
+__device__ __forceinline__ void st_release_smem(int* p, int v) {
+  asm volatile("st.release.cta.shared.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_smem(const int* p) {
+  int v;
+  asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+
+// Grid barrier among the consumer warps of every CTA.  CTA 0 adds
+// 2^31 - (G - 1), every other CTA adds 1, so the word's top bit flips exactly
+// once per barrier and the low bits return to their start value (the word is
+// reusable across barriers and launches).  Bounded spin.  Afterwards thread 0
+// publishes the number of completed barriers to the CTA's loader warp.
+__device__ void grid_sync(unsigned* bar, int* status, int* phase_cnt) {
+  fence_proxy_async_global();  // our global writes may be read by TMA next
   cbar();
   if (threadIdx.x == 0) {
-    const unsigned gen = ld_acquire_u32(bar + 1);
+    const unsigned inc = blockIdx.x == 0 ? (0x80000000u - (gridDim.x - 1)) : 1u;
     __threadfence();
-    const unsigned arrived = atomicAdd(bar, 1u);
-    if (arrived == gridDim.x - 1) {
-      atomicExch(bar, 0u);
-      __threadfence();
-      atomicAdd(bar + 1, 1u);
-    } else {
-      uint32_t i = 0;
-      while (ld_acquire_u32(bar + 1) == gen) {
-        __nanosleep(32);
-        if (++i > (1u << 25)) {
-          atomicOr(status, kDevWaitTimeout);
-          break;
-        }
+    const unsigned old = atomicAdd(bar, inc);
+    uint32_t i = 0;
+    while (((ld_acquire_u32(bar) ^ old) & 0x80000000u) == 0u) {
+      if (++i > (1u << 26)) {
+        atomicOr(status, kDevWaitTimeout);
+        break;
       }
     }
     __threadfence();
+    st_release_smem(phase_cnt, ld_acquire_smem(phase_cnt) + 1);
   }
   cbar();
 }
@@ -107,7 +120,7 @@ struct Smem {
   uint8_t* x;    // union region: epilogue tile / attention / lm-head reduce
   uint64_t* full;
   uint64_t* empty;
-  int* misc;  // [0] flag, [1..32] positions
+  int* misc;  // [0] ticket flag, [2] barriers done, [3] stages loaded, [32..63] row positions
   float* sc;  // [128]
   float* gam; // [128]
 };
@@ -124,60 +137,104 @@ __device__ __forceinline__ void rope_pair(float& x1, float& x2, int pos, double 
   x2 = b * cs + a * sn;
 }
 
-// ------------------------------------------------------------ producer ----
-template <typename F>
-__device__ __forceinline__ void for_gemm_units(int units, F f) {
-  const int G = gridDim.x, c = blockIdx.x;
-  const int u0 = unit_lo(c, units, G), u1 = unit_lo(c + 1, units, G);
-  for (int u = u0; u < u1; ++u) f(u);
-}
+// ------------------------------------------------------ weight schedule ----
+// Every weight stage of this CTA in consumption order, with the number of
+// grid barriers that must have completed before its activation slice exists.
+struct StageRef {
+  int kind;             // 0: packed int8 tile, 1: lm-head box
+  const uint8_t* wsrc;  // kind 0
+  int wx, wy;           // kind 1 box coordinates
+  int amap;             // activation tensor map: 0 u, 1 ao, 2 g, 3 h
+  int ax;               // activation column
+  int ready;            // barriers needed
+};
 
-__device__ void producer(const StepArgs& a, const CUtensorMap* lmmap, Smem& S) {
-  const uint64_t pol = policy_evict_first();
-  uint32_t gp = 0;
-  bool dead = false;
-  auto slot_ready = [&](int& slot) -> bool {
-    slot = (int)(gp % (uint32_t)a.ring_stages);
-    if (gp >= (uint32_t)a.ring_stages) {
-      if (!mbar_wait(&S.empty[slot], ((gp / a.ring_stages) - 1) & 1, a.status)) return false;
+template <typename F>
+__device__ __forceinline__ void for_each_stage(const StepArgs& a, F f) {
+  const int G = gridDim.x, c = blockIdx.x;
+  const int m = a.nsa > 1 ? 1 : 0, nbl = 7 + m;
+  auto gemm = [&](const StepW8& w, int amap, int ready) {
+    const int KT = w.K / kTile, units = (w.N / kTile) * KT;
+    const int u0 = unit_lo(c, units, G), u1 = unit_lo(c + 1, units, G);
+    for (int u = u0; u < u1; ++u) {
+      const int t = u / KT, kt = u - t * KT;
+      StageRef r{0, w.q + ((size_t)t * KT + kt) * kTileBytes, 0, 0, amap, kt * kTile, ready};
+      if (!f(r)) return false;
     }
     return true;
   };
-  auto push_bulk = [&](const uint8_t* src) {
-    if (dead) return;
-    int slot;
-    if (!slot_ready(slot)) {
-      dead = true;
-      return;
-    }
-    mbar_arrive_expect_tx(&S.full[slot], kStage);
-    bulk_g2s_hint(S.ring + slot * kStage, src, kStage, &S.full[slot], pol);
-    ++gp;
-  };
   for (int l = 0; l < a.L; ++l) {
-    const StepW8* ws[4] = {&a.qkv[l], &a.o[l], &a.gu[l], &a.down[l]};
-    for (int i = 0; i < 4; ++i) {
-      const StepW8& w = *ws[i];
-      const int KT = w.K / kTile, nt = w.N / kTile;
-      for_gemm_units(nt * KT, [&](int u) {
-        const int t = u / KT, kt = u - t * KT;
-        push_bulk(w.q + ((size_t)t * KT + kt) * kTileBytes);
-      });
-    }
+    const int base = 1 + l * nbl;
+    if (!gemm(a.qkv[l], 0, base)) return;
+    if (!gemm(a.o[l], 1, base + 2 + m)) return;
+    if (!gemm(a.gu[l], 0, base + 4 + m)) return;
+    if (!gemm(a.down[l], 2, base + 5 + m)) return;
   }
-  const int ntv = (a.V + 127) / 128, KS = a.H / 64;
-  for (int t = blockIdx.x; t < ntv && !dead; t += gridDim.x) {
+  const int ntv = (a.V + 127) / 128, KS = a.H / 64, ready = 1 + a.L * nbl;
+  for (int t = c; t < ntv; t += G)
     for (int ks = 0; ks < KS; ++ks) {
-      int slot;
-      if (!slot_ready(slot)) {
-        dead = true;
-        break;
-      }
-      mbar_arrive_expect_tx(&S.full[slot], kStage);
-      tma_load_2d_hint(S.ring + slot * kStage, lmmap, ks * 64, t * 128, &S.full[slot], pol);
-      ++gp;
+      StageRef r{1, nullptr, ks * 64, t * 128, 3, ks * 64, ready};
+      if (!f(r)) return;
     }
-  }
+}
+
+__device__ __forceinline__ const CUtensorMap* act_map(const StepMaps& mp, int i) {
+  return i == 0 ? &mp.u : (i == 1 ? &mp.ao : (i == 2 ? &mp.g : &mp.h));
+}
+
+// Loader warp (one thread): fills the shared ring stage by stage.
+__device__ void loader(const StepArgs& a, const StepMaps& mp, Smem& S, int mch) {
+  const uint64_t pol = policy_evict_first();
+  const int sb = kStage + 2 * mch * 128;  // stage stride
+  uint32_t gl = 0;
+  int seen = 0;
+  for_each_stage(a, [&](const StageRef& r) -> bool {
+    if (seen < r.ready) {
+      uint32_t i = 0;
+      while ((seen = ld_acquire_smem(S.misc + kMiscPhase)) < r.ready) {
+        if (++i > (1u << 28)) {
+          atomicOr(a.status, kDevWaitTimeout);
+          return false;
+        }
+      }
+      fence_proxy_async_global();
+    }
+    const int slot = (int)(gl % (uint32_t)a.ring_stages);
+    if (gl >= (uint32_t)a.ring_stages && !mbar_wait(&S.empty[slot], ((gl / a.ring_stages) - 1) & 1, a.status))
+      return false;
+    uint8_t* st = S.ring + (size_t)slot * sb;
+    const CUtensorMap* am = act_map(mp, r.amap);
+    if (r.kind == 0) {
+      mbar_arrive_expect_tx(&S.full[slot], kStage + 2 * mch * 128);
+      bulk_g2s_hint(st, r.wsrc, kStage, &S.full[slot], pol);
+      tma_load_2d(st + kStage, am, r.ax, 0, &S.full[slot]);
+      tma_load_2d(st + kStage + mch * 128, am, r.ax + 64, 0, &S.full[slot]);
+    } else {
+      mbar_arrive_expect_tx(&S.full[slot], kStage + mch * 128);
+      tma_load_2d_hint(st, &mp.lm, r.wx, r.wy, &S.full[slot], pol);
+      tma_load_2d(st + kStage, am, r.ax, 0, &S.full[slot]);
+    }
+    ++gl;
+    st_release_smem(S.misc + kMiscLoaded, (int)gl);
+    return true;
+  });
+}
+
+// Prefetch warp (one thread): keeps the next kPrefetchAhead weight tiles of
+// the schedule in flight towards L2.
+__device__ void prefetcher(const StepArgs& a, const StepMaps& mp, Smem& S) {
+  uint32_t gf = 0;
+  for_each_stage(a, [&](const StageRef& r) -> bool {
+    uint32_t i = 0;
+    while ((int)gf >= ld_acquire_smem(S.misc + kMiscLoaded) + kPrefetchAhead) {
+      __nanosleep(64);
+      if (++i > (1u << 24)) return false;
+    }
+    if (r.kind == 0) prefetch_l2_bulk(r.wsrc, kStage);
+    else prefetch_l2_tile(&mp.lm, r.wx, r.wy);
+    ++gf;
+    return true;
+  });
 }
 
 // ----------------------------------------------------------- consumers ----
@@ -188,19 +245,6 @@ struct Cons {
   uint32_t gc;  // weight stages consumed so far
   int warp, lane;
 };
-
-// Stage activation rows [0, mch) x 128 columns (fp16, row stride ld) into an
-// act buffer laid out as two 128-byte-swizzled [mch][64] halves.
-__device__ __forceinline__ void stage_act(Cons& C, uint8_t* buf, const __half* src, int ld, int k0) {
-  const int mch = C.geo.mch;
-  for (int c = threadIdx.x; c < mch * 16; c += kCT) {
-    const int m = c >> 4, ch16 = c & 15;
-    const int h = ch16 >> 3, ch = ch16 & 7;
-    const bool ok = m < C.a.M;
-    const __half* s = ok ? src + (size_t)m * ld + k0 + ch16 * 8 : src;
-    cp_async16(buf + h * mch * 128 + m * 128 + ((ch ^ (m & 7)) << 4), s, ok);
-  }
-}
 
 // One ring stage of a W8 GEMM: warp w owns m-group w (16 weight rows).
 template <int MT>
@@ -291,7 +335,7 @@ __device__ void step_epilogue(Cons& C, int ep, const StepW8& w, int t, const flo
   const float* gam = C.S.gam;
   const int lane = C.lane;
   for (int m = C.warp; m < M; m += kNC) {
-    const int p = C.S.misc[1 + m];
+    const int p = C.S.misc[32 + m];
     float v[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] = T[m * kTS + lane + 32 * i] * sc[lane + 32 * i];
@@ -336,12 +380,11 @@ __device__ void step_epilogue(Cons& C, int ep, const StepW8& w, int t, const flo
 
 // A W8A16 GEMM phase: activations act[M][K] fp16, weights w, epilogue ep.
 template <int MT>
-__device__ void gemm_phase(Cons& C, const StepW8& w, const __half* act, int ep, const float* gq, const float* gk) {
+__device__ void gemm_phase(Cons& C, const StepW8& w, int ep, const float* gq, const float* gk) {
   const StepArgs& a = C.a;
   const int G = gridDim.x, c = blockIdx.x;
   const int KT = w.K / kTile, ntiles = w.N / kTile, units = ntiles * KT;
   const int u0 = unit_lo(c, units, G), u1 = unit_lo(c + 1, units, G);
-  const int abytes = C.geo.mch * 256;
   const int g8 = C.lane >> 2, t4 = C.lane & 3;
   int u = u0;
   while (u < u1) {
@@ -366,29 +409,21 @@ __device__ void gemm_phase(Cons& C, const StepW8& w, const __half* act, int ep, 
     for (int j = 0; j < MT; ++j)
 #pragma unroll
       for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
-    // activation prologue: k-tiles 0 and 1 of the segment
-    stage_act(C, C.S.act + 0 * abytes, act, w.K, (kt0 + 0) * kTile);
-    cp_async_commit();
-    if (n > 1) stage_act(C, C.S.act + 1 * abytes, act, w.K, (kt0 + 1) * kTile);
-    cp_async_commit();
+    const int sb = kStage + 2 * C.geo.mch * 128;
     for (int i = 0; i < n; ++i) {
-      cp_async_wait<1>();
-      cbar();
-      if (i + 2 < n) stage_act(C, C.S.act + ((i + 2) % 3) * abytes, act, w.K, (kt0 + i + 2) * kTile);
-      cp_async_commit();
       const int slot = (int)(C.gc % (uint32_t)a.ring_stages);
       mbar_wait(&C.S.full[slot], (C.gc / a.ring_stages) & 1, a.status);
-      mma_w8_stage<MT>(C, C.S.ring + slot * kStage, C.S.act + (i % 3) * abytes, acc);
+      const uint8_t* st = C.S.ring + (size_t)slot * sb;
+      mma_w8_stage<MT>(C, st, st + kStage, acc);
       __syncwarp();
       if (C.lane == 0) mbar_arrive(&C.S.empty[slot]);
       ++C.gc;
     }
-    cp_async_wait<0>();
     // ---- segment end: partial or epilogue ----
+    cbar();  // every warp is done with the segment's stages and epilogue data
     int ns, slotp;
     tile_contrib(t, KT, units, G, c, ns, slotp);
     float* T = reinterpret_cast<float*>(C.S.x);
-    cbar();
     if (ns == 1) {
 #pragma unroll
       for (int j = 0; j < MT; ++j)
@@ -819,27 +854,13 @@ __device__ void lmhead_phase(Cons& C) {
   const int ntv = (a.V + 127) / 128, KS = a.H / 64;
   const int mch = MT * 8;
   const int M1 = a.b * (a.B - 1);
-  const int abytes = mch * 128;  // one [mch][64] bf16 half
   const int lane = C.lane, w = C.warp, g8 = lane >> 2, t4 = lane & 3;
   unsigned long long best[MT][2];
 #pragma unroll
   for (int jj = 0; jj < MT; ++jj) best[jj][0] = best[jj][1] = 0ull;
   int my_tiles = blockIdx.x < ntv ? (ntv - 1 - blockIdx.x) / gridDim.x + 1 : 0;
   const int total = my_tiles * KS;
-  auto stage_h = [&](int s) {
-    const int ks = s % KS;
-    uint8_t* buf = C.S.act + (s % 3) * abytes;
-    for (int c = threadIdx.x; c < mch * 8; c += kCT) {
-      const int m = c >> 3, ch = c & 7;
-      const bool ok = m < M1;
-      const __nv_bfloat16* src = ok ? a.h + (size_t)m * a.H + ks * 64 + ch * 8 : a.h;
-      cp_async16(buf + m * 128 + ((ch ^ (m & 7)) << 4), src, ok);
-    }
-  };
-  if (total > 0) stage_h(0);
-  cp_async_commit();
-  if (total > 1) stage_h(1);
-  cp_async_commit();
+  const int sb = kStage + 2 * mch * 128;
   float acc[MT][4];
   const int a_row = w * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
   const int a_ch = lane >> 4;
@@ -853,14 +874,10 @@ __device__ void lmhead_phase(Cons& C) {
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[jj][e] = 0.f;
     }
-    cp_async_wait<1>();
-    cbar();
-    if (s + 2 < total) stage_h(s + 2);
-    cp_async_commit();
     const int slot = (int)(C.gc % (uint32_t)a.ring_stages);
     mbar_wait(&C.S.full[slot], (C.gc / a.ring_stages) & 1, a.status);
-    const uint32_t wb = smem_u32(C.S.ring + slot * kStage);
-    const uint32_t hb = smem_u32(C.S.act + (s % 3) * abytes);
+    const uint32_t wb = smem_u32(C.S.ring + (size_t)slot * sb);
+    const uint32_t hb = wb + kStage;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       uint32_t af[4];
@@ -894,7 +911,7 @@ __device__ void lmhead_phase(Cons& C) {
         }
     }
   }
-  cp_async_wait<0>();
+  cbar();
   unsigned long long* red = reinterpret_cast<unsigned long long*>(C.S.x);
 #pragma unroll
   for (int jj = 0; jj < MT; ++jj)
@@ -922,35 +939,35 @@ __device__ void consumer(const StepArgs& a, Smem& S) {
   if (threadIdx.x < (unsigned)a.M) {
     const int m = threadIdx.x, j = m / a.B, slot = m - j * a.B;
     const int L0 = a.len[j];
-    S.misc[1 + m] = (L0 < 0 ? 0 : L0) + slot;
+    S.misc[32 + m] = (L0 < 0 ? 0 : L0) + slot;
   }
   embed_rows(C);
   cbar();  // the same CTA normalises the rows it embedded
   norm_rows(C, a.gamma_in, a.u);
-  grid_sync(a.bar, a.status);
+  grid_sync(a.bar, a.status, S.misc + kMiscPhase);
   for (int l = 0; l < a.L; ++l) {
-    gemm_phase<MT>(C, a.qkv[l], a.u, EP_QKV, a.gamma_q + (size_t)l * a.d, a.gamma_k + (size_t)l * a.d);
-    grid_sync(a.bar, a.status);
+    gemm_phase<MT>(C, a.qkv[l], EP_QKV, a.gamma_q + (size_t)l * a.d, a.gamma_k + (size_t)l * a.d);
+    grid_sync(a.bar, a.status, S.misc + kMiscPhase);
     if (a.d == 128) attn_phase<128>(C, l); else attn_phase<64>(C, l);
-    grid_sync(a.bar, a.status);
+    grid_sync(a.bar, a.status, S.misc + kMiscPhase);
     if (a.nsa > 1) {
       if (a.d == 128) merge_phase<128>(C); else merge_phase<64>(C);
-      grid_sync(a.bar, a.status);
+      grid_sync(a.bar, a.status, S.misc + kMiscPhase);
     }
-    gemm_phase<MT>(C, a.o[l], a.ao, EP_RESID, nullptr, nullptr);
-    grid_sync(a.bar, a.status);
+    gemm_phase<MT>(C, a.o[l], EP_RESID, nullptr, nullptr);
+    grid_sync(a.bar, a.status, S.misc + kMiscPhase);
     norm_rows(C, a.gamma_post + (size_t)l * a.H, a.u);
-    grid_sync(a.bar, a.status);
-    gemm_phase<MT>(C, a.gu[l], a.u, EP_SWIGLU, nullptr, nullptr);
-    grid_sync(a.bar, a.status);
-    gemm_phase<MT>(C, a.down[l], a.g, EP_RESID, nullptr, nullptr);
-    grid_sync(a.bar, a.status);
+    grid_sync(a.bar, a.status, S.misc + kMiscPhase);
+    gemm_phase<MT>(C, a.gu[l], EP_SWIGLU, nullptr, nullptr);
+    grid_sync(a.bar, a.status, S.misc + kMiscPhase);
+    gemm_phase<MT>(C, a.down[l], EP_RESID, nullptr, nullptr);
+    grid_sync(a.bar, a.status, S.misc + kMiscPhase);
     if (l + 1 < a.L) norm_rows(C, a.gamma_in + (size_t)(l + 1) * a.H, a.u);
     else final_rows(C);
-    grid_sync(a.bar, a.status);
+    grid_sync(a.bar, a.status, S.misc + kMiscPhase);
   }
   lmhead_phase<MT>(C);
-  grid_sync(a.bar, a.status);
+  grid_sync(a.bar, a.status, S.misc + kMiscPhase);
   if (blockIdx.x == 0) {
     const int M1 = a.b * (a.B - 1);
     for (int m = threadIdx.x; m < M1; m += kCT) {
@@ -961,14 +978,15 @@ __device__ void consumer(const StepArgs& a, Smem& S) {
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kThr, 1) draft_step_kernel(const __grid_constant__ CUtensorMap lmmap,
+__global__ void __launch_bounds__(kThr, 1) draft_step_kernel(const __grid_constant__ StepMaps maps,
                                                               const __grid_constant__ StepArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int kSB = kStage + 2 * (MT * 8) * 128;
   Smem S;
   S.ring = base;
-  S.act = S.ring + (size_t)a.ring_stages * kStage;
-  S.x = S.act + 3 * (MT * 8) * 256;
+  S.act = nullptr;
+  S.x = S.ring + (size_t)a.ring_stages * kSB;
   S.full = reinterpret_cast<uint64_t*>(S.x + a.xbytes);
   S.empty = S.full + a.ring_stages;
   S.misc = reinterpret_cast<int*>(S.empty + a.ring_stages);
@@ -979,15 +997,20 @@ __global__ void __launch_bounds__(kThr, 1) draft_step_kernel(const __grid_consta
       mbar_init(&S.full[i], 1);
       mbar_init(&S.empty[i], kNC);
     }
+    for (int i = 0; i < 64; ++i) S.misc[i] = 0;
     fence_mbar_init();
   }
   __syncthreads();
-  if (threadIdx.x >= kCT) {
-    if (threadIdx.x == kCT) {
-      prefetch_tmap(&lmmap);
-      producer(a, &lmmap, S);
-    }
-  } else {
+  if (threadIdx.x == kCT) {
+    prefetch_tmap(&maps.lm);
+    prefetch_tmap(&maps.u);
+    prefetch_tmap(&maps.ao);
+    prefetch_tmap(&maps.g);
+    prefetch_tmap(&maps.h);
+    loader(a, maps, S, MT * 8);
+  } else if (threadIdx.x == kCT + 32) {
+    prefetcher(a, maps, S);
+  } else if (threadIdx.x < kCT) {
     consumer<MT>(a, S);
   }
   __syncthreads();
@@ -997,9 +1020,10 @@ __global__ void __launch_bounds__(kThr, 1) draft_step_kernel(const __grid_consta
 
 int step_max_mch() { return 32; }
 
+size_t step_stage_bytes(int mt) { return kStage + 2 * (size_t)(mt * 8) * 128; }
+
 size_t step_smem_bytes(int mt, int ring_stages, size_t xbytes) {
-  return 1024 + (size_t)ring_stages * kStage + 3 * (size_t)(mt * 8) * 256 + xbytes + 2 * ring_stages * 8 + 64 * 4 +
-         256 * 4;
+  return 1024 + (size_t)ring_stages * step_stage_bytes(mt) + xbytes + 2 * ring_stages * 8 + 64 * 4 + 256 * 4;
 }
 
 size_t step_x_bytes(int mt, int d, int H) {
@@ -1038,15 +1062,25 @@ int step_nslots(int units_ntiles, int KT, int G) {
 cudaError_t draft_step(const StepArgs& a0, const __nv_bfloat16* lm_head, cudaStream_t st, int G) {
   StepArgs a = a0;
   const int mt = a.M <= 16 ? 2 : 4;
-  CUtensorMap lm;
-  if (!encode_tmap_2d(&lm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lm_head, (uint64_t)a.H, (uint64_t)a.V,
-                      (uint64_t)a.H * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B))
-    return cudaErrorInvalidValue;
+  const uint32_t mch = mt * 8;
+  StepMaps mp;
+  const int M1 = a.b * (a.B - 1);
+  bool ok = encode_tmap_2d(&mp.lm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, lm_head, (uint64_t)a.H, (uint64_t)a.V,
+                           (uint64_t)a.H * 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_tmap_2d(&mp.u, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.u, (uint64_t)a.H, (uint64_t)a.M,
+                            (uint64_t)a.H * 2, 64, mch, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_tmap_2d(&mp.ao, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.ao, (uint64_t)a.nq * a.d, (uint64_t)a.M,
+                            (uint64_t)a.nq * a.d * 2, 64, mch, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_tmap_2d(&mp.g, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.g, (uint64_t)a.F, (uint64_t)a.M,
+                            (uint64_t)a.F * 2, 64, mch, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && encode_tmap_2d(&mp.h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.h, (uint64_t)a.H, (uint64_t)M1,
+                            (uint64_t)a.H * 2, 64, mch, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return cudaErrorInvalidValue;
   const size_t smem = step_smem_bytes(mt, a.ring_stages, a.xbytes);
   const void* fn = mt == 2 ? (const void*)draft_step_kernel<2> : (const void*)draft_step_kernel<4>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  void* args[] = {&lm, &a};
+  void* args[] = {&mp, &a};
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(G);
   cfg.blockDim = dim3(kThr);

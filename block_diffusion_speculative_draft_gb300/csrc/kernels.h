@@ -141,7 +141,11 @@ struct StepArgs {
   unsigned* bar;
   int* status;
 };
+struct StepMaps {
+  CUtensorMap lm, u, ao, g, h;  // lm-head weights; activation buffers
+};
 int step_max_mch();
+size_t step_stage_bytes(int mt);
 size_t step_smem_bytes(int mt, int ring_stages, size_t xbytes);
 size_t step_x_bytes(int mt, int d, int H);
 int step_nslots(int ntiles, int KT, int G);
