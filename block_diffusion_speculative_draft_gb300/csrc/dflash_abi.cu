@@ -27,7 +27,7 @@ int* status_ptr() {
 }
 
 struct DevInfo {
-  int sms = 0, smem_optin = 0;
+  int sms = 0, smem_optin = 0, smem_sm = 0;
 };
 DevInfo dev_info() {
   static DevInfo cache[64];
@@ -36,6 +36,7 @@ DevInfo dev_info() {
   if (!cache[dev].sms) {
     cudaDeviceGetAttribute(&cache[dev].sms, cudaDevAttrMultiProcessorCount, dev);
     cudaDeviceGetAttribute(&cache[dev].smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaDeviceGetAttribute(&cache[dev].smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
   }
   return cache[dev];
 }
@@ -92,7 +93,7 @@ constexpr int kStepMaxSplits = 8;
 
 int step_rows_pad(const dflash_config& c) {
   const int rows = c.B * (c.nq / c.nkv);
-  return (rows + 127) / 128 * 128;
+  return (rows + 63) / 64 * 64;
 }
 
 int step_ntiles_max(const dflash_config& c) {
@@ -138,7 +139,7 @@ WS carve(const dflash_config& c, int b, int rps, uint8_t* base) {
   w.g = (__half*)take((size_t)M * c.F * 2);
   w.h = (__nv_bfloat16*)take((size_t)b * (c.B - 1) * c.H * 2);
   w.y = (float*)take((size_t)Mc * c.H * 4);
-  w.spart_bytes = step ? (size_t)step_ntiles_max(c) * step_nslots_for(c, kNumSMs) * 32 * 128 * sizeof(float) : 0;
+  w.spart_bytes = step ? (size_t)step_ntiles_max(c) * step_nslots_for(c, 2 * kNumSMs) * 32 * 128 * sizeof(float) : 0;
   w.spart = (float*)take(w.spart_bytes);
   const size_t na = step ? (size_t)b * c.nkv * kStepMaxSplits * step_rows_pad(c) : 0;
   w.sattn_o = (float*)take(na * c.d * sizeof(float));
@@ -284,16 +285,24 @@ int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const i
     const DevInfo di = dev_info();
     const int mt = M <= 16 ? 2 : 4;
     const size_t xb = step_x_bytes(mt, c.d, c.H);
-    int ring = 0;
-    if (di.smem_optin > 0) {
+    // two CTAs per SM: ring depth from half the SM's shared memory
+    int ring = 0, G = 0;
+    if (di.smem_sm > 0) {
+      const size_t per_cta = (size_t)di.smem_sm / 2 - 1024;
       const size_t fixed = step_smem_bytes(mt, 0, xb);
-      ring = fixed < (size_t)di.smem_optin ? (int)(((size_t)di.smem_optin - fixed) / (step_stage_bytes(mt) + 16)) : 0;
-      ring = ring > 8 ? 8 : ring;
+      ring = fixed < per_cta ? (int)((per_cta - fixed) / (step_stage_bytes(mt) + 16)) : 0;
+      ring = ring > 4 ? 4 : ring;
+      if (ring >= 2) {
+        const int occ = step_occupancy(mt, step_smem_bytes(mt, ring, xb));
+        G = occ >= 1 ? di.sms * (occ > 2 ? 2 : occ) : 0;
+      }
     }
-    const int G = di.sms;
+    const size_t ring_bytes = (size_t)ring * step_stage_bytes(mt);
+    const int akt = ring_bytes >= step_attn_bytes(c.d, 64) ? 64 : 32;
     const int nslots = G > 0 ? step_nslots_for(c, G) : 0;
     const size_t need_part = (size_t)step_ntiles_max(c) * nslots * 32 * 128 * sizeof(float);
-    if (ring >= 3 && G > 0 && need_part <= s.spart_bytes) {
+    if (ring_bytes < step_attn_bytes(c.d, akt)) ring = 0;
+    if (ring >= 2 && G > 0 && need_part <= s.spart_bytes) {
       StepArgs a;
       memset(&a, 0, sizeof(a));
       a.L = c.L;
@@ -308,7 +317,7 @@ int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const i
       a.M = M;
       a.mask_id = c.mask_id;
       a.cap = kv->cap;
-      const int nrc = step_rows_pad(c) / 128;
+      const int nrc = step_rows_pad(c) / 64;
       int nsa = (G + 2 * b * c.nkv * nrc - 1) / (2 * b * c.nkv * nrc);
       const int maxk = (kv->cap + c.B + 127) / 128;
       nsa = nsa > maxk ? maxk : nsa;
@@ -317,6 +326,7 @@ int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const i
       a.ring_stages = ring;
       a.nslots = nslots;
       a.xbytes = (int)xb;
+      a.attn_kt = akt;
       a.eps = c.eps;
       for (int p = 0; p < 64; ++p) a.inv_freq[p] = p < c.d / 2 ? pow((double)c.rope_theta, -2.0 * p / c.d) : 0.0;
       auto sw = [](const dflash_w8& x) {

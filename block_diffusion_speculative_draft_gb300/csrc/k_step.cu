@@ -7,17 +7,14 @@
 // one CTA per SM runs the whole step (embedding, L x {QKV + QK-norm + RoPE,
 // block attention, o + residual, RMSNorm, gate|up + SwiGLU, down +
 // residual, RMSNorm}, final norm, lm-head + argmax):
-//  * a prefetch warp walks the CTA's weight schedule for the WHOLE step and
-//    pulls each 16 KB tile into L2 (bulk / tensor prefetch) a fixed distance
-//    ahead; weights never depend on activations, so HBM keeps streaming
-//    straight through phase boundaries, with L2 as the deep buffer;
-//  * a loader warp follows the same schedule into an mbarrier ring in shared
-//    memory: per stage one weight tile (1-D bulk copy of a packed int8 tile,
-//    or a 2-D TMA box of the bf16 lm-head, now an L2 hit) plus the matching
-//    activation slice (2-D TMA, 128-byte swizzle, rows past M zero-filled),
-//    issued once the phase's inputs are complete;
-//  * eight consumer warps convert int8 to fp16 exactly in registers and issue
-//    m16n8k16 MMAs (fp32 accumulate);
+//  * a loader warp walks the CTA's weight schedule for the whole step and
+//    fills an mbarrier ring in shared memory: per stage one weight tile (1-D
+//    bulk copy of a packed int8 tile, or a 2-D TMA box of the bf16 lm-head)
+//    plus the matching activation slice (2-D TMA, 128-byte swizzle, rows past
+//    M zero-filled), issued once the phase's inputs are complete;
+//  * four consumer warps (32 weight rows each) convert int8 to fp16 exactly in
+//    registers and issue m16n8k16 MMAs (fp32 accumulate); two CTAs share each
+//    SM, since one CTA's load/consume pipeline alone tops out near 30 GB/s;
 //  * the GEMM work of a phase is split stream-K style: CTA c owns a
 //    contiguous range of (row tile, k-tile) units; a row tile spanning several
 //    CTAs is finished by the last to arrive (atomic ticket), which sums the
@@ -27,6 +24,8 @@
 //    bounded spin); the launch is cooperative, so all CTAs are co-resident.
 // Data written by other CTAs inside the kernel is read with L1-bypassing
 // loads (cp.async.cg, ld.global.cg) after the grid barrier's acquire.
+// Phases without weights (attention, norms) reuse the idle ring as scratch:
+// the loader issues nothing until the next GEMM phase's inputs are complete.
 // Only the activation rows M = b * B <= 32 path uses this kernel.
 #include "kernels.h"
 #include "ptx.cuh"
@@ -35,14 +34,14 @@ namespace dfl {
 
 namespace {
 
-constexpr int kNC = 8;             // consumer warps
+constexpr int kNC = 4;             // consumer warps (two CTAs share an SM)
 constexpr int kCT = kNC * 32;      // consumer threads
-constexpr int kThr = kCT + 64;     // + loader warp + L2-prefetch warp
+constexpr int kThr = kCT + 32;     // + loader warp
 constexpr int kStage = 16384;      // weight bytes of one ring stage
-constexpr int kPrefetchAhead = 24; // L2 prefetch distance, in weight tiles
 constexpr int kMiscPhase = 2;      // misc[] slot: grid barriers completed
-constexpr int kMiscLoaded = 3;     // misc[] slot: stages issued by the loader
 constexpr int kTS = 132;           // epilogue tile stride (floats)
+constexpr int kAR = kNC * 16;      // attention query rows per item
+constexpr int kNV = 8192 / 4 / kCT; // float4 per thread covering a row of up to 8192
 
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"r"(kCT) : "memory"); }
 
@@ -120,7 +119,7 @@ struct Smem {
   uint8_t* x;    // union region: epilogue tile / attention / lm-head reduce
   uint64_t* full;
   uint64_t* empty;
-  int* misc;  // [0] ticket flag, [2] barriers done, [3] stages loaded, [32..63] row positions
+  int* misc;  // [0] ticket flag, [2] barriers done, [32..63] row positions
   float* sc;  // [128]
   float* gam; // [128]
 };
@@ -215,24 +214,6 @@ __device__ void loader(const StepArgs& a, const StepMaps& mp, Smem& S, int mch) 
       tma_load_2d(st + kStage, am, r.ax, 0, &S.full[slot]);
     }
     ++gl;
-    st_release_smem(S.misc + kMiscLoaded, (int)gl);
-    return true;
-  });
-}
-
-// Prefetch warp (one thread): keeps the next kPrefetchAhead weight tiles of
-// the schedule in flight towards L2.
-__device__ void prefetcher(const StepArgs& a, const StepMaps& mp, Smem& S) {
-  uint32_t gf = 0;
-  for_each_stage(a, [&](const StageRef& r) -> bool {
-    uint32_t i = 0;
-    while ((int)gf >= ld_acquire_smem(S.misc + kMiscLoaded) + kPrefetchAhead) {
-      __nanosleep(64);
-      if (++i > (1u << 24)) return false;
-    }
-    if (r.kind == 0) prefetch_l2_bulk(r.wsrc, kStage);
-    else prefetch_l2_tile(&mp.lm, r.wx, r.wy);
-    ++gf;
     return true;
   });
 }
@@ -246,20 +227,24 @@ struct Cons {
   int warp, lane;
 };
 
-// One ring stage of a W8 GEMM: warp w owns m-group w (16 weight rows).
+// One ring stage of a W8 GEMM: warp w owns m-groups 2w and 2w+1 (32 weight
+// rows), all eight k16 steps of the 128-column tile.
 template <int MT>
-__device__ __forceinline__ void mma_w8_stage(Cons& C, const uint8_t* stage, const uint8_t* abuf, float (&acc)[MT][4]) {
+__device__ __forceinline__ void mma_w8_stage(Cons& C, const uint8_t* stage, const uint8_t* abuf,
+                                             float (&acc)[2][MT][4]) {
   const int w = C.warp, lane = C.lane;
-  const uint8_t* wl = stage + (((w >> 1) * 8) * 32 + lane) * 16 + (w & 1) * 8;
+  const uint8_t* wl = stage + ((w * 8) * 32 + lane) * 16;
   const int g_tok_lo = (lane & 7) + ((lane >> 4) << 3);
   const int ch_hi = (lane >> 3) & 1;
   const uint32_t abase = smem_u32(abuf);
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
-    const uint2 wv = *reinterpret_cast<const uint2*>(wl + ks * 32 * 16);
-    uint32_t af[4];
-    biased_u8x4_to_half2x2(wv.x, af[0], af[1]);
-    biased_u8x4_to_half2x2(wv.y, af[2], af[3]);
+    const uint4 wv = *reinterpret_cast<const uint4*>(wl + ks * 32 * 16);
+    uint32_t af[2][4];
+    biased_u8x4_to_half2x2(wv.x, af[0][0], af[0][1]);
+    biased_u8x4_to_half2x2(wv.y, af[0][2], af[0][3]);
+    biased_u8x4_to_half2x2(wv.z, af[1][0], af[1][1]);
+    biased_u8x4_to_half2x2(wv.w, af[1][2], af[1][3]);
     const uint32_t hbase = abase + (ks >> 2) * (MT * 8 * 128);
     const int ch = ((ks & 3) << 1) + ch_hi;
 #pragma unroll
@@ -267,8 +252,10 @@ __device__ __forceinline__ void mma_w8_stage(Cons& C, const uint8_t* stage, cons
       const int tok = p * 16 + g_tok_lo;
       uint32_t b0, b1, b2, b3;
       ldsm_x4(hbase + tok * 128 + ((ch ^ (tok & 7)) << 4), b0, b1, b2, b3);
-      mma_f16(acc[2 * p], af, b0, b1);
-      mma_f16(acc[2 * p + 1], af, b2, b3);
+      mma_f16(acc[0][2 * p], af[0], b0, b1);
+      mma_f16(acc[1][2 * p], af[1], b0, b1);
+      mma_f16(acc[0][2 * p + 1], af[0], b2, b3);
+      mma_f16(acc[1][2 * p + 1], af[1], b2, b3);
     }
   }
 }
@@ -404,11 +391,13 @@ __device__ void gemm_phase(Cons& C, const StepW8& w, int ep, const float* gq, co
         C.S.gam[threadIdx.x] = threadIdx.x < a.d ? gsrc[threadIdx.x] : 1.f;
       }
     }
-    float acc[MT][4];
+    float acc[2][MT][4];
 #pragma unroll
-    for (int j = 0; j < MT; ++j)
+    for (int x = 0; x < 2; ++x)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+      for (int j = 0; j < MT; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[x][j][e] = 0.f;
     const int sb = kStage + 2 * C.geo.mch * 128;
     for (int i = 0; i < n; ++i) {
       const int slot = (int)(C.gc % (uint32_t)a.ring_stages);
@@ -426,10 +415,12 @@ __device__ void gemm_phase(Cons& C, const StepW8& w, int ep, const float* gq, co
     float* T = reinterpret_cast<float*>(C.S.x);
     if (ns == 1) {
 #pragma unroll
-      for (int j = 0; j < MT; ++j)
+      for (int x = 0; x < 2; ++x)
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          T[(j * 8 + 2 * t4 + (e & 1)) * kTS + C.warp * 16 + g8 + ((e >> 1) << 3)] = acc[j][e];
+        for (int j = 0; j < MT; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            T[(j * 8 + 2 * t4 + (e & 1)) * kTS + C.warp * 32 + x * 16 + g8 + ((e >> 1) << 3)] = acc[x][j][e];
       cbar();
       step_epilogue<MT>(C, ep, w, t, T, gq, gk);
       cbar();
@@ -437,10 +428,12 @@ __device__ void gemm_phase(Cons& C, const StepW8& w, int ep, const float* gq, co
       const int mch = C.geo.mch;
       float* P = a.part + ((size_t)t * a.nslots + slotp) * mch * kTile;
 #pragma unroll
-      for (int j = 0; j < MT; ++j)
+      for (int x = 0; x < 2; ++x)
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          P[(j * 8 + 2 * t4 + (e & 1)) * kTile + C.warp * 16 + g8 + ((e >> 1) << 3)] = acc[j][e];
+        for (int j = 0; j < MT; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            P[(j * 8 + 2 * t4 + (e & 1)) * kTile + C.warp * 32 + x * 16 + g8 + ((e >> 1) << 3)] = acc[x][j][e];
       __threadfence();
       cbar();
       if (threadIdx.x == 0) {
@@ -490,15 +483,15 @@ __device__ void norm_rows(Cons& C, const float* gamma, __half* out) {
   for (int m = blockIdx.x; m < a.M; m += gridDim.x) {
     const float4* xr = reinterpret_cast<const float4*>(a.x + (size_t)m * a.H);
     const int n4 = a.H >> 2;
-    float4 v[8];
+    float4 v[kNV];
     float ss = 0.f;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kNV; ++i) {
       const int c4 = threadIdx.x + i * kCT;
       v[i] = c4 < n4 ? __ldcg(xr + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+    for (int i = 0; i < kNV; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (C.lane == 0) red[C.warp] = ss;
@@ -509,7 +502,7 @@ __device__ void norm_rows(Cons& C, const float* gamma, __half* out) {
     const float inv = rsqrtf(tot / a.H + a.eps);
     const float4* g4 = reinterpret_cast<const float4*>(gamma);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < kNV; ++i) {
       const int c4 = threadIdx.x + i * kCT;
       if (c4 < n4) {
         const float4 gg = g4[c4];
@@ -553,15 +546,15 @@ __device__ void final_rows(Cons& C) {
     const int j = o / (a.B - 1), i = o - j * (a.B - 1);
     const float4* xr = reinterpret_cast<const float4*>(a.x + ((size_t)j * a.B + i + 1) * a.H);
     const int n4 = a.H >> 2;
-    float4 v[8];
+    float4 v[kNV];
     float ss = 0.f;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < kNV; ++q) {
       const int c4 = threadIdx.x + q * kCT;
       v[q] = c4 < n4 ? __ldcg(xr + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int q = 0; q < 8; ++q) ss += v[q].x * v[q].x + v[q].y * v[q].y + v[q].z * v[q].z + v[q].w * v[q].w;
+    for (int q = 0; q < kNV; ++q) ss += v[q].x * v[q].x + v[q].y * v[q].y + v[q].z * v[q].z + v[q].w * v[q].w;
 #pragma unroll
     for (int s = 16; s > 0; s >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, s);
     if (C.lane == 0) red[C.warp] = ss;
@@ -572,7 +565,7 @@ __device__ void final_rows(Cons& C) {
     const float inv = rsqrtf(tot / a.H + a.eps);
     const float4* g4 = reinterpret_cast<const float4*>(a.gamma_final);
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
+    for (int q = 0; q < kNV; ++q) {
       const int c4 = threadIdx.x + q * kCT;
       if (c4 < n4) {
         const float4 gg = g4[c4];
@@ -591,18 +584,18 @@ __device__ void final_rows(Cons& C) {
 }
 
 // Block attention of one layer: items (sequence, kv head, key split,
-// query-row chunk of <= 128 rows); non-causal over [context || block].
-template <int D>
+// query-row chunk of <= kAR rows); non-causal over [context || block]; key
+// tiles of KT keys.
+template <int D, int KT>
 __device__ void attn_phase(Cons& C, int l) {
   const StepArgs& a = C.a;
   constexpr int RB = D * 2;
-  constexpr int KT = 64;
   const int grp = a.nq / a.nkv, rows = a.B * grp;
-  const int nrc = (rows + 127) / 128;
+  const int nrc = (rows + kAR - 1) / kAR;
   const int NS = a.nsa;
   const int items = a.b * a.nkv * NS * nrc;
-  uint8_t* sQ = C.S.x;
-  uint8_t* sK = sQ + 128 * RB;
+  uint8_t* sQ = C.S.ring;  // the ring is idle while attention runs
+  uint8_t* sK = sQ + kAR * RB;
   uint8_t* sV = sK + 2 * KT * RB;
   const __half* kc = a.kc + (size_t)l * a.b * a.nkv * a.cap * D;
   const __half* vc = a.vc + (size_t)l * a.b * a.nkv * a.cap * D;
@@ -613,7 +606,7 @@ __device__ void attn_phase(Cons& C, int l) {
     const int sp = (item / nrc) % NS;
     const int g = (item / (nrc * NS)) % a.nkv;
     const int j = item / (nrc * NS * a.nkv);
-    const int r0 = rc * 128, r1 = min(rows, r0 + 128);
+    const int r0 = rc * kAR, r1 = min(rows, r0 + kAR);
     const int nrw = (r1 - r0 + 15) / 16;  // row groups in this chunk
     int L = a.len[j];
     L = L < 0 ? 0 : (L > a.cap ? a.cap : L);
@@ -684,15 +677,15 @@ __device__ void attn_phase(Cons& C, int l) {
         }
         const uint32_t kb = smem_u32(sK + (it & 1) * KT * RB);
         const uint32_t vb = smem_u32(sV + (it & 1) * KT * RB);
-        float s[8][4];
+        float s[KT / 8][4];
 #pragma unroll
-        for (int n = 0; n < 8; ++n)
+        for (int n = 0; n < KT / 8; ++n)
 #pragma unroll
           for (int e = 0; e < 4; ++e) s[n][e] = 0.f;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
-          for (int n16 = 0; n16 < 4; ++n16) {
+          for (int n16 = 0; n16 < KT / 16; ++n16) {
             const int key = n16 * 16 + (lane & 7) + ((lane >> 4) << 3);
             const int ch = 2 * ks + ((lane >> 3) & 1);
             uint32_t b0, b1, b2, b3;
@@ -704,7 +697,7 @@ __device__ void attn_phase(Cons& C, int l) {
         const int kbase = k0 + it * KT;
         float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-        for (int n = 0; n < 8; ++n)
+        for (int n = 0; n < KT / 8; ++n)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int key = kbase + n * 8 + 2 * t4 + (e & 1);
@@ -724,9 +717,9 @@ __device__ void attn_phase(Cons& C, int l) {
           corr[r] = exp2f(mrow[r] - mnew[r]);
           mrow[r] = mnew[r];
         }
-        uint32_t pf[4][4];
+        uint32_t pf[KT / 16][4];
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
+        for (int n = 0; n < KT / 8; ++n) {
           const float p0 = exp2f(s[n][0] - mnew[0]), p1 = exp2f(s[n][1] - mnew[0]);
           const float p2 = exp2f(s[n][2] - mnew[1]), p3 = exp2f(s[n][3] - mnew[1]);
           rs[0] += p0 + p1;
@@ -749,7 +742,7 @@ __device__ void attn_phase(Cons& C, int l) {
           o[i][3] *= corr[1];
         }
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
+        for (int kk = 0; kk < KT / 16; ++kk) {
 #pragma unroll
           for (int dp = 0; dp < D / 16; ++dp) {
             const int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -771,7 +764,7 @@ __device__ void attn_phase(Cons& C, int l) {
         inv[r] = lrow[r] > 0.f ? 1.f / lrow[r] : 0.f;
         lse[r] = lrow[r] > 0.f ? mrow[r] + log2f(lrow[r]) : -INFINITY;
       }
-      const int rows_pad = nrc * 128;
+      const int rows_pad = nrc * kAR;
 #pragma unroll
       for (int i = 0; i < D / 8; ++i)
 #pragma unroll
@@ -802,7 +795,7 @@ template <int D>
 __device__ void merge_phase(Cons& C) {
   const StepArgs& a = C.a;
   const int grp = a.nq / a.nkv, rows = a.B * grp;
-  const int rows_pad = ((rows + 127) / 128) * 128;
+  const int rows_pad = ((rows + kAR - 1) / kAR) * kAR;
   const int NS = a.nsa;
   constexpr int CPR = D / 8;            // 8-dim chunks per row
   constexpr int RPI = kCT / CPR;        // rows per item
@@ -861,8 +854,8 @@ __device__ void lmhead_phase(Cons& C) {
   int my_tiles = blockIdx.x < ntv ? (ntv - 1 - blockIdx.x) / gridDim.x + 1 : 0;
   const int total = my_tiles * KS;
   const int sb = kStage + 2 * mch * 128;
-  float acc[MT][4];
-  const int a_row = w * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+  float acc[2][MT][4];
+  const int a_row0 = w * 32 + (lane & 7) + ((lane >> 3) & 1) * 8;  // + 16 mg
   const int a_ch = lane >> 4;
   const int b_tok = (lane & 7) + ((lane >> 4) << 3);
   const int b_ch = (lane >> 3) & 1;
@@ -870,9 +863,11 @@ __device__ void lmhead_phase(Cons& C) {
     const int ks = s % KS;
     if (ks == 0) {
 #pragma unroll
-      for (int jj = 0; jj < MT; ++jj)
+      for (int x = 0; x < 2; ++x)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[jj][e] = 0.f;
+        for (int jj = 0; jj < MT; ++jj)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[x][jj][e] = 0.f;
     }
     const int slot = (int)(C.gc % (uint32_t)a.ring_stages);
     mbar_wait(&C.S.full[slot], (C.gc / a.ring_stages) & 1, a.status);
@@ -880,17 +875,23 @@ __device__ void lmhead_phase(Cons& C) {
     const uint32_t hb = wb + kStage;
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
-      uint32_t af[4];
+      uint32_t af[2][4];
       const int ch = 2 * kk + a_ch;
-      ldsm_x4(wb + a_row * 128 + ((ch ^ (a_row & 7)) << 4), af[0], af[1], af[2], af[3]);
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {
+        const int row = a_row0 + 16 * x;
+        ldsm_x4(wb + row * 128 + ((ch ^ (row & 7)) << 4), af[x][0], af[x][1], af[x][2], af[x][3]);
+      }
 #pragma unroll
       for (int p = 0; p < MT / 2; ++p) {
         const int tok = p * 16 + b_tok;
         const int chb = 2 * kk + b_ch;
         uint32_t b0, b1, b2, b3;
         ldsm_x4(hb + tok * 128 + ((chb ^ (tok & 7)) << 4), b0, b1, b2, b3);
-        mma_bf16(acc[2 * p], af, b0, b1);
-        mma_bf16(acc[2 * p + 1], af, b2, b3);
+        mma_bf16(acc[0][2 * p], af[0], b0, b1);
+        mma_bf16(acc[1][2 * p], af[1], b0, b1);
+        mma_bf16(acc[0][2 * p + 1], af[0], b2, b3);
+        mma_bf16(acc[1][2 * p + 1], af[1], b2, b3);
       }
     }
     __syncwarp();
@@ -899,16 +900,18 @@ __device__ void lmhead_phase(Cons& C) {
     if (ks == KS - 1) {
       const int tile = blockIdx.x + (s / KS) * gridDim.x;
 #pragma unroll
-      for (int jj = 0; jj < MT; ++jj)
+      for (int x = 0; x < 2; ++x)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int v = tile * 128 + w * 16 + g8 + ((e >> 1) << 3);
-          const int m = jj * 8 + 2 * t4 + (e & 1);
-          if (v < a.V) {
-            best[jj][e & 1] = umax64(best[jj][e & 1], argmax_key(acc[jj][e], (uint32_t)v));
-            if (a.logits_out && m < M1) a.logits_out[(size_t)m * a.V + v] = acc[jj][e];
+        for (int jj = 0; jj < MT; ++jj)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int v = tile * 128 + w * 32 + 16 * x + g8 + ((e >> 1) << 3);
+            const int m = jj * 8 + 2 * t4 + (e & 1);
+            if (v < a.V) {
+              best[jj][e & 1] = umax64(best[jj][e & 1], argmax_key(acc[x][jj][e], (uint32_t)v));
+              if (a.logits_out && m < M1) a.logits_out[(size_t)m * a.V + v] = acc[x][jj][e];
+            }
           }
-        }
     }
   }
   cbar();
@@ -948,7 +951,11 @@ __device__ void consumer(const StepArgs& a, Smem& S) {
   for (int l = 0; l < a.L; ++l) {
     gemm_phase<MT>(C, a.qkv[l], EP_QKV, a.gamma_q + (size_t)l * a.d, a.gamma_k + (size_t)l * a.d);
     grid_sync(a.bar, a.status, S.misc + kMiscPhase);
-    if (a.d == 128) attn_phase<128>(C, l); else attn_phase<64>(C, l);
+    if (a.d == 128) {
+      if (a.attn_kt == 64) attn_phase<128, 64>(C, l); else attn_phase<128, 32>(C, l);
+    } else {
+      attn_phase<64, 64>(C, l);
+    }
     grid_sync(a.bar, a.status, S.misc + kMiscPhase);
     if (a.nsa > 1) {
       if (a.d == 128) merge_phase<128>(C); else merge_phase<64>(C);
@@ -978,7 +985,7 @@ __device__ void consumer(const StepArgs& a, Smem& S) {
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kThr, 1) draft_step_kernel(const __grid_constant__ StepMaps maps,
+__global__ void __launch_bounds__(kThr, 2) draft_step_kernel(const __grid_constant__ StepMaps maps,
                                                               const __grid_constant__ StepArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -986,7 +993,7 @@ __global__ void __launch_bounds__(kThr, 1) draft_step_kernel(const __grid_consta
   Smem S;
   S.ring = base;
   S.act = nullptr;
-  S.x = S.ring + (size_t)a.ring_stages * kSB;
+  S.x = S.ring + (size_t)a.ring_stages * kSB;  // epilogue tile / reductions
   S.full = reinterpret_cast<uint64_t*>(S.x + a.xbytes);
   S.empty = S.full + a.ring_stages;
   S.misc = reinterpret_cast<int*>(S.empty + a.ring_stages);
@@ -1008,8 +1015,6 @@ __global__ void __launch_bounds__(kThr, 1) draft_step_kernel(const __grid_consta
     prefetch_tmap(&maps.g);
     prefetch_tmap(&maps.h);
     loader(a, maps, S, MT * 8);
-  } else if (threadIdx.x == kCT + 32) {
-    prefetcher(a, maps, S);
   } else if (threadIdx.x < kCT) {
     consumer<MT>(a, S);
   }
@@ -1028,12 +1033,24 @@ size_t step_smem_bytes(int mt, int ring_stages, size_t xbytes) {
 
 size_t step_x_bytes(int mt, int d, int H) {
   const size_t tile = (size_t)(mt * 8) * kTS * 4;
-  const size_t attn = (size_t)128 * d * 2 + 4 * 64 * (size_t)d * 2;
   const size_t lm = (size_t)kNC * (mt * 8) * 8;
-  size_t x = tile > attn ? tile : attn;
-  x = x > lm ? x : lm;
+  size_t x = tile > lm ? tile : lm;
+  (void)d;
   (void)H;
   return (x + 1023) / 1024 * 1024;
+}
+
+// attention scratch (aliases the ring): query rows + double-buffered K and V
+size_t step_attn_bytes(int d, int kt) { return (size_t)kAR * d * 2 + 4 * (size_t)kt * d * 2; }
+
+int step_threads() { return kThr; }
+
+int step_occupancy(int mt, size_t smem) {
+  const void* fn = mt == 2 ? (const void*)draft_step_kernel<2> : (const void*)draft_step_kernel<4>;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, kThr, smem) != cudaSuccess) return 0;
+  return n;
 }
 
 int step_nslots(int units_ntiles, int KT, int G) {

@@ -108,7 +108,8 @@ struct StepArgs {
   int nsa;          // attention key splits
   int ring_stages;  // weight ring depth
   int nslots;       // partial slots per row tile
-  int xbytes;       // shared union region bytes
+  int xbytes;       // epilogue / reduction region bytes
+  int attn_kt;      // attention key tile (64 or 32)
   float eps;
   double inv_freq[64];
   StepW8 qkv[8], o[8], gu[8], down[8];
@@ -149,6 +150,9 @@ size_t step_stage_bytes(int mt);
 size_t step_smem_bytes(int mt, int ring_stages, size_t xbytes);
 size_t step_x_bytes(int mt, int d, int H);
 int step_nslots(int ntiles, int KT, int G);
+size_t step_attn_bytes(int d, int kt);
+int step_threads();
+int step_occupancy(int mt, size_t smem);
 cudaError_t draft_step(const StepArgs& a, const __nv_bfloat16* lm_head, cudaStream_t st, int G);
 
 // Allocation-free variant of verify_accept: scratch lives in a fixed device
