@@ -127,7 +127,7 @@ WS carve(const dflash_config& c, int b, int rps, uint8_t* base) {
   };
   w.lm = take(lmhead_ws_bytes(b * (c.B - 1)));
   const bool step = M <= 32;
-  w.stick = (int*)take(step ? (size_t)step_ntiles_max(c) * sizeof(int) : 0);
+  w.stick = (int*)take(step ? 2 * (size_t)step_ntiles_max(c) * sizeof(int) : 0);
   w.skeys = (unsigned long long*)take(step ? 32 * sizeof(unsigned long long) : 0);
   w.sbar = (unsigned*)take(step ? 2 * sizeof(unsigned) : 0);
   w.x = (float*)take((size_t)M * c.H * 4);
@@ -327,6 +327,7 @@ int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const i
       a.nslots = nslots;
       a.xbytes = (int)xb;
       a.attn_kt = akt;
+      a.ntmax = step_ntiles_max(c);
       a.eps = c.eps;
       for (int p = 0; p < 64; ++p) a.inv_freq[p] = p < c.d / 2 ? pow((double)c.rope_theta, -2.0 * p / c.d) : 0.0;
       auto sw = [](const dflash_w8& x) {

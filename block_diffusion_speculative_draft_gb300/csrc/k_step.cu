@@ -9,9 +9,10 @@
 // residual, RMSNorm}, final norm, lm-head + argmax):
 //  * a loader warp walks the CTA's weight schedule for the whole step and
 //    fills an mbarrier ring in shared memory: per stage one weight tile (1-D
-//    bulk copy of a packed int8 tile, or a 2-D TMA box of the bf16 lm-head)
-//    plus the matching activation slice (2-D TMA, 128-byte swizzle, rows past
-//    M zero-filled), issued once the phase's inputs are complete;
+//    bulk copy of a packed int8 tile, or a 2-D TMA box of the bf16 lm-head),
+//    issued as soon as the slot frees so weights stream ahead through phase
+//    boundaries, plus the matching activation slice (2-D TMA, 128-byte
+//    swizzle, rows past M zero-filled), issued once the phase's inputs exist;
 //  * four consumer warps (32 weight rows each) convert int8 to fp16 exactly in
 //    registers and issue m16n8k16 MMAs (fp32 accumulate); two CTAs share each
 //    SM, since one CTA's load/consume pipeline alone tops out near 30 GB/s;
@@ -24,8 +25,8 @@
 //    bounded spin); the launch is cooperative, so all CTAs are co-resident.
 // Data written by other CTAs inside the kernel is read with L1-bypassing
 // loads (cp.async.cg, ld.global.cg) after the grid barrier's acquire.
-// Phases without weights (attention, norms) reuse the idle ring as scratch:
-// the loader issues nothing until the next GEMM phase's inputs are complete.
+// Attention reuses the ring as scratch: the loader holds back each layer's
+// o-projection tiles until that layer's attention phase has ended.
 // Only the activation rows M = b * B <= 32 path uses this kernel.
 #include "kernels.h"
 #include "ptx.cuh"
@@ -145,77 +146,139 @@ struct StageRef {
   int wx, wy;           // kind 1 box coordinates
   int amap;             // activation tensor map: 0 u, 1 ao, 2 g, 3 h
   int ax;               // activation column
-  int ready;            // barriers needed
+  int ready;            // barriers needed before the activation slice
+  int wready;           // barriers needed before the weight tile (the ring
+                        // doubles as attention scratch until attention ends)
 };
 
-template <typename F>
-__device__ __forceinline__ void for_each_stage(const StepArgs& a, F f) {
-  const int G = gridDim.x, c = blockIdx.x;
-  const int m = a.nsa > 1 ? 1 : 0, nbl = 7 + m;
-  auto gemm = [&](const StepW8& w, int amap, int ready) {
-    const int KT = w.K / kTile, units = (w.N / kTile) * KT;
-    const int u0 = unit_lo(c, units, G), u1 = unit_lo(c + 1, units, G);
-    for (int u = u0; u < u1; ++u) {
-      const int t = u / KT, kt = u - t * KT;
-      StageRef r{0, w.q + ((size_t)t * KT + kt) * kTileBytes, 0, 0, amap, kt * kTile, ready};
-      if (!f(r)) return false;
+// Iterator over the schedule (GEMMs qkv, o, gu, down per layer, then the
+// lm-head tiles of this CTA).
+struct StageIter {
+  const StepArgs* a;
+  int gi;      // GEMM index 0 .. 4L-1, then 4L for the lm-head
+  int u, u1, KT;
+  int t, ks;   // lm-head tile / 64-column step
+  __device__ void start_gemm() {
+    const int G = gridDim.x, c = blockIdx.x;
+    const StepW8& w = gemm_w();
+    KT = w.K / kTile;
+    const int units = (w.N / kTile) * KT;
+    u = unit_lo(c, units, G);
+    u1 = unit_lo(c + 1, units, G);
+  }
+  __device__ const StepW8& gemm_w() const {
+    const int l = gi >> 2, k = gi & 3;
+    return k == 0 ? a->qkv[l] : (k == 1 ? a->o[l] : (k == 2 ? a->gu[l] : a->down[l]));
+  }
+  __device__ void init(const StepArgs* args) {
+    a = args;
+    gi = 0;
+    t = blockIdx.x;
+    ks = 0;
+    start_gemm();
+  }
+  __device__ bool next(StageRef& r) {
+    const int m = a->nsa > 1 ? 1 : 0, nbl = 7 + m;
+    while (gi < 4 * a->L) {
+      if (u < u1) {
+        const StepW8& w = gemm_w();
+        const int l = gi >> 2, k = gi & 3;
+        const int base = 1 + l * nbl;
+        const int tt = u / KT, kt = u - tt * KT;
+        r.kind = 0;
+        r.wsrc = w.q + ((size_t)tt * KT + kt) * kTileBytes;
+        r.wx = r.wy = 0;
+        r.amap = k == 1 ? 1 : (k == 3 ? 2 : 0);
+        r.ax = kt * kTile;
+        r.ready = k == 0 ? base : (k == 1 ? base + 2 + m : (k == 2 ? base + 4 + m : base + 5 + m));
+        r.wready = k == 1 ? base + 2 : 0;
+        ++u;
+        return true;
+      }
+      ++gi;
+      if (gi < 4 * a->L) start_gemm();
+    }
+    const int ntv = (a->V + 127) / 128, KS = a->H / 64;
+    if (t >= ntv) return false;
+    r.kind = 1;
+    r.wsrc = nullptr;
+    r.wx = ks * 64;
+    r.wy = t * 128;
+    r.amap = 3;
+    r.ax = ks * 64;
+    r.ready = 1 + a->L * nbl;
+    r.wready = 0;
+    if (++ks == KS) {
+      ks = 0;
+      t += gridDim.x;
     }
     return true;
-  };
-  for (int l = 0; l < a.L; ++l) {
-    const int base = 1 + l * nbl;
-    if (!gemm(a.qkv[l], 0, base)) return;
-    if (!gemm(a.o[l], 1, base + 2 + m)) return;
-    if (!gemm(a.gu[l], 0, base + 4 + m)) return;
-    if (!gemm(a.down[l], 2, base + 5 + m)) return;
   }
-  const int ntv = (a.V + 127) / 128, KS = a.H / 64, ready = 1 + a.L * nbl;
-  for (int t = c; t < ntv; t += G)
-    for (int ks = 0; ks < KS; ++ks) {
-      StageRef r{1, nullptr, ks * 64, t * 128, 3, ks * 64, ready};
-      if (!f(r)) return;
-    }
-}
+};
 
 __device__ __forceinline__ const CUtensorMap* act_map(const StepMaps& mp, int i) {
   return i == 0 ? &mp.u : (i == 1 ? &mp.ao : (i == 2 ? &mp.g : &mp.h));
 }
 
-// Loader warp (one thread): fills the shared ring stage by stage.
+// Loader warp (one thread).  Each ring stage completes on two arrivals: the
+// weight tile, issued as soon as the slot is free (weights never depend on
+// activations, so they stream ahead through phase boundaries), and the
+// activation slice, issued once the grid barriers its phase needs are done.
 __device__ void loader(const StepArgs& a, const StepMaps& mp, Smem& S, int mch) {
   const uint64_t pol = policy_evict_first();
-  const int sb = kStage + 2 * mch * 128;  // stage stride
-  uint32_t gl = 0;
+  const int sb = kStage + 2 * mch * 128;
+  const int RS = a.ring_stages;
+  StageIter iw, ia;
+  iw.init(&a);
+  ia.init(&a);
+  StageRef rw, ra;
+  bool hw = iw.next(rw), ha = ia.next(ra);
+  uint32_t gw = 0, ga = 0, idle = 0;
   int seen = 0;
-  for_each_stage(a, [&](const StageRef& r) -> bool {
-    if (seen < r.ready) {
-      uint32_t i = 0;
-      while ((seen = ld_acquire_smem(S.misc + kMiscPhase)) < r.ready) {
-        if (++i > (1u << 28)) {
-          atomicOr(a.status, kDevWaitTimeout);
-          return false;
-        }
+  while (hw || ha) {
+    bool progress = false;
+    if (ha && ga < gw) {
+      if (seen < ra.ready) {
+        seen = ld_acquire_smem(S.misc + kMiscPhase);
+        if (seen >= ra.ready) fence_proxy_async_global();
       }
-      fence_proxy_async_global();
+      if (seen >= ra.ready) {
+        const int slot = (int)(ga % (uint32_t)RS);
+        uint8_t* st = S.ring + (size_t)slot * sb + kStage;
+        const CUtensorMap* am = act_map(mp, ra.amap);
+        if (ra.kind == 0) {
+          mbar_arrive_expect_tx(&S.full[slot], 2 * mch * 128);
+          tma_load_2d(st, am, ra.ax, 0, &S.full[slot]);
+          tma_load_2d(st + mch * 128, am, ra.ax + 64, 0, &S.full[slot]);
+        } else {
+          mbar_arrive_expect_tx(&S.full[slot], mch * 128);
+          tma_load_2d(st, am, ra.ax, 0, &S.full[slot]);
+        }
+        ++ga;
+        ha = ia.next(ra);
+        progress = true;
+      }
     }
-    const int slot = (int)(gl % (uint32_t)a.ring_stages);
-    if (gl >= (uint32_t)a.ring_stages && !mbar_wait(&S.empty[slot], ((gl / a.ring_stages) - 1) & 1, a.status))
-      return false;
-    uint8_t* st = S.ring + (size_t)slot * sb;
-    const CUtensorMap* am = act_map(mp, r.amap);
-    if (r.kind == 0) {
-      mbar_arrive_expect_tx(&S.full[slot], kStage + 2 * mch * 128);
-      bulk_g2s_hint(st, r.wsrc, kStage, &S.full[slot], pol);
-      tma_load_2d(st + kStage, am, r.ax, 0, &S.full[slot]);
-      tma_load_2d(st + kStage + mch * 128, am, r.ax + 64, 0, &S.full[slot]);
-    } else {
-      mbar_arrive_expect_tx(&S.full[slot], kStage + mch * 128);
-      tma_load_2d_hint(st, &mp.lm, r.wx, r.wy, &S.full[slot], pol);
-      tma_load_2d(st + kStage, am, r.ax, 0, &S.full[slot]);
+    if (hw && seen < rw.wready) seen = ld_acquire_smem(S.misc + kMiscPhase);
+    if (hw && seen >= rw.wready) {
+      const int slot = (int)(gw % (uint32_t)RS);
+      if (gw < (uint32_t)RS || mbar_try_wait(&S.empty[slot], ((gw / RS) - 1) & 1)) {
+        uint8_t* st = S.ring + (size_t)slot * sb;
+        mbar_arrive_expect_tx(&S.full[slot], kStage);
+        if (rw.kind == 0) bulk_g2s_hint(st, rw.wsrc, kStage, &S.full[slot], pol);
+        else tma_load_2d_hint(st, &mp.lm, rw.wx, rw.wy, &S.full[slot], pol);
+        ++gw;
+        hw = iw.next(rw);
+        progress = true;
+      }
     }
-    ++gl;
-    return true;
-  });
+    if (progress) {
+      idle = 0;
+    } else if (++idle > (1u << 28)) {
+      atomicOr(a.status, kDevWaitTimeout);
+      return;
+    }
+  }
 }
 
 // ----------------------------------------------------------- consumers ----
@@ -264,21 +327,19 @@ enum { EP_QKV = 0, EP_RESID = 1, EP_SWIGLU = 2 };
 
 // Fused epilogue on the reduced, unscaled tile T[tok][kTS] of row tile t.
 template <int MT>
-__device__ void step_epilogue(Cons& C, int ep, const StepW8& w, int t, const float* T, const float* gq,
-                              const float* gk) {
+__device__ void step_epilogue(Cons& C, int ep, const StepW8& w, int t, const float* T, int mlo, int mhi) {
   const StepArgs& a = C.a;
   const int tid = threadIdx.x;
-  const int M = a.M;
   const float* sc = C.S.sc;
   if (ep == EP_RESID) {
-    const int items = M * 32;
+    const int items = (mhi - mlo) * 32;
     for (int base = tid; base < items; base += 2 * kCT) {
       float4 xo[2];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int it = base + u * kCT;
         if (it < items) {
-          const int m = it >> 5, r = 4 * (it & 31);
+          const int m = mlo + (it >> 5), r = 4 * (it & 31);
           xo[u] = __ldcg(reinterpret_cast<const float4*>(a.x + (size_t)m * a.H + t * kTile + r));
         }
       }
@@ -286,7 +347,7 @@ __device__ void step_epilogue(Cons& C, int ep, const StepW8& w, int t, const flo
       for (int u = 0; u < 2; ++u) {
         const int it = base + u * kCT;
         if (it >= items) continue;
-        const int m = it >> 5, r = 4 * (it & 31);
+        const int m = mlo + (it >> 5), r = 4 * (it & 31);
         const float* tt = T + m * kTS + r;
         float4 v = make_float4(tt[0] * sc[r] + xo[u].x, tt[1] * sc[r + 1] + xo[u].y, tt[2] * sc[r + 2] + xo[u].z,
                                tt[3] * sc[r + 3] + xo[u].w);
@@ -297,8 +358,8 @@ __device__ void step_epilogue(Cons& C, int ep, const StepW8& w, int t, const flo
   }
   if (ep == EP_SWIGLU) {
     const int F = a.F;
-    for (int it = tid; it < M * 16; it += kCT) {
-      const int m = it >> 4, r = 4 * (it & 15);
+    for (int it = tid; it < (mhi - mlo) * 16; it += kCT) {
+      const int m = mlo + (it >> 4), r = 4 * (it & 15);
       const float* tt = T + m * kTS;
       float g[4];
 #pragma unroll
@@ -321,7 +382,7 @@ __device__ void step_epilogue(Cons& C, int ep, const StepW8& w, int t, const flo
   const int kind = prow0 < qd ? 0 : (prow0 < qd + kd ? 1 : 2);
   const float* gam = C.S.gam;
   const int lane = C.lane;
-  for (int m = C.warp; m < M; m += kNC) {
+  for (int m = mlo + C.warp; m < mhi; m += kNC) {
     const int p = C.S.misc[32 + m];
     float v[4];
 #pragma unroll
@@ -361,11 +422,32 @@ __device__ void step_epilogue(Cons& C, int ep, const StepW8& w, int t, const flo
       else a.vb[(size_t)m * kd + (row - qd - kd)] = hv;
     }
   }
-  (void)gq;
-  (void)gk;
 }
 
 // A W8A16 GEMM phase: activations act[M][K] fp16, weights w, epilogue ep.
+// Row-tile scales (and the Q/K gamma) for the epilogue, into shared memory.
+__device__ __forceinline__ void load_tile_side(Cons& C, const StepW8& w, int t, int ep, const float* gq,
+                                               const float* gk) {
+  if (threadIdx.x < 128) {
+    const int prow = t * kTile + threadIdx.x;
+    int lrow = prow;
+    if (w.layout == 1) {
+      const int tl = prow >> 7, rr = prow & 127;
+      lrow = rr < 64 ? tl * 64 + rr : (w.N >> 1) + tl * 64 + (rr - 64);
+    }
+    C.S.sc[threadIdx.x] = __half2float(w.s[lrow]);
+    if (ep == EP_QKV) {
+      const float* gsrc = t * kTile < C.a.nq * C.a.d ? gq : gk;
+      C.S.gam[threadIdx.x] = threadIdx.x < C.a.d ? gsrc[threadIdx.x] : 1.f;
+    }
+  }
+}
+
+// A W8A16 GEMM phase: stream-K over (row tile, k-tile) units.  A row tile
+// held whole by this CTA is finished at once; a shared tile's partial is
+// written without waiting, and at the end of the phase every contributor
+// waits (bounded) for the tile's other partials and sums and finishes its
+// own slice of activation rows, in contributor order (deterministic).
 template <int MT>
 __device__ void gemm_phase(Cons& C, const StepW8& w, int ep, const float* gq, const float* gk) {
   const StepArgs& a = C.a;
@@ -373,24 +455,16 @@ __device__ void gemm_phase(Cons& C, const StepW8& w, int ep, const float* gq, co
   const int KT = w.K / kTile, ntiles = w.N / kTile, units = ntiles * KT;
   const int u0 = unit_lo(c, units, G), u1 = unit_lo(c + 1, units, G);
   const int g8 = C.lane >> 2, t4 = C.lane & 3;
+  const int mch = C.geo.mch;
+  float* T = reinterpret_cast<float*>(C.S.x);
+  int nsplit = 0, sp_t[4], sp_rank[4], sp_ns[4];
   int u = u0;
   while (u < u1) {
     const int t = u / KT, kt0 = u - t * KT;
     const int n = min(KT - kt0, u1 - u);
-    // weight-side epilogue data for this row tile
-    if (threadIdx.x < 128) {
-      const int prow = t * kTile + threadIdx.x;
-      int lrow = prow;
-      if (w.layout == 1) {
-        const int tl = prow >> 7, rr = prow & 127;
-        lrow = rr < 64 ? tl * 64 + rr : (w.N >> 1) + tl * 64 + (rr - 64);
-      }
-      C.S.sc[threadIdx.x] = __half2float(w.s[lrow]);
-      if (ep == EP_QKV) {
-        const float* gsrc = t * kTile < a.nq * a.d ? gq : gk;
-        C.S.gam[threadIdx.x] = threadIdx.x < a.d ? gsrc[threadIdx.x] : 1.f;
-      }
-    }
+    int ns, rank;
+    tile_contrib(t, KT, units, G, c, ns, rank);
+    if (ns == 1) load_tile_side(C, w, t, ep, gq, gk);
     float acc[2][MT][4];
 #pragma unroll
     for (int x = 0; x < 2; ++x)
@@ -398,7 +472,7 @@ __device__ void gemm_phase(Cons& C, const StepW8& w, int ep, const float* gq, co
       for (int j = 0; j < MT; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[x][j][e] = 0.f;
-    const int sb = kStage + 2 * C.geo.mch * 128;
+    const int sb = kStage + 2 * mch * 128;
     for (int i = 0; i < n; ++i) {
       const int slot = (int)(C.gc % (uint32_t)a.ring_stages);
       mbar_wait(&C.S.full[slot], (C.gc / a.ring_stages) & 1, a.status);
@@ -408,12 +482,8 @@ __device__ void gemm_phase(Cons& C, const StepW8& w, int ep, const float* gq, co
       if (C.lane == 0) mbar_arrive(&C.S.empty[slot]);
       ++C.gc;
     }
-    // ---- segment end: partial or epilogue ----
-    cbar();  // every warp is done with the segment's stages and epilogue data
-    int ns, slotp;
-    tile_contrib(t, KT, units, G, c, ns, slotp);
-    float* T = reinterpret_cast<float*>(C.S.x);
     if (ns == 1) {
+      cbar();
 #pragma unroll
       for (int x = 0; x < 2; ++x)
 #pragma unroll
@@ -422,11 +492,10 @@ __device__ void gemm_phase(Cons& C, const StepW8& w, int ep, const float* gq, co
           for (int e = 0; e < 4; ++e)
             T[(j * 8 + 2 * t4 + (e & 1)) * kTS + C.warp * 32 + x * 16 + g8 + ((e >> 1) << 3)] = acc[x][j][e];
       cbar();
-      step_epilogue<MT>(C, ep, w, t, T, gq, gk);
+      step_epilogue<MT>(C, ep, w, t, T, 0, a.M);
       cbar();
     } else {
-      const int mch = C.geo.mch;
-      float* P = a.part + ((size_t)t * a.nslots + slotp) * mch * kTile;
+      float* P = a.part + ((size_t)t * a.nslots + rank) * mch * kTile;
 #pragma unroll
       for (int x = 0; x < 2; ++x)
 #pragma unroll
@@ -436,43 +505,69 @@ __device__ void gemm_phase(Cons& C, const StepW8& w, int ep, const float* gq, co
             P[(j * 8 + 2 * t4 + (e & 1)) * kTile + C.warp * 32 + x * 16 + g8 + ((e >> 1) << 3)] = acc[x][j][e];
       __threadfence();
       cbar();
-      if (threadIdx.x == 0) {
-        const int old = atomicAdd(&a.tickets[t], 1);
-        C.S.misc[0] = old == ns - 1;
+      if (threadIdx.x == 0) atomicAdd(&a.tickets[t], 1);
+      if (nsplit < 4) {
+        sp_t[nsplit] = t;
+        sp_rank[nsplit] = rank;
+        sp_ns[nsplit] = ns;
+        ++nsplit;
       }
-      cbar();
-      if (C.S.misc[0]) {
-        __threadfence();
-        const float* P0 = a.part + (size_t)t * a.nslots * mch * kTile;
-        const int items = a.M * 32;  // float4 items of the live rows
-        for (int it = threadIdx.x; it < items; it += kCT) {
-          const int m = it >> 5, c4 = it & 31;
-          const float4* src = reinterpret_cast<const float4*>(P0 + m * kTile) + c4;
-          float4 s = __ldcg(src);
-          int q = 1;
-          for (; q + 3 < ns; q += 4) {
-            float4 v0 = __ldcg(src + (size_t)(q + 0) * mch * 32);
-            float4 v1 = __ldcg(src + (size_t)(q + 1) * mch * 32);
-            float4 v2 = __ldcg(src + (size_t)(q + 2) * mch * 32);
-            float4 v3 = __ldcg(src + (size_t)(q + 3) * mch * 32);
-            s.x += v0.x; s.y += v0.y; s.z += v0.z; s.w += v0.w;
-            s.x += v1.x; s.y += v1.y; s.z += v1.z; s.w += v1.w;
-            s.x += v2.x; s.y += v2.y; s.z += v2.z; s.w += v2.w;
-            s.x += v3.x; s.y += v3.y; s.z += v3.z; s.w += v3.w;
-          }
-          for (; q < ns; ++q) {
-            float4 v0 = __ldcg(src + (size_t)q * mch * 32);
-            s.x += v0.x; s.y += v0.y; s.z += v0.z; s.w += v0.w;
-          }
-          *reinterpret_cast<float4*>(T + m * kTS + 4 * c4) = s;
-        }
-        cbar();
-        step_epilogue<MT>(C, ep, w, t, T, gq, gk);
-        if (threadIdx.x == 0) a.tickets[t] = 0;
-      }
-      cbar();
     }
     u += n;
+  }
+  // finish this CTA's slices of its shared tiles, last segment first (its
+  // other contributors start that tile first, so it completes earliest)
+  for (int q = nsplit - 1; q >= 0; --q) {
+    const int t = sp_t[q], rank = sp_rank[q], ns = sp_ns[q];
+    const int mlo = (rank * a.M) / ns, mhi = ((rank + 1) * a.M) / ns;
+    load_tile_side(C, w, t, ep, gq, gk);
+    if (threadIdx.x == 0) {
+      uint32_t i = 0;
+      while ((int)ld_acquire_u32(reinterpret_cast<const unsigned*>(a.tickets + t)) < ns) {
+        if (++i > (1u << 26)) {
+          atomicOr(a.status, kDevWaitTimeout);
+          break;
+        }
+      }
+      __threadfence();
+    }
+    cbar();
+    if (mlo < mhi) {
+      const float* P0 = a.part + (size_t)t * a.nslots * mch * kTile;
+      const int items = (mhi - mlo) * 32;
+      for (int it = threadIdx.x; it < items; it += kCT) {
+        const int m = mlo + (it >> 5), c4 = it & 31;
+        const float4* src = reinterpret_cast<const float4*>(P0 + m * kTile) + c4;
+        float4 sacc = __ldcg(src);
+        int k = 1;
+        for (; k + 3 < ns; k += 4) {
+          const float4 v0 = __ldcg(src + (size_t)(k + 0) * mch * 32);
+          const float4 v1 = __ldcg(src + (size_t)(k + 1) * mch * 32);
+          const float4 v2 = __ldcg(src + (size_t)(k + 2) * mch * 32);
+          const float4 v3 = __ldcg(src + (size_t)(k + 3) * mch * 32);
+          sacc.x += v0.x; sacc.y += v0.y; sacc.z += v0.z; sacc.w += v0.w;
+          sacc.x += v1.x; sacc.y += v1.y; sacc.z += v1.z; sacc.w += v1.w;
+          sacc.x += v2.x; sacc.y += v2.y; sacc.z += v2.z; sacc.w += v2.w;
+          sacc.x += v3.x; sacc.y += v3.y; sacc.z += v3.z; sacc.w += v3.w;
+        }
+        for (; k < ns; ++k) {
+          const float4 v0 = __ldcg(src + (size_t)k * mch * 32);
+          sacc.x += v0.x; sacc.y += v0.y; sacc.z += v0.z; sacc.w += v0.w;
+        }
+        *reinterpret_cast<float4*>(T + m * kTS + 4 * c4) = sacc;
+      }
+      cbar();
+      step_epilogue<MT>(C, ep, w, t, T, mlo, mhi);
+    }
+    cbar();
+    if (threadIdx.x == 0) {
+      // the last contributor to finish resets the tile's counters
+      const int d = atomicAdd(&a.tickets[a.ntmax + t], 1);
+      if (d == ns - 1) {
+        a.tickets[t] = 0;
+        a.tickets[a.ntmax + t] = 0;
+      }
+    }
   }
 }
 
@@ -1001,7 +1096,7 @@ __global__ void __launch_bounds__(kThr, 2) draft_step_kernel(const __grid_consta
   S.gam = S.sc + 128;
   if (threadIdx.x == 0) {
     for (int i = 0; i < a.ring_stages; ++i) {
-      mbar_init(&S.full[i], 1);
+      mbar_init(&S.full[i], 2);  // weight arrival + activation arrival
       mbar_init(&S.empty[i], kNC);
     }
     for (int i = 0; i < 64; ++i) S.misc[i] = 0;

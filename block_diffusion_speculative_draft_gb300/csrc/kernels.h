@@ -110,6 +110,7 @@ struct StepArgs {
   int nslots;       // partial slots per row tile
   int xbytes;       // epilogue / reduction region bytes
   int attn_kt;      // attention key tile (64 or 32)
+  int ntmax;        // row tiles of the widest projection (counter stride)
   float eps;
   double inv_freq[64];
   StepW8 qkv[8], o[8], gu[8], down[8];
