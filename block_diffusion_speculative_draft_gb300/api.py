@@ -25,7 +25,7 @@ DEV_KV_CAPACITY, DEV_BAD_TOKEN, DEV_BAD_LENGTH, DEV_WAIT_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTS = [
     "dflash_version", "dflash_status_string", "dflash_workspace_size", "dflash_pack_w8a16",
-    "dflash_w8a16_linear_workspace_size", "dflash_w8a16_linear", "dflash_draft_block",
+    "dflash_w8a16_linear_workspace_size", "dflash_w8a16_linear", "dflash_draft_block", "dflash_draft_block_fused",
     "dflash_lmhead_workspace_size", "dflash_lmhead_argmax", "dflash_verify_workspace_size",
     "dflash_verify_accept", "dflash_verify_accept_noalloc", "dflash_kv_commit", "dflash_get_status",
 ]
@@ -84,6 +84,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dflash_w8a16_linear_workspace_size": ([I64, I64, I64, PSZ], I32),
         "dflash_w8a16_linear": ([ctypes.POINTER(W8), P, I64, P, P, SZ, P], I32),
         "dflash_draft_block": ([ctypes.POINTER(Weights), ctypes.POINTER(KV), P, P, P, P, P, SZ, P], I32),
+        "dflash_draft_block_fused": ([ctypes.POINTER(Weights), ctypes.POINTER(KV), P, P, P, P, P, SZ, P], I32),
         "dflash_lmhead_workspace_size": ([I64, PSZ], I32),
         "dflash_lmhead_argmax": ([P, P, I64, I64, I64, P, P, P, P, SZ, P], I32),
         "dflash_verify_workspace_size": ([I32, I32, I64, PSZ], I32),
@@ -218,6 +219,14 @@ def dflash_verify_accept_noalloc(logits, draft, n_out, corr_out, emitted=None, n
 def dflash_draft_block(model: "DeviceDrafter", kv: "KVCache", last_tok, draft_out, ws, hidden=None, logits=None,
                        stream=None):
     _check("dflash_draft_block", load_library().dflash_draft_block(
+        ctypes.byref(model.c), ctypes.byref(kv.c), last_tok.data_ptr(), draft_out.data_ptr(), _ptr(hidden),
+        _ptr(logits), ws.data_ptr(), ws.numel(), _stream(stream)))
+
+
+def dflash_draft_block_fused(model: "DeviceDrafter", kv: "KVCache", last_tok, draft_out, ws, hidden=None,
+                             logits=None, stream=None):
+    """The draft step as one persistent cooperative kernel (b * B <= 32)."""
+    _check("dflash_draft_block_fused", load_library().dflash_draft_block_fused(
         ctypes.byref(model.c), ctypes.byref(kv.c), last_tok.data_ptr(), draft_out.data_ptr(), _ptr(hidden),
         _ptr(logits), ws.data_ptr(), ws.numel(), _stream(stream)))
 

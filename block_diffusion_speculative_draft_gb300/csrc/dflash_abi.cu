@@ -261,8 +261,9 @@ static int check_kv(const dflash_kv* kv) {
   return DFLASH_OK;
 }
 
-int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const int32_t* last_tok, int32_t* draft_out,
-                           float* hidden_out, float* logits_out, void* ws, size_t ws_bytes, void* stream) {
+static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, const int32_t* last_tok,
+                                int32_t* draft_out, float* hidden_out, float* logits_out, void* ws, size_t ws_bytes,
+                                void* stream, bool fused) {
   if (int r = check_weights(w)) return r;
   if (int r = check_kv(kv)) return r;
   if (!last_tok || !draft_out) return DFLASH_EINVAL;
@@ -280,7 +281,8 @@ int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const i
   const int qd = c.nq * c.d, kd = c.nkv * c.d;
   const size_t layer_kv = (size_t)b * c.nkv * kv->cap * c.d;
   cudaError_t e;
-  if (M <= step_max_mch() && c.L <= 8) {
+  if (fused) {
+    if (M > step_max_mch() || c.L > 8) return DFLASH_EUNSUPPORTED;
     // the whole step as one persistent kernel when it fits
     const DevInfo di = dev_info();
     const int mt = M <= 16 ? 2 : 4;
@@ -375,6 +377,7 @@ int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const i
       a.status = status;
       return map_err(draft_step(a, reinterpret_cast<const __nv_bfloat16*>(w->lm_head), st, G));
     }
+    return DFLASH_EUNSUPPORTED;
   }
   e = embed_rmsnorm(reinterpret_cast<const __nv_bfloat16*>(w->embed), last_tok, c.mask_id, c.V, b, c.B, c.H,
                     w->gamma_in, c.eps, s.x, s.u, st, false, status);
@@ -443,6 +446,17 @@ int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const i
   e = lmhead_argmax(s.h, reinterpret_cast<const __nv_bfloat16*>(w->lm_head), b * (c.B - 1), c.V, c.H, draft_out,
                     nullptr, logits_out, s.lm, st, true, status);
   return map_err(e);
+}
+
+int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const int32_t* last_tok, int32_t* draft_out,
+                           float* hidden_out, float* logits_out, void* ws, size_t ws_bytes, void* stream) {
+  return draft_block_impl(w, kv, last_tok, draft_out, hidden_out, logits_out, ws, ws_bytes, stream, false);
+}
+
+int32_t dflash_draft_block_fused(const dflash_weights* w, const dflash_kv* kv, const int32_t* last_tok,
+                                 int32_t* draft_out, float* hidden_out, float* logits_out, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  return draft_block_impl(w, kv, last_tok, draft_out, hidden_out, logits_out, ws, ws_bytes, stream, true);
 }
 
 int32_t dflash_lmhead_workspace_size(int64_t M, size_t* bytes) {

@@ -234,15 +234,18 @@ __device__ void loader(const StepArgs& a, const StepMaps& mp, Smem& S, int mch) 
   StageRef rw, ra;
   bool hw = iw.next(rw), ha = ia.next(ra);
   uint32_t gw = 0, ga = 0, idle = 0;
-  int seen = 0;
+  int seen_a = 0, seen_w = 0;  // barriers observed by each cursor
   while (hw || ha) {
     bool progress = false;
     if (ha && ga < gw) {
-      if (seen < ra.ready) {
-        seen = ld_acquire_smem(S.misc + kMiscPhase);
-        if (seen >= ra.ready) fence_proxy_async_global();
+      if (seen_a < ra.ready) {
+        const int now = ld_acquire_smem(S.misc + kMiscPhase);
+        // activation data written before these barriers is read through the
+        // async proxy next: order it after the generic-proxy writes
+        if (now > seen_a) fence_proxy_async_global();
+        seen_a = now;
       }
-      if (seen >= ra.ready) {
+      if (seen_a >= ra.ready) {
         const int slot = (int)(ga % (uint32_t)RS);
         uint8_t* st = S.ring + (size_t)slot * sb + kStage;
         const CUtensorMap* am = act_map(mp, ra.amap);
@@ -259,8 +262,8 @@ __device__ void loader(const StepArgs& a, const StepMaps& mp, Smem& S, int mch) 
         progress = true;
       }
     }
-    if (hw && seen < rw.wready) seen = ld_acquire_smem(S.misc + kMiscPhase);
-    if (hw && seen >= rw.wready) {
+    if (hw && seen_w < rw.wready) seen_w = ld_acquire_smem(S.misc + kMiscPhase);
+    if (hw && seen_w >= rw.wready) {
       const int slot = (int)(gw % (uint32_t)RS);
       if (gw < (uint32_t)RS || mbar_try_wait(&S.empty[slot], ((gw / RS) - 1) & 1)) {
         uint8_t* st = S.ring + (size_t)slot * sb;

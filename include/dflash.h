@@ -198,6 +198,21 @@ DFLASH_API int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* 
                            float* hidden_out, float* logits_out, void* ws,
                            size_t ws_bytes, void* stream);
 
+/* The same draft step as dflash_draft_block, computed by ONE persistent
+ * cooperative kernel (all phases of the step inside one launch, two CTAs per
+ * SM, weights streamed through a shared-memory ring across phase boundaries,
+ * grid barriers between dependent phases).  Same arguments, results within
+ * the same tolerances.  Requires b * B <= 32 and L <= 8; otherwise, or when
+ * the device cannot hold two such CTAs per SM, returns DFLASH_EUNSUPPORTED.
+ * Uses the same workspace as dflash_draft_block. */
+DFLASH_API int32_t dflash_draft_block_fused(const dflash_weights* w,
+                                           const dflash_kv* kv,
+                                           const int32_t* last_tok,
+                                           int32_t* draft_out,
+                                           float* hidden_out,
+                                           float* logits_out, void* ws,
+                                           size_t ws_bytes, void* stream);
+
 /* Workspace bytes for dflash_lmhead_argmax with M rows. */
 DFLASH_API int32_t dflash_lmhead_workspace_size(int64_t M, size_t* bytes);
 
