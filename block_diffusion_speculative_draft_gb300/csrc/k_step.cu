@@ -25,8 +25,8 @@
 //    bounded spin); the launch is cooperative, so all CTAs are co-resident.
 // Data written by other CTAs inside the kernel is read with L1-bypassing
 // loads (cp.async.cg, ld.global.cg) after the grid barrier's acquire.
-// Attention reuses the ring as scratch: the loader holds back each layer's
-// o-projection tiles until that layer's attention phase has ended.
+// Attention reuses the ring as scratch: the loader holds back every weight
+// tile scheduled after a layer's attention until that attention has ended.
 // Only the activation rows M = b * B <= 32 path uses this kernel.
 #include "kernels.h"
 #include "ptx.cuh"
@@ -191,7 +191,8 @@ struct StageIter {
         r.amap = k == 1 ? 1 : (k == 3 ? 2 : 0);
         r.ax = kt * kTile;
         r.ready = k == 0 ? base : (k == 1 ? base + 2 + m : (k == 2 ? base + 4 + m : base + 5 + m));
-        r.wready = k == 1 ? base + 2 : 0;
+        // every stage scheduled after an attention phase waits for its end
+        r.wready = k >= 1 ? base + 2 : (l > 0 ? base - nbl + 2 : 0);
         ++u;
         return true;
       }
@@ -207,7 +208,7 @@ struct StageIter {
     r.amap = 3;
     r.ax = ks * 64;
     r.ready = 1 + a->L * nbl;
-    r.wready = 0;
+    r.wready = 1 + (a->L - 1) * nbl + 2;
     if (++ks == KS) {
       ks = 0;
       t += gridDim.x;

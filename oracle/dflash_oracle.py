@@ -149,15 +149,18 @@ class Drafter:
     (qkv rows: q heads | k heads | v heads; gu rows: gate F | up F) and to
     arrays for gammas and the bf16 embedding / lm-head bit patterns."""
 
-    def __init__(self, cfg, W: Dict[str, object]):
-        self.cfg, self.W = cfg, W
+    def __init__(self, cfg, W: Dict[str, object], cache: bool = True):
+        self.cfg, self.W, self.cache = cfg, W, cache
         self._cache: Dict[str, np.ndarray] = {}
 
     def w(self, name: str) -> np.ndarray:
-        if name not in self._cache:
-            q, s = self.W[name]
-            self._cache[name] = dequant_w8(q, s)
-        return self._cache[name]
+        if name in self._cache:
+            return self._cache[name]
+        q, s = self.W[name]
+        w = dequant_w8(q, s)
+        if self.cache:
+            self._cache[name] = w
+        return w
 
     def drop(self):
         self._cache.clear()
