@@ -248,6 +248,14 @@ def run_ours(args, rank, world, local_rank):
 
     g_step = capture(step)
     g_draft = capture(draft_only)
+    g_fused = None
+    if cfg.M <= 32:
+        try:
+            api.dflash_draft_block_fused(model, kv, t0, draft, ws)
+            torch.cuda.synchronize()
+            g_fused = capture(lambda: api.dflash_draft_block_fused(model, kv, t0, draft, ws))
+        except api.DflashError:
+            g_fused = None
     VREP = 100
     g_verify = capture(lambda: api.dflash_verify_accept(logits, draft, n_out, corr, emitted, nxt, vws), VREP)
     M1 = b * (cfg.B - 1)
@@ -281,6 +289,7 @@ def run_ours(args, rank, world, local_rank):
         total_ms, per_ms = timed(g_step, K, Wm)
     clocks = clk.summary()
     _, draft_ms = timed(g_draft, K, Wm)
+    fused_ms = timed(g_fused, K, Wm)[1] if g_fused is not None else None
     _, ver_ms = timed(g_verify, max(3, K // 5), 2)
     _, lm_ms = timed(g_lm, K, Wm)
     assert api.dflash_get_status() == 0, "device status flagged during the timed region"
@@ -343,6 +352,7 @@ def run_ours(args, rank, world, local_rank):
         "draft_step_us": {"median": dms * 1e3, "p10": float(np.percentile(draft_ms, 10)) * 1e3,
                           "p90": float(np.percentile(draft_ms, 90)) * 1e3},
         "draft_step_weight_GBps": step_bytes / (dms * 1e-3) / 1e9,
+        "draft_step_fused_kernel_us": None if fused_ms is None else statistics.median(fused_ms) * 1e3,
         "step_roofline": {"bytes": step_bytes, "frac_of_measured": step_bytes / (dms * 1e-3) / 1e9 / hbm,
                           "frac_of_8TBps": step_bytes / (dms * 1e-3) / 1e9 / 8000.0},
         "verify_accept_blocks_per_s": b / (statistics.median(ver_ms) / VREP / 1e3),
