@@ -116,9 +116,11 @@ class ClockSampler:
 
 
 def launches_per_step(cfg) -> int:
-    draft = 7 * cfg.L + 2      # embed, per layer qkv/attn/o/norm/gu/down(+norm), final norm, lm-head
+    # draft: embed+norm, per layer qkv/attn/o/gu/down (the RMSNorms between
+    # them are applied inside the GEMM epilogues), final norm, lm-head
+    draft = 5 * cfg.L + 3
     verify = 1
-    commit = cfg.L + 3         # fc, norm, per-layer K/V, length update
+    commit = cfg.L + 2         # fc, per-layer K/V, length update
     return draft + verify + commit
 
 

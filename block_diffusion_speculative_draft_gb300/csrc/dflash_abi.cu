@@ -76,7 +76,7 @@ struct WS {
   __half* ao;
   __half* g;
   __nv_bfloat16* h;
-  float* y;
+  float* ss;  // per-row, per-128-column sums of squares of x (deferred RMSNorm)
   void* lm;
   // fused-step kernel
   int* stick;
@@ -138,7 +138,7 @@ WS carve(const dflash_config& c, int b, int rps, uint8_t* base) {
   w.ao = (__half*)take((size_t)M * c.nq * c.d * 2);
   w.g = (__half*)take((size_t)M * c.F * 2);
   w.h = (__nv_bfloat16*)take((size_t)b * (c.B - 1) * c.H * 2);
-  w.y = (float*)take((size_t)Mc * c.H * 4);
+  w.ss = (float*)take((size_t)Mx * (c.H / 128) * 4);
   w.spart_bytes = step ? (size_t)step_ntiles_max(c) * step_nslots_for(c, 2 * kNumSMs) * 32 * 128 * sizeof(float) : 0;
   w.spart = (float*)take(w.spart_bytes);
   const size_t na = step ? (size_t)b * c.nkv * kStepMaxSplits * step_rows_pad(c) : 0;
@@ -400,6 +400,10 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
     a.rows_per_seq = c.B;
     a.b = b;
     a.cap = kv->cap;
+    if (l > 0) {  // layer 0 reads the embedding, normalised by its own kernel
+      a.ss_in = s.ss;
+      a.nss_in = c.H / 128;
+    }
     if ((e = w8_gemm(a, s.u, st, true)) != cudaSuccess) return DFLASH_ECUDA;
     // block attention over [context || block]
     AttnArgs at;
@@ -419,25 +423,36 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
     at.status = status;
     if ((e = attention(at, st, true)) != cudaSuccess) return DFLASH_ECUDA;
     // x += W8(o) attn
+    // x += W8(o) attn; the epilogue also leaves u = x * gamma_post and the
+    // row sums of squares, so the post-attention RMSNorm is applied by the
+    // next GEMM's epilogue (RMSNorm is a per-row scale, which commutes with
+    // the contraction)
     W8Args ao = base_args(w->o[l], M, EPI_RESID_F32);
     ao.out_f32 = s.x;
     ao.ldo = c.H;
+    ao.xg_out = s.u;
+    ao.g_next = w->gamma_post + (size_t)l * c.H;
+    ao.ss_out = s.ss;
+    ao.nss_out = c.H / 128;
     if ((e = w8_gemm(ao, s.ao, st, true)) != cudaSuccess) return DFLASH_ECUDA;
-    if ((e = rmsnorm_f16(s.x, M, c.H, w->gamma_post + (size_t)l * c.H, c.eps, s.u, st, true)) != cudaSuccess)
-      return DFLASH_ECUDA;
-    // g = silu(gate) * up
+    // g = silu(gate) * up, gate/up scaled by the deferred norm factor
     W8Args ag = base_args(w->gu[l], M, EPI_SWIGLU);
     ag.out_h = s.g;
+    ag.ss_in = s.ss;
+    ag.nss_in = c.H / 128;
+    ag.eps = c.eps;
     if ((e = w8_gemm(ag, s.u, st, true)) != cudaSuccess) return DFLASH_ECUDA;
-    // x += W8(down) g
+    // x += W8(down) g; for all but the last layer also u = x * gamma_in[l+1]
     W8Args ad = base_args(w->down[l], M, EPI_RESID_F32);
     ad.out_f32 = s.x;
     ad.ldo = c.H;
-    if ((e = w8_gemm(ad, s.g, st, true)) != cudaSuccess) return DFLASH_ECUDA;
     if (l + 1 < c.L) {
-      if ((e = rmsnorm_f16(s.x, M, c.H, w->gamma_in + (size_t)(l + 1) * c.H, c.eps, s.u, st, true)) != cudaSuccess)
-        return DFLASH_ECUDA;
+      ad.xg_out = s.u;
+      ad.g_next = w->gamma_in + (size_t)(l + 1) * c.H;
+      ad.ss_out = s.ss;
+      ad.nss_out = c.H / 128;
     }
+    if ((e = w8_gemm(ad, s.g, st, true)) != cudaSuccess) return DFLASH_ECUDA;
   }
   (void)qd;
   (void)kd;
@@ -529,11 +544,15 @@ int32_t dflash_kv_commit(const dflash_weights* w, const dflash_kv* kv, const uin
   const size_t layer_kv = (size_t)b * c.nkv * kv->cap * c.d;
   cudaError_t e;
   // c = RMSNorm(W8(fc) h; gamma_hid)
+  // the epilogue writes u = y * gamma_hid and the row sums of squares; the
+  // K/V GEMMs apply the RMSNorm factor to their results
   W8Args af = base_args(w->fc, Mc, EPI_STORE_F32);
-  af.out_f32 = s.y;
   af.ldo = c.H;
+  af.xg_out = s.u;
+  af.g_next = w->gamma_hid;
+  af.ss_out = s.ss;
+  af.nss_out = c.H / 128;
   if ((e = w8_gemm(af, reinterpret_cast<const __half*>(hid), st, false)) != cudaSuccess) return DFLASH_ECUDA;
-  if ((e = rmsnorm_f16(s.y, Mc, c.H, w->gamma_hid, c.eps, s.u, st, true)) != cudaSuccess) return DFLASH_ECUDA;
   for (int l = 0; l < c.L; ++l) {
     W8Args a = base_args(w->qkv[l], Mc, EPI_KVCOMMIT);
     fill_inv_freq(a, c.rope_theta, c.d);
@@ -552,6 +571,8 @@ int32_t dflash_kv_commit(const dflash_weights* w, const dflash_kv* kv, const uin
     a.rows_per_seq = rows_per_seq;
     a.b = b;
     a.cap = kv->cap;
+    a.ss_in = s.ss;
+    a.nss_in = c.H / 128;
     if ((e = w8_gemm(a, s.u, st, true)) != cudaSuccess) return DFLASH_ECUDA;
   }
   return map_err(commit_len_update(kv->len, n, b, rows_per_seq, kv->cap, st, true, status));

@@ -51,7 +51,9 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
   float* sLse = reinterpret_cast<float*>(sV + 2 * kKT * RB);  // [rows_pad]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-  pdl_wait();
+  // The context K/V and its length are inputs of the whole draft pass (no
+  // kernel of the pass writes them), so the first tile's context keys are
+  // fetched before waiting for the kernel that produces q and the block K/V.
   int L = a.len[j];
   if (L < 0) L = 0;
   if (L > a.cap) L = a.cap;
@@ -59,26 +61,19 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
   int k0, k1;
   split_range(total, sp, ns, k0, k1);
 
-  // ---- Q tile: row rho = tok * grp + hh  ->  q[(j B + tok)][g grp + hh][:]
-  for (int c = threadIdx.x; c < rows_pad * (D / 8); c += blockDim.x) {
-    int rho = c / (D / 8), ch = c % (D / 8);
-    bool ok = rho < rows;
-    const __half* src = a.q;
-    if (ok) {
-      int tok = rho / grp, hh = rho - tok * grp;
-      src = a.q + ((size_t)(j * a.B + tok) * a.nq + (g * grp + hh)) * D + ch * 8;
-    }
-    cp_async16(sQ + rho * RB + ((ch ^ (rho & 7)) << 4), src, ok);
-  }
-  auto load_kv = [&](int buf, int t0) {
+  // part 0: context keys t < L only; 1: block keys and the zero fill; 2: all
+  auto load_kv = [&](int buf, int t0, int part) {
     for (int c = threadIdx.x; c < kKT * (D / 8); c += blockDim.x) {
       int r = c / (D / 8), ch = c % (D / 8);
       int t = t0 + r;
       bool ok = t < k1;
+      const bool ctx = ok && t < L;
+      if (part == 0 && !ctx) continue;
+      if (part == 1 && ctx) continue;
       const __half* ks = a.kc;
       const __half* vs = a.vc;
       if (ok) {
-        if (t < L) {
+        if (ctx) {
           size_t off = (((size_t)j * a.nkv + g) * a.cap + t) * D + ch * 8;
           ks = a.kc + off;
           vs = a.vc + off;
@@ -94,7 +89,21 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
     }
   };
   const int ntile = (k1 - k0 + kKT - 1) / kKT;
-  load_kv(0, k0);
+  load_kv(0, k0, 0);
+  pdl_wait();
+
+  // ---- Q tile: row rho = tok * grp + hh  ->  q[(j B + tok)][g grp + hh][:]
+  for (int c = threadIdx.x; c < rows_pad * (D / 8); c += blockDim.x) {
+    int rho = c / (D / 8), ch = c % (D / 8);
+    bool ok = rho < rows;
+    const __half* src = a.q;
+    if (ok) {
+      int tok = rho / grp, hh = rho - tok * grp;
+      src = a.q + ((size_t)(j * a.B + tok) * a.nq + (g * grp + hh)) * D + ch * 8;
+    }
+    cp_async16(sQ + rho * RB + ((ch ^ (rho & 7)) << 4), src, ok);
+  }
+  load_kv(0, k0, 1);
   cp_async_commit();
 
   const float sl2 = rsqrtf((float)D) * 1.4426950408889634f;
@@ -108,7 +117,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
   uint32_t qf[D / 16][4];
 
   for (int it = 0; it < ntile; ++it) {
-    if (it + 1 < ntile) load_kv((it + 1) & 1, k0 + (it + 1) * kKT);
+    if (it + 1 < ntile) load_kv((it + 1) & 1, k0 + (it + 1) * kKT, 2);
     cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();

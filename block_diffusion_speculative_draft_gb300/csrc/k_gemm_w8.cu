@@ -42,8 +42,9 @@ struct Geo {
   static constexpr int TSTRIDE = 132;  // epilogue tile row stride (floats)
   static constexpr int TBYTES = (MCH * TSTRIDE * 4 + 1023) / 1024 * 1024;
   static_assert(2 * TBYTES <= kStages * STAGE, "epilogue tiles must fit in the ring");
-  // side data after the barriers: row scales, gamma, per-row positions
-  static constexpr int SIDE = 128 * 4 + 128 * 4 + MCH * 4;
+  // side data after the barriers: row scales, gamma, next gamma, per-row
+  // positions, per-row norm factors
+  static constexpr int SIDE = 128 * 4 + 128 * 4 + 128 * 4 + MCH * 4 + MCH * 4;
   static constexpr size_t SMEM = 1024 + kStages * (size_t)STAGE + 2 * kStages * 8 + 64 + SIDE;
 };
 
@@ -77,13 +78,20 @@ __device__ __forceinline__ void rope_pair(float& x1, float& x2, int pos, double 
 // staged in shared memory before the main loop so that no global load sits on
 // the epilogue's critical path except the residual read, issued in batches.
 template <int MT>
-__device__ void epilogue(const W8Args& a, const float* T, const float* sc, const float* gam, const int* pos,
-                         int nt, int z, int tlo, int thi, int warp, int lane) {
+__device__ void epilogue(const W8Args& a, float* T, const float* sc, const float* gam, const int* pos,
+                         const float* gn, const float* rr, int nt, int z, int tlo, int thi, int warp, int lane) {
   using G = Geo<MT>;
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
   const int ntok = thi - tlo;
   const int prow0 = a.row0 + nt * kTile;  // first packed row of this tile
+  if (a.ss_in) {  // deferred RMSNorm of the input rows: one factor per row
+    for (int i = tid; i < ntok * kTile; i += nthr) {
+      const int tok = tlo + (i >> 7);
+      T[tok * G::TSTRIDE + (i & 127)] *= rr[tok];
+    }
+    __syncthreads();
+  }
   if (a.epi == EPI_STORE_F32 || a.epi == EPI_RESID_F32) {
     const int items = ntok * (kTile / 4);  // groups of 4 consecutive rows
     for (int base = tid; base < items; base += 4 * nthr) {
@@ -112,7 +120,37 @@ __device__ void epilogue(const W8Args& a, const float* T, const float* sc, const
         const float* t = T + tok * G::TSTRIDE + r;
         float4 v = make_float4(t[0] * sc[r] + xo[u].x, t[1] * sc[r + 1] + xo[u].y, t[2] * sc[r + 2] + xo[u].z,
                                t[3] * sc[r + 3] + xo[u].w);
-        *reinterpret_cast<float4*>(a.out_f32 + (size_t)m * a.ldo + (n - a.row0)) = v;
+        if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + (size_t)m * a.ldo + (n - a.row0)) = v;
+        if (a.xg_out) {
+          __half2 h0 = __floats2half2_rn(v.x * gn[r], v.y * gn[r + 1]);
+          __half2 h1 = __floats2half2_rn(v.z * gn[r + 2], v.w * gn[r + 3]);
+          uint2 pk;
+          pk.x = *reinterpret_cast<uint32_t*>(&h0);
+          pk.y = *reinterpret_cast<uint32_t*>(&h1);
+          *reinterpret_cast<uint2*>(a.xg_out + (size_t)m * a.ldo + (n - a.row0)) = pk;
+        }
+      }
+      if (a.xg_out) {
+        // each warp holds one row's 128 columns for a given u: sum of squares
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int it = base + u * nthr;
+          float ss = 0.f;
+          int m = -1;
+          if (it < items) {
+            const int tok = tlo + it / (kTile / 4), r = 4 * (it % (kTile / 4));
+            m = z * G::MCH + tok;
+            if (m < a.M) {
+              const float* t = T + tok * G::TSTRIDE + r;
+              float4 v = make_float4(t[0] * sc[r] + xo[u].x, t[1] * sc[r + 1] + xo[u].y,
+                                     t[2] * sc[r + 2] + xo[u].z, t[3] * sc[r + 3] + xo[u].w);
+              ss = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+            }
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+          if (lane == 0 && m >= 0 && m < a.M) a.ss_out[(size_t)m * a.nss_out + (prow0 >> 7)] = ss;
+        }
       }
     }
     return;
@@ -214,7 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
   uint64_t* empty = full + kStages;
   float* s_sc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(empty + kStages) + 64);  // [128]
   float* s_gam = s_sc + 128;                                                                 // [128]
-  int* s_pos = reinterpret_cast<int*>(s_gam + 128);                                          // [MCH]
+  float* s_gn = s_gam + 128;                                                                 // [128]
+  int* s_pos = reinterpret_cast<int*>(s_gn + 128);                                           // [MCH]
+  float* s_rr = reinterpret_cast<float*>(s_pos + G::MCH);                                    // [MCH]
 
   const int nt = blockIdx.x, sp = blockIdx.y, z = blockIdx.z;
   const int KT = a.K / kTile;
@@ -279,8 +319,20 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
         const float* gsrc = (a.row0 + nt * kTile) < qd ? a.gq : a.gk;
         s_gam[r] = (gsrc && r < a.d) ? gsrc[r] : 1.f;
       }
+      if (a.xg_out) s_gn[r] = a.g_next[logical_row(prow, a.layout, a.N) - a.row0];
     }
     pdl_wait();
+    if (a.ss_in && threadIdx.x < G::MCH) {
+      // deferred RMSNorm factor of each activation row (fixed summation order)
+      const int m = z * G::MCH + threadIdx.x;
+      float rf = 0.f;
+      if (m < a.M) {
+        float sum = 0.f;
+        for (int i = 0; i < a.nss_in; ++i) sum += a.ss_in[(size_t)m * a.nss_in + i];
+        rf = rsqrtf(sum / a.K + a.eps);
+      }
+      s_rr[threadIdx.x] = rf;
+    }
     if ((a.epi == EPI_QKV || a.epi == EPI_KVCOMMIT) && threadIdx.x < G::MCH) {
       // position of each activation row of this chunk, -1 when not written
       const int t = threadIdx.x, m = z * G::MCH + t;
@@ -353,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
   }
   if (a.splits == 1) {
     __syncthreads();
-    epilogue<MT>(a, P, s_sc, s_gam, s_pos, nt, z, 0, G::MCH, warp, lane);
+    epilogue<MT>(a, P, s_sc, s_gam, s_pos, s_gn, s_rr, nt, z, 0, G::MCH, warp, lane);
     return;
   }
   // ---- split-K reduction across the cluster through distributed smem ----
@@ -383,7 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
     *reinterpret_cast<float4*>(T + tok * G::TSTRIDE + 4 * c4) = accv;
   }
   cluster_sync();  // every peer has finished reading this CTA's partial
-  epilogue<MT>(a, T, s_sc, s_gam, s_pos, nt, z, tlo, thi, warp, lane);
+  epilogue<MT>(a, T, s_sc, s_gam, s_pos, s_gn, s_rr, nt, z, tlo, thi, warp, lane);
 }
 
 // ------------------------------------------------------------- packing ----

@@ -44,6 +44,17 @@ struct W8Args {
   int rows_per_seq;  // activation rows per sequence
   int b, cap;
   int* status;
+  // Deferred RMSNorm.  Reader side: when ss_in is set, the activations are
+  // x * gamma (not yet normalised) and the epilogue scales each row's result
+  // by rsqrt(sum_i ss_in[m][i] / K + eps), i < nss_in.  Writer side (STORE /
+  // RESID): when xg_out is set, also write fp16(y * g_next) and each row's
+  // sum of squares over this 128-column tile into ss_out[m][tile].
+  const float* ss_in;
+  int nss_in;
+  float* ss_out;
+  int nss_out;
+  __half* xg_out;
+  const float* g_next;
   double inv_freq[64];  // RoPE theta^(-2p/d), p < d/2 (per-head epilogues)
 };
 
