@@ -166,10 +166,16 @@ W8Args base_args(const dflash_w8& w, int M, int epi) {
   return a;
 }
 
-// RoPE frequencies theta^(-2p/d) for the per-head epilogues, in double
-void fill_inv_freq(W8Args& a, float theta, int d) {
-  for (int p = 0; p < 64; ++p) a.inv_freq[p] = p < d / 2 ? pow((double)theta, -2.0 * p / d) : 0.0;
+// RoPE frequencies theta^(-2p/d), computed in double and split into float
+// pairs hi + lo for the single-precision angle reduction of the epilogues
+void split_inv_freq(float* hi, float* lo, float theta, int d) {
+  for (int p = 0; p < 64; ++p) {
+    const double v = p < d / 2 ? pow((double)theta, -2.0 * p / d) : 0.0;
+    hi[p] = (float)v;
+    lo[p] = (float)(v - (double)hi[p]);
+  }
 }
+void fill_inv_freq(W8Args& a, float theta, int d) { split_inv_freq(a.inv_hi, a.inv_lo, theta, d); }
 
 }  // namespace
 
@@ -257,6 +263,7 @@ static int check_weights(const dflash_weights* w) {
 static int check_kv(const dflash_kv* kv) {
   if (!kv || !kv->k || !kv->v || !kv->len) return DFLASH_EINVAL;
   if (kv->b < 1 || kv->cap < 1) return DFLASH_EINVAL;
+  if (kv->cap > (1 << 24) - 64) return DFLASH_EUNSUPPORTED;  // positions stay exact in fp32
   if (!aligned16(kv->k) || !aligned16(kv->v)) return DFLASH_EINVAL;
   return DFLASH_OK;
 }
@@ -331,7 +338,7 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
       a.attn_kt = akt;
       a.ntmax = step_ntiles_max(c);
       a.eps = c.eps;
-      for (int p = 0; p < 64; ++p) a.inv_freq[p] = p < c.d / 2 ? pow((double)c.rope_theta, -2.0 * p / c.d) : 0.0;
+      split_inv_freq(a.inv_hi, a.inv_lo, c.rope_theta, c.d);
       auto sw = [](const dflash_w8& x) {
         StepW8 r;
         r.q = static_cast<const uint8_t*>(x.q);
@@ -406,7 +413,7 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
     }
     if ((e = w8_gemm(a, s.u, st, true)) != cudaSuccess) return DFLASH_ECUDA;
     // block attention over [context || block]
-    AttnArgs at;
+    AttnArgs at{};
     at.q = s.q;
     at.kblk = s.kb;
     at.vblk = s.vb;

@@ -16,6 +16,10 @@
 // distributed shared memory, in split order.  Q.K^T and P.V run on m16n8k16
 // tensor-core MMAs with fp32 accumulation; K/V tiles of 64 keys are
 // double-buffered with cp.async into XOR-swizzled shared memory.
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -23,8 +27,9 @@ namespace dfl {
 
 namespace {
 
-constexpr int kMaxSplits = 8;  // one portable cluster
-constexpr int kKT = 64;        // keys per tile
+constexpr int kMaxSplits = 16;  // one (non-portable) cluster of splits
+constexpr int kPortable = 8;    // largest cluster every sm_90+ part accepts
+constexpr int kKT = 64;         // keys per tile
 
 // keys [k0, k1) of split sp out of ns equal, 64-aligned chunks of `total`
 __device__ __forceinline__ void split_range(int total, int sp, int ns, int& k0, int& k1) {
@@ -239,79 +244,126 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
       }
     return;
   }
-  // partial O [rows_pad][D] fp32 over the (now idle) Q/K/V buffers; an empty
-  // split may still have zero-fill copies in flight
-  cp_async_wait<0>();
-  __syncthreads();
-  float* sO = reinterpret_cast<float*>(sQ);
+  // Push this split's normalised partial rows and log-sum-exps into the
+  // shared memory of the CTA that owns them (CTA p merges rows
+  // [p rows / ns, (p + 1) rows / ns)); remote stores do not wait for a reply,
+  // and the owner then merges from its own shared memory.  The receive area
+  // is separate from Q/K/V, so no barrier is needed before the pushes.
+  const int maxr = (rows + ns - 1) / ns;
+  constexpr int RS = D + 4;  // row stride (floats): conflict-free float2 stores
+  float* rO = reinterpret_cast<float*>(sLse + rows_pad);  // [ns][maxr][RS]
+  float* rL = rO + (size_t)ns * maxr * RS;                 // [ns][maxr]
+  const uint32_t rObase = smem_u32(rO), rLbase = smem_u32(rL);
 #pragma unroll
-  for (int i = 0; i < D / 8; ++i)
+  for (int h = 0; h < 2; ++h) {
+    const int rho = warp * 16 + g8 + 8 * h;
+    if (rho >= rows) continue;
+    const int own = ((rho + 1) * ns - 1) / rows;
+    const int lr = rho - (own * rows) / ns;
+    const uint32_t dst = dsmem_addr(rObase + (uint32_t)((sp * maxr + lr) * RS + 2 * t4) * 4u, (uint32_t)own);
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      int rho = warp * 16 + g8 + ((e >> 1) << 3);
-      int dim = i * 8 + 2 * t4 + (e & 1);
-      sO[rho * D + dim] = o[i][e] * inv[e >> 1];
-    }
-  if (t4 == 0) {
-    sLse[warp * 16 + g8] = lse[0];
-    sLse[warp * 16 + g8 + 8] = lse[1];
+    for (int i = 0; i < D / 8; ++i) st_dsmem_f2(dst + i * 32u, o[i][2 * h] * inv[h], o[i][2 * h + 1] * inv[h]);
+    if (t4 == 0) st_dsmem_f32(dsmem_addr(rLbase + (uint32_t)(sp * maxr + lr) * 4u, (uint32_t)own), lse[h]);
   }
-  cluster_sync();
-  // merge rows [r0, r1) over the ns splits, in split order
+  cp_async_wait<0>();  // an empty split may still have zero-fill copies in flight
+  cluster_sync();      // every push into this CTA is visible
+  // merge the owned rows over the ns splits, in split order
   const int r0 = (sp * rows) / ns, r1 = ((sp + 1) * rows) / ns;
-  const uint32_t obase = smem_u32(sO), lbase = smem_u32(sLse);
   for (int it = threadIdx.x; it < (r1 - r0) * (D / 4); it += blockDim.x) {
-    const int rho = r0 + it / (D / 4), c4 = it % (D / 4);
-    float ls[kMaxSplits];
+    const int lr = it / (D / 4), c4 = it % (D / 4);
     float mmax = -INFINITY;
-#pragma unroll
-    for (int s2 = 0; s2 < kMaxSplits; ++s2) {
-      ls[s2] = s2 < ns ? ld_dsmem_f32(dsmem_addr(lbase + rho * 4u, (uint32_t)s2)) : -INFINITY;
-      mmax = fmaxf(mmax, ls[s2]);
-    }
-    float4 ov[kMaxSplits];
-#pragma unroll
-    for (int s2 = 0; s2 < kMaxSplits; ++s2)
-      if (s2 < ns) ov[s2] = ld_dsmem_f4(dsmem_addr(obase + (uint32_t)(rho * D + 4 * c4) * 4u, (uint32_t)s2));
+    for (int s2 = 0; s2 < ns; ++s2) mmax = fmaxf(mmax, rL[s2 * maxr + lr]);
     float den = 0.f;
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int s2 = 0; s2 < kMaxSplits; ++s2)
-      if (s2 < ns) {
-        float w = exp2f(ls[s2] - mmax);
-        den += w;
-        num.x += w * ov[s2].x;
-        num.y += w * ov[s2].y;
-        num.z += w * ov[s2].z;
-        num.w += w * ov[s2].w;
-      }
+    for (int s2 = 0; s2 < ns; ++s2) {
+      const float w = exp2f(rL[s2 * maxr + lr] - mmax);
+      const float4 ov = *reinterpret_cast<const float4*>(rO + (size_t)(s2 * maxr + lr) * RS + 4 * c4);
+      den += w;
+      num.x += w * ov.x;
+      num.y += w * ov.y;
+      num.z += w * ov.z;
+      num.w += w * ov.w;
+    }
     const float id = 1.f / den;
+    const int rho = r0 + lr;
     int tok = rho / grp, hh = rho - tok * grp;
     __half2* dst = reinterpret_cast<__half2*>(a.out + ((size_t)(j * a.B + tok) * a.nq + g * grp + hh) * D + 4 * c4);
     dst[0] = __floats2half2_rn(num.x * id, num.y * id);
     dst[1] = __floats2half2_rn(num.z * id, num.w * id);
   }
-  cluster_sync();  // peers are done reading this CTA's partial
 }
 
 }  // namespace
+
+// Whether a cluster of ns splits can be resident (non-portable sizes above 8
+// need the opt-in attribute and enough free SMs in one GPC).
+// The answer is cached per (device, kernel, ns, threads, smem).
+static bool attn_cluster_fits(const void* fn, int ns, int threads, size_t smem) {
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, fn, ns, threads, smem);
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, int, int, size_t>, bool> cache;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ns, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = ns;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 0;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = n > 0;
+  return n > 0;
+}
 
 cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
   AttnArgs a = a0;
   const int rows = a.B * (a.nq / a.nkv);
   const int nw = (rows + 15) / 16;
   const int rows_pad = nw * 16;
-  int ns = (a.cap + a.B + 127) / 128;  // splits sized for the longest possible context
+  const void* fn = a.d == 128 ? (const void*)attn_kernel<128> : (const void*)attn_kernel<64>;
+  // one 64-key tile per split while the longest possible context allows it,
+  // so the (latency-bound) pass is as short as the split count permits
+  int ns = (a.cap + a.B + kKT - 1) / kKT;
   if (ns > kMaxSplits) ns = kMaxSplits;
   if (ns < 1) ns = 1;
+  auto smem_for = [&](int n) {
+    // Q, double-buffered K/V, per-row lse, then the merge's receive area
+    size_t b = 128 + (size_t)rows_pad * a.d * 2 + 4 * kKT * a.d * 2 + rows_pad * 4;
+    if (n > 1) {
+      const size_t maxr = (rows + n - 1) / n;
+      b += (size_t)n * maxr * (a.d + 4) * 4 + (size_t)n * maxr * 4;
+    }
+    return b;
+  };
+  size_t smem = smem_for(ns);
+  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (ns > kPortable && !attn_cluster_fits(fn, ns, nw * 32, smem)) {
+    ns = kPortable;
+    smem = smem_for(ns);
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  }
   a.max_splits = ns;
-  size_t smem = 128 + (size_t)rows_pad * a.d * 2 + 4 * kKT * a.d * 2 + rows_pad * 4;
-  const size_t need_o = 128 + (size_t)rows_pad * a.d * 4 + rows_pad * 4;  // partial O over Q/K/V
-  if (need_o > smem) smem = need_o;
   dim3 grid(ns, a.nkv, a.b);
   void* args[] = {&a};
-  const void* fn = a.d == 128 ? (const void*)attn_kernel<128> : (const void*)attn_kernel<64>;
-  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   return launch_kc(fn, grid, dim3(nw * 32), smem, st, pdl, dim3(ns, 1, 1), args);
 }
 

@@ -23,6 +23,10 @@
 //    epilogue for that slice; no partial ever touches global memory;
 //  * programmatic dependent launch: the weight copies of the first stages are
 //    issued before griddepcontrol.wait, overlapping the previous kernel's tail.
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -57,20 +61,6 @@ __device__ __forceinline__ int logical_row(int prow, int layout, int N) {
   return prow;
 }
 
-__device__ __forceinline__ void rope_pair(float& x1, float& x2, int pos, double inv) {
-  // angle = pos * theta^(-2p/d) (inv = theta^(-2p/d) from the host, in
-  // double), formed and range-reduced in double, then evaluated with the
-  // single-precision sincosf.
-  double ang = (double)pos * inv;
-  const double two_pi = 6.283185307179586476925286766559;
-  const double inv_two_pi = 0.15915494309189533576888376337251;
-  ang -= two_pi * rint(ang * inv_two_pi);
-  float sn, cs;
-  sincosf((float)ang, &sn, &cs);
-  float a = x1, b = x2;
-  x1 = a * cs - b * sn;
-  x2 = b * cs + a * sn;
-}
 
 // Epilogue for the chunk's activation rows [tlo, thi).  T holds the reduced,
 // unscaled fp32 tile as [row][TSTRIDE]; sc[r] is packed row r's scale, gam
@@ -109,47 +99,37 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
           }
         }
       }
+      // one row's 128 columns span exactly one warp for a given u (items is a
+      // multiple of 32 and nthr of 32), so the row sum of squares is a warp sum
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int it = base + u * nthr;
-        if (it >= items) continue;
-        const int tok = tlo + it / (kTile / 4), r = 4 * (it % (kTile / 4));
-        const int m = z * G::MCH + tok;
-        if (m >= a.M) continue;
-        const int n = logical_row(prow0 + r, a.layout, a.N);
-        const float* t = T + tok * G::TSTRIDE + r;
-        float4 v = make_float4(t[0] * sc[r] + xo[u].x, t[1] * sc[r + 1] + xo[u].y, t[2] * sc[r + 2] + xo[u].z,
-                               t[3] * sc[r + 3] + xo[u].w);
-        if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + (size_t)m * a.ldo + (n - a.row0)) = v;
-        if (a.xg_out) {
-          __half2 h0 = __floats2half2_rn(v.x * gn[r], v.y * gn[r + 1]);
-          __half2 h1 = __floats2half2_rn(v.z * gn[r + 2], v.w * gn[r + 3]);
-          uint2 pk;
-          pk.x = *reinterpret_cast<uint32_t*>(&h0);
-          pk.y = *reinterpret_cast<uint32_t*>(&h1);
-          *reinterpret_cast<uint2*>(a.xg_out + (size_t)m * a.ldo + (n - a.row0)) = pk;
-        }
-      }
-      if (a.xg_out) {
-        // each warp holds one row's 128 columns for a given u: sum of squares
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int it = base + u * nthr;
-          float ss = 0.f;
-          int m = -1;
-          if (it < items) {
-            const int tok = tlo + it / (kTile / 4), r = 4 * (it % (kTile / 4));
-            m = z * G::MCH + tok;
-            if (m < a.M) {
-              const float* t = T + tok * G::TSTRIDE + r;
-              float4 v = make_float4(t[0] * sc[r] + xo[u].x, t[1] * sc[r + 1] + xo[u].y,
-                                     t[2] * sc[r + 2] + xo[u].z, t[3] * sc[r + 3] + xo[u].w);
+        float ss = 0.f;
+        int m = a.M;
+        if (it < items) {
+          const int tok = tlo + it / (kTile / 4), r = 4 * (it % (kTile / 4));
+          m = z * G::MCH + tok;
+          if (m < a.M) {
+            const int n = logical_row(prow0 + r, a.layout, a.N);
+            const float* t = T + tok * G::TSTRIDE + r;
+            float4 v = make_float4(t[0] * sc[r] + xo[u].x, t[1] * sc[r + 1] + xo[u].y,
+                                   t[2] * sc[r + 2] + xo[u].z, t[3] * sc[r + 3] + xo[u].w);
+            if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + (size_t)m * a.ldo + (n - a.row0)) = v;
+            if (a.xg_out) {
+              __half2 h0 = __floats2half2_rn(v.x * gn[r], v.y * gn[r + 1]);
+              __half2 h1 = __floats2half2_rn(v.z * gn[r + 2], v.w * gn[r + 3]);
+              uint2 pk;
+              pk.x = *reinterpret_cast<uint32_t*>(&h0);
+              pk.y = *reinterpret_cast<uint32_t*>(&h1);
+              *reinterpret_cast<uint2*>(a.xg_out + (size_t)m * a.ldo + (n - a.row0)) = pk;
               ss = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
             }
           }
+        }
+        if (a.xg_out && it < items) {  // warp-uniform condition
 #pragma unroll
           for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-          if (lane == 0 && m >= 0 && m < a.M) a.ss_out[(size_t)m * a.nss_out + (prow0 >> 7)] = ss;
+          if (lane == 0 && m < a.M) a.ss_out[(size_t)m * a.nss_out + (prow0 >> 7)] = ss;
         }
       }
     }
@@ -200,8 +180,8 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
         float inv = rsqrtf(ss / 128.0f + a.eps);
 #pragma unroll
         for (int i = 0; i < 4; ++i) v[i] *= inv * gam[lane + 32 * i];
-        rope_pair(v[0], v[2], p, a.inv_freq[lane]);
-        rope_pair(v[1], v[3], p, a.inv_freq[lane + 32]);
+        rope_rot(v[0], v[2], p, a.inv_hi[lane], a.inv_lo[lane]);
+        rope_rot(v[1], v[3], p, a.inv_hi[lane + 32], a.inv_lo[lane + 32]);
       } else {  // d == 64: rows 0..63 head A, 64..127 head B
         float sa = v[0] * v[0] + v[1] * v[1];
         float sb = v[2] * v[2] + v[3] * v[3];
@@ -215,8 +195,8 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
         v[1] *= ia * gam[lane + 32];
         v[2] *= ib * gam[lane];
         v[3] *= ib * gam[lane + 32];
-        rope_pair(v[0], v[1], p, a.inv_freq[lane]);
-        rope_pair(v[2], v[3], p, a.inv_freq[lane]);
+        rope_rot(v[0], v[1], p, a.inv_hi[lane], a.inv_lo[lane]);
+        rope_rot(v[2], v[3], p, a.inv_hi[lane], a.inv_lo[lane]);
       }
     }
     if (a.epi == EPI_QKV) {
@@ -529,22 +509,61 @@ int w8_pick_splits(int units, int KT) {
 
 static int pick_mt(int M) { return M <= 16 ? 2 : 4; }
 
+// How many clusters of (1, s, 1) CTAs can be resident at once: clusters are
+// placed within one GPC, so sizes that do not divide a GPC's CTA slots leave
+// slots unused and a grid that looked like one wave may need two.  Cached per
+// (device, kernel, s).
+static int max_active_clusters(const void* fn, size_t smem, int s) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, fn, s);
+  static std::mutex mu;
+  static std::map<std::tuple<int, const void*, int>, int> cache;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, s, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 1;
+  at[0].val.clusterDim.y = s;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    n = 1 << 30;  // unknown: do not constrain the split count
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  cache[key] = n;
+  return n;
+}
+
 cudaError_t w8_gemm(const W8Args& a0, const __half* x, cudaStream_t st, bool pdl) {
   W8Args a = a0;
   const int mt = pick_mt(a.M);
   const int mch = mt * 8;
   const int chunks = (a.M + mch - 1) / mch;
   const int ntiles = a.nrows / kTile;
-  a.splits = w8_pick_splits(chunks * ntiles, a.K / kTile);
+  const void* fn = mt == 2 ? (const void*)w8_gemm_kernel<2> : (const void*)w8_gemm_kernel<4>;
+  const size_t smem = mt == 2 ? Geo<2>::SMEM : Geo<4>::SMEM;
+  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const int units = chunks * ntiles;
+  a.splits = w8_pick_splits(units, a.K / kTile);
+  // keep the whole grid resident in one wave
+  while (a.splits > 1 && units > max_active_clusters(fn, smem, a.splits)) --a.splits;
   CUtensorMap map;
   if (!encode_tmap_2d(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, (uint64_t)a.K, (uint64_t)a.M,
                       (uint64_t)a.K * 2, 64, (uint32_t)mch, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   void* args[] = {&map, &a};
   dim3 grid(ntiles, a.splits, chunks);
-  const void* fn = mt == 2 ? (const void*)w8_gemm_kernel<2> : (const void*)w8_gemm_kernel<4>;
-  const size_t smem = mt == 2 ? Geo<2>::SMEM : Geo<4>::SMEM;
-  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   return launch_kc(fn, grid, dim3(kThreads), smem, st, pdl, dim3(1, a.splits, 1), args);
 }
 

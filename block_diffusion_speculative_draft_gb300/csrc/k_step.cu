@@ -125,17 +125,6 @@ struct Smem {
   float* gam; // [128]
 };
 
-__device__ __forceinline__ void rope_pair(float& x1, float& x2, int pos, double inv) {
-  double ang = (double)pos * inv;
-  const double two_pi = 6.283185307179586476925286766559;
-  const double inv_two_pi = 0.15915494309189533576888376337251;
-  ang -= two_pi * rint(ang * inv_two_pi);
-  float sn, cs;
-  sincosf((float)ang, &sn, &cs);
-  float a = x1, b = x2;
-  x1 = a * cs - b * sn;
-  x2 = b * cs + a * sn;
-}
 
 // ------------------------------------------------------ weight schedule ----
 // Every weight stage of this CTA in consumption order, with the number of
@@ -399,8 +388,8 @@ __device__ void step_epilogue(Cons& C, int ep, const StepW8& w, int t, const flo
         const float inv = rsqrtf(ss / 128.0f + a.eps);
 #pragma unroll
         for (int i = 0; i < 4; ++i) v[i] *= inv * gam[lane + 32 * i];
-        rope_pair(v[0], v[2], p, a.inv_freq[lane]);
-        rope_pair(v[1], v[3], p, a.inv_freq[lane + 32]);
+        rope_rot(v[0], v[2], p, a.inv_hi[lane], a.inv_lo[lane]);
+        rope_rot(v[1], v[3], p, a.inv_hi[lane + 32], a.inv_lo[lane + 32]);
       } else {
         float sa = v[0] * v[0] + v[1] * v[1], sb = v[2] * v[2] + v[3] * v[3];
 #pragma unroll
@@ -413,8 +402,8 @@ __device__ void step_epilogue(Cons& C, int ep, const StepW8& w, int t, const flo
         v[1] *= ia * gam[lane + 32];
         v[2] *= ib * gam[lane];
         v[3] *= ib * gam[lane + 32];
-        rope_pair(v[0], v[1], p, a.inv_freq[lane]);
-        rope_pair(v[2], v[3], p, a.inv_freq[lane]);
+        rope_rot(v[0], v[1], p, a.inv_hi[lane], a.inv_lo[lane]);
+        rope_rot(v[2], v[3], p, a.inv_hi[lane], a.inv_lo[lane]);
       }
     }
 #pragma unroll

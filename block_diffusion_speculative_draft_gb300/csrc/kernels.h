@@ -55,7 +55,10 @@ struct W8Args {
   int nss_out;
   __half* xg_out;
   const float* g_next;
-  double inv_freq[64];  // RoPE theta^(-2p/d), p < d/2 (per-head epilogues)
+  // RoPE frequencies theta^(-2p/d), p < d/2, as float pairs hi + lo of the
+  // double value (per-head epilogues)
+  float inv_hi[64];
+  float inv_lo[64];
 };
 
 // Tensor-map encoder from the driver (resolved once through the runtime).
@@ -123,7 +126,8 @@ struct StepArgs {
   int attn_kt;      // attention key tile (64 or 32)
   int ntmax;        // row tiles of the widest projection (counter stride)
   float eps;
-  double inv_freq[64];
+  float inv_hi[64];  // RoPE frequencies as float pairs (see W8Args)
+  float inv_lo[64];
   StepW8 qkv[8], o[8], gu[8], down[8];
   const float* gamma_in;
   const float* gamma_post;

@@ -161,6 +161,43 @@ __device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
                : "memory");
   return v;
 }
+// Rotates (x1, x2) by the RoPE angle pos * inv, where inv = inv_hi + inv_lo
+// (a double split into two floats on the host), in single precision only
+// (FP64 issue is far too slow on this part for an epilogue).  The product is
+// carried as a float pair (the FMA gives the exact rounding error of
+// pos * inv_hi), and 2*pi is removed by Cody-Waite reduction with 2*pi split
+// into two floats (W. J. Cody, W. Waite, "Software Manual for the Elementary
+// Functions", 1980), so the reduced angle r (|r| <= pi + 1e-5) is within
+// about 1e-6 rad of the exact one for pos < 2^24.  On that range the
+// hardware sine/cosine approximation (__sincosf) has an absolute error near
+// 2^-21, far below the fp16 rounding of the rotated outputs, at a fraction of
+// the latency of the general sincosf.
+__device__ __forceinline__ void rope_rot(float& x1, float& x2, int pos, float inv_hi, float inv_lo) {
+  constexpr float kTwoPiHi = 0x1.921fb6p+2f;    // float(2 pi)
+  constexpr float kTwoPiLo = -0x1.777a5cp-23f;  // float(2 pi - kTwoPiHi)
+  constexpr float kInvTwoPi = 0x1.45f306p-3f;
+  const float p = (float)pos;  // exact below 2^24
+  const float a_hi = p * inv_hi;
+  const float a_lo = fmaf(p, inv_lo, fmaf(p, inv_hi, -a_hi));
+  const float k = rintf(a_hi * kInvTwoPi);
+  float r = fmaf(-k, kTwoPiHi, a_hi);
+  r = fmaf(-k, kTwoPiLo, r);
+  r += a_lo;
+  float sn, cs;
+  __sincosf(r, &sn, &cs);
+  const float a = x1, b = x2;
+  x1 = a * cs - b * sn;
+  x2 = b * cs + a * sn;
+}
+
+// Stores into another CTA's shared memory (made visible to it by the next
+// cluster barrier's release/acquire pair).
+__device__ __forceinline__ void st_dsmem_f2(uint32_t addr, float x, float y) {
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(addr), "f"(x), "f"(y) : "memory");
+}
+__device__ __forceinline__ void st_dsmem_f32(uint32_t addr, float x) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(x) : "memory");
+}
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t addr) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
