@@ -138,7 +138,9 @@ typedef struct dflash_kv {
   uint16_t* v;
   int32_t* len;
   int32_t b;   /* sequences */
-  int32_t cap; /* rows per sequence */
+  int32_t cap; /* rows per sequence; at most 2^24 - 64 (positions are carried
+                  exactly in fp32 by the RoPE epilogues), else the calls that
+                  take a dflash_kv return DFLASH_EUNSUPPORTED */
 } dflash_kv;
 
 /* Library version string (static storage). */
