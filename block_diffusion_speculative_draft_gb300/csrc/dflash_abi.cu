@@ -90,6 +90,8 @@ struct WS {
 };
 
 constexpr int kStepMaxSplits = 8;
+// bytes of the lm-head table prefetched into L2 during the layers' attention
+constexpr size_t kLmPrefetchBytes = (size_t)64 << 20;
 
 int step_rows_pad(const dflash_config& c) {
   const int rows = c.B * (c.nq / c.nkv);
@@ -386,6 +388,14 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
     }
     return DFLASH_EUNSUPPORTED;
   }
+  // L2 prefetch of the lm-head: a whole number of rows of each first-round
+  // tile, about kLmPrefetchBytes in total
+  int lm_first = lmhead_first_tiles(b * (c.B - 1), c.V);
+  if (lm_first > c.V / 128) lm_first = c.V / 128;  // whole tiles only: never past the table
+  const size_t row_bytes = (size_t)c.H * 2;
+  size_t lm_rows = kLmPrefetchBytes / ((size_t)lm_first * row_bytes);
+  if (lm_rows > 128) lm_rows = 128;
+  const uint32_t lm_pf_bytes = (uint32_t)(lm_rows * row_bytes);
   e = embed_rmsnorm(reinterpret_cast<const __nv_bfloat16*>(w->embed), last_tok, c.mask_id, c.V, b, c.B, c.H,
                     w->gamma_in, c.eps, s.x, s.u, st, false, status);
   if (e != cudaSuccess) return DFLASH_ECUDA;
@@ -428,6 +438,14 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
     at.d = c.d;
     at.cap = kv->cap;
     at.status = status;
+    // HBM is nearly idle during attention: pull a prefix of each vocabulary
+    // tile that starts an lm-head CTA's stream into L2 (a share per layer),
+    // so the lm-head reads that part from L2
+    at.pf_base = reinterpret_cast<const uint8_t*>(w->lm_head);
+    at.pf_stride = (size_t)128 * c.H * 2;
+    at.pf_bytes = lm_pf_bytes;
+    at.pf_i0 = (int)((long long)lm_first * l / c.L);
+    at.pf_i1 = (int)((long long)lm_first * (l + 1) / c.L);
     if ((e = attention(at, st, true)) != cudaSuccess) return DFLASH_ECUDA;
     // x += W8(o) attn
     // x += W8(o) attn; the epilogue also leaves u = x * gamma_post and the

@@ -95,6 +95,9 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
   };
   const int ntile = (k1 - k0 + kKT - 1) / kKT;
   load_kv(0, k0, 0);
+  if (a.pf_base && threadIdx.x == 0)
+    prefetch_l2_job(a.pf_base, a.pf_stride, a.pf_bytes, a.pf_i0, a.pf_i1,
+                    blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z), gridDim.x * gridDim.y * gridDim.z);
   pdl_wait();
 
   // ---- Q tile: row rho = tok * grp + hh  ->  q[(j B + tok)][g grp + hh][:]

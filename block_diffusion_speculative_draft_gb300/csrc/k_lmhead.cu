@@ -210,6 +210,14 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_kernel(const __grid_consta
 
 size_t lmhead_ws_bytes(int64_t M) { return 128 * sizeof(unsigned long long) + 256; }
 
+int lmhead_first_tiles(int M, int V) {
+  const int chunks = (M + (M <= 16 ? 16 : 32) - 1) / (M <= 16 ? 16 : 32);
+  const int ntiles = (V + 127) / 128;
+  int per_chunk = (2 * kNumSMs) / chunks;
+  if (per_chunk < 1) per_chunk = 1;
+  return ntiles < per_chunk ? ntiles : per_chunk;  // one CTA per tile of the first round
+}
+
 cudaError_t lmhead_argmax(const __nv_bfloat16* h, const __nv_bfloat16* w, int M, int V, int H, int* idx_out,
                           float* maxlogit, float* logits, void* ws, cudaStream_t st, bool pdl, int* status) {
   const int mt = M <= 16 ? 2 : 4;
@@ -232,11 +240,7 @@ cudaError_t lmhead_argmax(const __nv_bfloat16* h, const __nv_bfloat16* w, int M,
   if (!encode_tmap_2d(&hm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, (uint64_t)H, (uint64_t)M, (uint64_t)H * 2, 64,
                       (uint32_t)mch, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  const int ntiles = (V + 127) / 128;
-  int per_chunk = (2 * kNumSMs) / chunks;
-  if (per_chunk < 1) per_chunk = 1;
-  int ctas = ntiles < per_chunk ? ntiles : per_chunk;
-  dim3 grid(ctas, chunks);
+  dim3 grid(lmhead_first_tiles(M, V), chunks);
   void* args[] = {&wm, &hm, &a};
   if (mt == 2) {
     cudaFuncSetAttribute((const void*)lmhead_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,

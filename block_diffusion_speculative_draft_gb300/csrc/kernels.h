@@ -79,6 +79,9 @@ cudaError_t w8_pack(const void* w, int w_dtype, int64_t N, int64_t K, int layout
 
 // --- lm-head GEMM + argmax (k_lmhead.cu) ---
 size_t lmhead_ws_bytes(int64_t M);
+// Vocabulary tiles (128 rows each) the lm-head kernel reads first: tiles
+// [0, n) start every CTA's stream.
+int lmhead_first_tiles(int M, int V);
 cudaError_t lmhead_argmax(const __nv_bfloat16* h, const __nv_bfloat16* w, int M, int V, int H, int* idx_out,
                           float* maxlogit, float* logits, void* ws, cudaStream_t st, bool pdl, int* status);
 
@@ -94,6 +97,12 @@ struct AttnArgs {
   int b, B, nq, nkv, d, cap;
   int max_splits;
   int* status;
+  // L2 prefetch issued while the kernel would otherwise leave HBM idle:
+  // pieces [pf_i0, pf_i1) of base + i * pf_stride, pf_bytes each (or none)
+  const uint8_t* pf_base;
+  size_t pf_stride;
+  uint32_t pf_bytes;
+  int pf_i0, pf_i1;
 };
 cudaError_t attention(const AttnArgs& a, cudaStream_t st, bool pdl);
 

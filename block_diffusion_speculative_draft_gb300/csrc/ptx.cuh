@@ -97,6 +97,19 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
 __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
+// Pieces [i0, i1) of a strided L2 prefetch job (piece i covers
+// [base + i * stride, + bytes)), dealt round-robin to the ncta CTAs of the
+// grid and issued in 32 KB bulk prefetches.  base, stride and bytes are
+// multiples of 16 bytes.
+__device__ __forceinline__ void prefetch_l2_job(const uint8_t* base, size_t stride, uint32_t bytes, int i0, int i1,
+                                                unsigned cta, unsigned ncta) {
+  constexpr uint32_t kPiece = 32u << 10;
+  for (int i = i0 + (int)cta; i < i1; i += (int)ncta) {
+    const uint8_t* p = base + (size_t)i * stride;
+    for (uint32_t off = 0; off < bytes; off += kPiece)
+      prefetch_l2_bulk(p + off, bytes - off < kPiece ? bytes - off : kPiece);
+  }
+}
 // Same for one box of a 2-D tensor map.
 __device__ __forceinline__ void prefetch_l2_tile(const CUtensorMap* map, int x, int y) {
   asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x), "r"(y)
