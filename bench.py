@@ -117,8 +117,8 @@ class ClockSampler:
 
 def launches_per_step(cfg) -> int:
     # draft: embed+norm, per layer qkv/attn/o/gu/down (the RMSNorms between
-    # them are applied inside the GEMM epilogues), final norm, lm-head
-    draft = 5 * cfg.L + 3
+    # them, and the final one, are applied inside the GEMM epilogues), lm-head
+    draft = 5 * cfg.L + 2
     verify = 1
     commit = cfg.L + 2         # fc, per-layer K/V, length update
     return draft + verify + commit

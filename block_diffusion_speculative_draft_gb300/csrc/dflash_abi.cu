@@ -91,7 +91,7 @@ struct WS {
 
 constexpr int kStepMaxSplits = 8;
 // bytes of the lm-head table prefetched into L2 during the layers' attention
-constexpr size_t kLmPrefetchBytes = (size_t)64 << 20;
+constexpr size_t kLmPrefetchBytes = (size_t)96 << 20;
 
 int step_rows_pad(const dflash_config& c) {
   const int rows = c.B * (c.nq / c.nkv);
@@ -390,6 +390,7 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
   }
   // L2 prefetch of the lm-head: a whole number of rows of each first-round
   // tile, about kLmPrefetchBytes in total
+  const bool debug_out = hidden_out || logits_out;
   int lm_first = lmhead_first_tiles(b * (c.B - 1), c.V);
   if (lm_first > c.V / 128) lm_first = c.V / 128;  // whole tiles only: never past the table
   const size_t row_bytes = (size_t)c.H * 2;
@@ -476,12 +477,19 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
       ad.g_next = w->gamma_in + (size_t)(l + 1) * c.H;
       ad.ss_out = s.ss;
       ad.nss_out = c.H / 128;
+    } else if (!debug_out) {
+      // the lm-head input straight from the last residual update
+      ad.hb_out = s.h;
+      ad.hb_rps = c.B;
+      ad.g_next = w->gamma_final;
     }
     if ((e = w8_gemm(ad, s.g, st, true)) != cudaSuccess) return DFLASH_ECUDA;
   }
   (void)qd;
   (void)kd;
-  if ((e = final_norm(s.x, b, c.B, c.H, w->gamma_final, c.eps, s.h, hidden_out, st, true)) != cudaSuccess)
+  // normalised hidden rows (and so true logits) only when asked for them
+  if (debug_out &&
+      (e = final_norm(s.x, b, c.B, c.H, w->gamma_final, c.eps, s.h, hidden_out, st, true)) != cudaSuccess)
     return DFLASH_ECUDA;
   e = lmhead_argmax(s.h, reinterpret_cast<const __nv_bfloat16*>(w->lm_head), b * (c.B - 1), c.V, c.H, draft_out,
                     nullptr, logits_out, s.lm, st, true, status);

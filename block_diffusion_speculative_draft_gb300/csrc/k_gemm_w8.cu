@@ -124,6 +124,18 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
               *reinterpret_cast<uint2*>(a.xg_out + (size_t)m * a.ldo + (n - a.row0)) = pk;
               ss = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
             }
+            if (a.hb_out) {
+              const int seq = m / a.hb_rps, slot = m - seq * a.hb_rps;
+              if (slot > 0) {
+                __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x * gn[r], v.y * gn[r + 1]);
+                __nv_bfloat162 h1 = __floats2bfloat162_rn(v.z * gn[r + 2], v.w * gn[r + 3]);
+                uint2 pk;
+                pk.x = *reinterpret_cast<uint32_t*>(&h0);
+                pk.y = *reinterpret_cast<uint32_t*>(&h1);
+                const size_t o = (size_t)seq * (a.hb_rps - 1) + (slot - 1);
+                *reinterpret_cast<uint2*>(a.hb_out + o * a.ldo + (n - a.row0)) = pk;
+              }
+            }
           }
         }
         if (a.xg_out && it < items) {  // warp-uniform condition
@@ -299,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
         const float* gsrc = (a.row0 + nt * kTile) < qd ? a.gq : a.gk;
         s_gam[r] = (gsrc && r < a.d) ? gsrc[r] : 1.f;
       }
-      if (a.xg_out) s_gn[r] = a.g_next[logical_row(prow, a.layout, a.N) - a.row0];
+      if (a.xg_out || a.hb_out) s_gn[r] = a.g_next[logical_row(prow, a.layout, a.N) - a.row0];
     }
     pdl_wait();
     if (a.ss_in && threadIdx.x < G::MCH) {

@@ -55,6 +55,12 @@ struct W8Args {
   int nss_out;
   __half* xg_out;
   const float* g_next;
+  // Lm-head input (RESID): when set, rows with slot m % hb_rps > 0 also go to
+  // hb_out, compacted to row (m / hb_rps) (hb_rps - 1) + slot - 1, as
+  // bf16(y * g_next): the final RMSNorm's per-row factor is left out, which
+  // the argmax over each row's logits does not see.
+  __nv_bfloat16* hb_out;
+  int hb_rps;
   // RoPE frequencies theta^(-2p/d), p < d/2, as float pairs hi + lo of the
   // double value (per-head epilogues)
   float inv_hi[64];

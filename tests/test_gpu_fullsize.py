@@ -49,6 +49,12 @@ def test_fullsize_step(cfg, seqs):
         torch.cuda.synchronize()
         assert api.dflash_get_status() == 0
         outs.append((draft.cpu().numpy(), hidden.cpu().numpy(), logits.cpu().numpy()))
+    # the argmax-only pass (no optional outputs: final RMSNorm folded away)
+    draft_fast = torch.empty((b, cfg.B - 1), dtype=torch.int32, device=DEV)
+    api.dflash_draft_block(model, kv, last, draft_fast, ws)
+    torch.cuda.synchronize()
+    assert api.dflash_get_status() == 0
+    draft_fast = draft_fast.cpu().numpy()
     D = O.Drafter(cfg, W, cache=False)
     for j in seqs:
         Ks, Vs = O.context_kv(D, hids[j])
@@ -58,6 +64,7 @@ def test_fullsize_step(cfg, seqs):
             assert rel_err(hidden[j], ref["hidden"]) <= 2e-2
             assert rel_err(logits[j], ref["logits"]) <= 2e-2
             assert np.array_equal(draft[j][ok], ref["draft"][ok])
+        assert np.array_equal(draft_fast[j][ok], ref["draft"][ok])
         # committed context K/V of this sequence, two layers sampled
         C = int(ctx[j])
         for l in sorted({0, cfg.L - 1}):
