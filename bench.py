@@ -120,7 +120,7 @@ def launches_per_step(cfg) -> int:
     # them, and the final one, are applied inside the GEMM epilogues), lm-head
     draft = 5 * cfg.L + 2
     verify = 1
-    commit = cfg.L + 2         # fc, per-layer K/V, length update
+    commit = 2 + (cfg.L + 7) // 8  # fc, K/V of up to 8 layers per launch, length update
     return draft + verify + commit
 
 

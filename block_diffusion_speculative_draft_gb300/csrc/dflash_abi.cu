@@ -586,14 +586,24 @@ int32_t dflash_kv_commit(const dflash_weights* w, const dflash_kv* kv, const uin
   af.ss_out = s.ss;
   af.nss_out = c.H / 128;
   if ((e = w8_gemm(af, reinterpret_cast<const __half*>(hid), st, false)) != cudaSuccess) return DFLASH_ECUDA;
-  for (int l = 0; l < c.L; ++l) {
-    W8Args a = base_args(w->qkv[l], Mc, EPI_KVCOMMIT);
+  // K = rope(knorm(W_k c)), V = W_v c for every layer: the K/V rows of each
+  // layer's qkv projection, up to kLayersPerLaunch layers in one launch
+  for (int l0 = 0; l0 < c.L; l0 += kLayersPerLaunch) {
+    const int nl = c.L - l0 < kLayersPerLaunch ? c.L - l0 : kLayersPerLaunch;
+    W8Args a = base_args(w->qkv[l0], Mc, EPI_KVCOMMIT);
     fill_inv_freq(a, c.rope_theta, c.d);
     a.row0 = c.nq * c.d;
     a.nrows = 2 * c.nkv * c.d;
-    a.kout = reinterpret_cast<__half*>(kv->k) + l * layer_kv;
-    a.vout = reinterpret_cast<__half*>(kv->v) + l * layer_kv;
-    a.gk = w->gamma_k + (size_t)l * c.d;
+    a.nl = nl;
+    a.ntl = a.nrows / kTile;
+    for (int i = 0; i < nl; ++i) {
+      const int l = l0 + i;
+      a.lq[i] = static_cast<const uint8_t*>(w->qkv[l].q);
+      a.ls[i] = reinterpret_cast<const __half*>(w->qkv[l].s);
+      a.lk[i] = reinterpret_cast<__half*>(kv->k) + l * layer_kv;
+      a.lv[i] = reinterpret_cast<__half*>(kv->v) + l * layer_kv;
+      a.lgk[i] = w->gamma_k + (size_t)l * c.d;
+    }
     a.nq = c.nq;
     a.nkv = c.nkv;
     a.d = c.d;

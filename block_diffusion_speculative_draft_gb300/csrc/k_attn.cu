@@ -245,6 +245,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
         int dim = i * 8 + 2 * t4 + (e & 1);
         a.out[((size_t)(j * a.B + tok) * a.nq + g * grp + hh) * D + dim] = __float2half_rn(o[i][e] * inv[e >> 1]);
       }
+    fence_proxy_async_global();  // the o projection reads the output with TMA
     return;
   }
   // Push this split's normalised partial rows and log-sum-exps into the
@@ -294,6 +295,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
     dst[0] = __floats2half2_rn(num.x * id, num.y * id);
     dst[1] = __floats2half2_rn(num.z * id, num.w * id);
   }
+  fence_proxy_async_global();  // the o projection reads the output with TMA
 }
 
 }  // namespace

@@ -69,7 +69,8 @@ __device__ __forceinline__ int logical_row(int prow, int layout, int N) {
 // the epilogue's critical path except the residual read, issued in batches.
 template <int MT>
 __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float* gam, const int* pos,
-                         const float* gn, const float* rr, int nt, int z, int tlo, int thi, int warp, int lane) {
+                         const float* gn, const float* rr, __half* kout, __half* vout, int nt, int z, int tlo,
+                         int thi, int warp, int lane) {
   using G = Geo<MT>;
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
@@ -217,8 +218,8 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
         int row = prow0 + lane + 32 * i;
         __half hv = __float2half_rn(v[i]);
         if (kind == 0) a.out_h[(size_t)m * qd + row] = hv;
-        else if (kind == 1) a.kout[(size_t)m * kd + (row - qd)] = hv;
-        else a.vout[(size_t)m * kd + (row - qd - kd)] = hv;
+        else if (kind == 1) kout[(size_t)m * kd + (row - qd)] = hv;
+        else vout[(size_t)m * kd + (row - qd - kd)] = hv;
       }
     } else {  // EPI_KVCOMMIT: cache [b][nkv][cap][d]
 #pragma unroll
@@ -228,7 +229,7 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
         int rr = isv ? row - kd : row;
         int h = rr / a.d, e = rr - h * a.d;
         size_t off = (((size_t)seq * a.nkv + h) * a.cap + p) * a.d + e;
-        (isv ? a.vout : a.kout)[off] = __float2half_rn(v[i]);
+        (isv ? vout : kout)[off] = __float2half_rn(v[i]);
       }
     }
   }
@@ -248,7 +249,23 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
   int* s_pos = reinterpret_cast<int*>(s_gn + 128);                                           // [MCH]
   float* s_rr = reinterpret_cast<float*>(s_pos + G::MCH);                                    // [MCH]
 
-  const int nt = blockIdx.x, sp = blockIdx.y, z = blockIdx.z;
+  const int sp = blockIdx.y, z = blockIdx.z;
+  // this CTA's projection (one layer of a batched launch, or the only one)
+  int nt = blockIdx.x;
+  const uint8_t* wq = a.q;
+  const __half* wsc = a.s;
+  __half* kout = a.kout;
+  __half* vout = a.vout;
+  const float* gk = a.gk;
+  if (a.nl > 0) {
+    const int li = nt / a.ntl;
+    nt -= li * a.ntl;
+    wq = a.lq[li];
+    wsc = a.ls[li];
+    kout = a.lk[li];
+    vout = a.lv[li];
+    gk = a.lgk[li];
+  }
   const int KT = a.K / kTile;
   const int kt0 = (int)(((long long)sp * KT) / a.splits);
   const int kt1 = (int)(((long long)(sp + 1) * KT) / a.splits);
@@ -276,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
     // ---------------- producer ----------------
     if (lane == 0) {
       prefetch_tmap(&xmap);
-      const uint8_t* wsrc = a.q + ((size_t)((a.row0 >> 7) + nt) * KT + kt0) * kTileBytes;
+      const uint8_t* wsrc = wq + ((size_t)((a.row0 >> 7) + nt) * KT + kt0) * kTileBytes;
       const uint64_t pol = policy_evict_first();
       const int pre = nk < kStages ? nk : kStages;
       for (int i = 0; i < pre; ++i) {
@@ -305,10 +322,10 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
     {  // weights-side data first (independent of the preceding kernel)
       const int r = threadIdx.x;  // 0..127
       const int prow = a.row0 + nt * kTile + r;
-      s_sc[r] = __half2float(a.s[logical_row(prow, a.layout, a.N)]);
+      s_sc[r] = __half2float(wsc[logical_row(prow, a.layout, a.N)]);
       if (a.epi == EPI_QKV || a.epi == EPI_KVCOMMIT) {
         const int qd = a.nq * a.d;
-        const float* gsrc = (a.row0 + nt * kTile) < qd ? a.gq : a.gk;
+        const float* gsrc = (a.row0 + nt * kTile) < qd ? a.gq : gk;
         s_gam[r] = (gsrc && r < a.d) ? gsrc[r] : 1.f;
       }
       if (a.xg_out || a.hb_out) s_gn[r] = a.g_next[logical_row(prow, a.layout, a.N) - a.row0];
@@ -397,7 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
   }
   if (a.splits == 1) {
     __syncthreads();
-    epilogue<MT>(a, P, s_sc, s_gam, s_pos, s_gn, s_rr, nt, z, 0, G::MCH, warp, lane);
+    epilogue<MT>(a, P, s_sc, s_gam, s_pos, s_gn, s_rr, kout, vout, nt, z, 0, G::MCH, warp, lane);
+    // the next kernel reads these outputs with TMA (async proxy)
+    fence_proxy_async_global();
     return;
   }
   // ---- split-K reduction across the cluster through distributed smem ----
@@ -427,7 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
     *reinterpret_cast<float4*>(T + tok * G::TSTRIDE + 4 * c4) = accv;
   }
   cluster_sync();  // every peer has finished reading this CTA's partial
-  epilogue<MT>(a, T, s_sc, s_gam, s_pos, s_gn, s_rr, nt, z, tlo, thi, warp, lane);
+  epilogue<MT>(a, T, s_sc, s_gam, s_pos, s_gn, s_rr, kout, vout, nt, z, tlo, thi, warp, lane);
+  fence_proxy_async_global();  // the next kernel reads these outputs with TMA
 }
 
 // ------------------------------------------------------------- packing ----
@@ -562,7 +582,7 @@ cudaError_t w8_gemm(const W8Args& a0, const __half* x, cudaStream_t st, bool pdl
   const int mt = pick_mt(a.M);
   const int mch = mt * 8;
   const int chunks = (a.M + mch - 1) / mch;
-  const int ntiles = a.nrows / kTile;
+  const int ntiles = a.nrows / kTile * (a.nl > 0 ? a.nl : 1);
   const void* fn = mt == 2 ? (const void*)w8_gemm_kernel<2> : (const void*)w8_gemm_kernel<4>;
   const size_t smem = mt == 2 ? Geo<2>::SMEM : Geo<4>::SMEM;
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -169,6 +169,7 @@ __global__ void __launch_bounds__(kNormThreads) embed_rmsnorm_kernel(const __nv_
     if (c < n4) xr[c] = v[i];
   }
   store_f16_row(u + (size_t)m * H, H, v, inv, gamma);
+  fence_proxy_async_global();  // the next GEMM reads u with TMA
 }
 
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_f16_kernel(const float* x, int H, const float* gamma,
@@ -180,6 +181,7 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_f16_kernel(const float* 
   float inv = rsqrtf(load_row(x + (size_t)m * H, H, v, sh) / H + eps);
   pdl_trigger();
   store_f16_row(u + (size_t)m * H, H, v, inv, gamma);
+  fence_proxy_async_global();  // the next GEMM reads u with TMA
 }
 
 // rows 1..B-1 of every sequence: h = RMSNorm(x; gamma_final) as bf16
@@ -209,6 +211,7 @@ __global__ void __launch_bounds__(kNormThreads) final_norm_kernel(const float* x
       if (hidden_out) reinterpret_cast<float4*>(hidden_out + (size_t)o * H)[c] = y;
     }
   }
+  fence_proxy_async_global();  // the lm-head reads h with TMA
 }
 
 // len[j] += min(n[j] + 1, rows_per_seq) unless that would pass cap

@@ -9,7 +9,8 @@
 
 namespace dfl {
 
-constexpr int kTile = 128;         // packed W8 tile edge (rows x k-columns)
+constexpr int kTile = 128;
+constexpr int kLayersPerLaunch = 8;  // layers batched into one commit GEMM         // packed W8 tile edge (rows x k-columns)
 constexpr int kTileBytes = 16384;  // one packed int8 tile
 constexpr int kNumSMs = 152;
 
@@ -61,6 +62,16 @@ struct W8Args {
   // the argmax over each row's logits does not see.
   __nv_bfloat16* hb_out;
   int hb_rps;
+  // Several layers' projections in one launch (the K/V rows of every
+  // layer's qkv for a commit): tile columns [i ntl, (i + 1) ntl) of the grid
+  // belong to layer i < nl and use lq/ls/lk/lv/lgk[i] in place of
+  // q/s/kout/vout/gk.  nl = 0: a single projection.
+  int nl, ntl;
+  const uint8_t* lq[kLayersPerLaunch];
+  const __half* ls[kLayersPerLaunch];
+  __half* lk[kLayersPerLaunch];
+  __half* lv[kLayersPerLaunch];
+  const float* lgk[kLayersPerLaunch];
   // RoPE frequencies theta^(-2p/d), p < d/2, as float pairs hi + lo of the
   // double value (per-head epilogues)
   float inv_hi[64];
