@@ -39,8 +39,8 @@ FALLBACK_HBM_GBS = 6800.0
 # of the named kernel on the named workload, keyed by a hash of the kernel's
 # source file; ignored (reported null) once that source has changed.
 NCU_TRAFFIC = {
-    "lmhead_kernel": {"workload": "qwen3-4b-shaped-5L-h2560-b16-ctx512", "bytes": 780937216,
-                      "src": "44ee09dfad9f58df"},
+    "lmhead_kernel": {"workload": "qwen3-4b-shaped-5L-h2560-b16-ctx512", "bytes": 781344512,
+                      "src": "c2a3fcc391c2da2a"},
 }
 
 
@@ -384,7 +384,7 @@ def run_ours(args, rank, world, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=3000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
