@@ -172,17 +172,6 @@ __global__ void __launch_bounds__(kNormThreads) embed_rmsnorm_kernel(const __nv_
   fence_proxy_async_global();  // the next GEMM reads u with TMA
 }
 
-__global__ void __launch_bounds__(kNormThreads) rmsnorm_f16_kernel(const float* x, int H, const float* gamma,
-                                                                  float eps, __half* u) {
-  __shared__ float sh[32];
-  pdl_wait();
-  const int m = blockIdx.x;
-  float4 v[kNormVec];
-  float inv = rsqrtf(load_row(x + (size_t)m * H, H, v, sh) / H + eps);
-  pdl_trigger();
-  store_f16_row(u + (size_t)m * H, H, v, inv, gamma);
-  fence_proxy_async_global();  // the next GEMM reads u with TMA
-}
 
 // rows 1..B-1 of every sequence: h = RMSNorm(x; gamma_final) as bf16
 __global__ void __launch_bounds__(kNormThreads) final_norm_kernel(const float* x, int B, int H, const float* gamma,
@@ -354,11 +343,6 @@ cudaError_t embed_rmsnorm(const __nv_bfloat16* E, const int* last_tok, int mask_
   return launch_k((const void*)embed_rmsnorm_kernel, dim3(b * B), dim3(kNormThreads), 0, st, pdl, args);
 }
 
-cudaError_t rmsnorm_f16(const float* x, int M, int H, const float* gamma, float eps, __half* u, cudaStream_t st,
-                        bool pdl) {
-  void* args[] = {&x, &H, &gamma, &eps, &u};
-  return launch_k((const void*)rmsnorm_f16_kernel, dim3(M), dim3(kNormThreads), 0, st, pdl, args);
-}
 
 cudaError_t final_norm(const float* x, int b, int B, int H, const float* gamma, float eps, __nv_bfloat16* h,
                        float* hidden_out, cudaStream_t st, bool pdl) {

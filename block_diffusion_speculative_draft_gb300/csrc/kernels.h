@@ -127,8 +127,6 @@ cudaError_t attention(const AttnArgs& a, cudaStream_t st, bool pdl);
 cudaError_t embed_rmsnorm(const __nv_bfloat16* E, const int* last_tok, int mask_id, int V, int b, int B, int H,
                           const float* gamma, float eps, float* x, __half* u, cudaStream_t st, bool pdl,
                           int* status);
-cudaError_t rmsnorm_f16(const float* x, int M, int H, const float* gamma, float eps, __half* u, cudaStream_t st,
-                        bool pdl);
 cudaError_t final_norm(const float* x, int b, int B, int H, const float* gamma, float eps, __nv_bfloat16* h,
                        float* hidden_out, cudaStream_t st, bool pdl);
 cudaError_t commit_len_update(int* len, const int* nacc, int b, int rows_per_seq, int cap, cudaStream_t st,
