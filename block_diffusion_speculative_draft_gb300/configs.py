@@ -6,8 +6,8 @@ README, "How It Works": 5 drafter layers, block 32). Hidden sizes follow the
 Qwen3-4B / Qwen3-8B / 27B-class targets that the pages pair with their drafters
 (mirror-sd README, "Supported Models" and "Results" table).
 
-Conventions that the pages leave open are fixed here and listed in the design doc:
-RMSNorm eps 1e-6 and RoPE base 1e6 (Qwen3 conventions), mask token id V-1.
+Conventions that the pages leave open are fixed here: RMSNorm eps 1e-6 and
+RoPE base 1e6 (Qwen3 conventions), mask token id V-1.
 """
 from __future__ import annotations
 

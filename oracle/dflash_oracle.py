@@ -22,10 +22,10 @@ Sources (web pages on DFlash; cited by page title and section):
                conditioned on intermediate target activations, longest
                matching prefix accepted, one target forward verifies a block.
 
-Where the pages are silent the plainest reading is taken; every such reading
-is listed in DESIGN.md ("Readings of the pages").  Parity status of each
-function is stated in its docstring; the whole-drafter composition (norm
-placement, context path, RoPE base, eps) is "parity unpinned" by the pages.
+Where the pages are silent the plainest reading is taken and the docstring of
+the function that takes it says so.  Parity status of each function is stated
+in its docstring; the whole-drafter composition (norm placement, context path,
+RoPE base, eps) is "parity unpinned" by the pages.
 """
 from __future__ import annotations
 
