@@ -328,6 +328,89 @@ def verify_accept(logits: np.ndarray, draft: np.ndarray):
     return n, corr, emitted, next_tok
 
 
+# ----------------------------------------------------------------------------
+# temperature speculative-sampling accept  [mlx-dspark v0.0.3 release notes,
+# "Highlights": with --temperature > 0 the loop stays lossless, every emitted
+# token an exact sample from the target at temperature T, "via the same
+# acceptance rule as DSpark"]
+# ----------------------------------------------------------------------------
+def softmax_t(z: np.ndarray, T: float) -> np.ndarray:
+    """Target distribution at temperature T over the last axis, float64."""
+    zt = np.asarray(z, dtype=F64) / F64(T)
+    zt = zt - zt.max(axis=-1, keepdims=True)
+    e = np.exp(zt)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def gumbel_scores(z_row: np.ndarray, T: float, u: np.ndarray) -> np.ndarray:
+    """Gumbel-max scores z/T - log(-log u), in float32 (the precision the
+    sample decision is taken in): argmax of the scores is an exact draw from
+    softmax(z/T) when u is uniform on (0, 1).  Pinned: frequencies against
+    softmax_t."""
+    zf = np.asarray(z_row, dtype=np.float32) / np.float32(T)
+    uf = np.asarray(u, dtype=np.float32)
+    return zf - np.log(-np.log(uf))
+
+
+def verify_accept_sample(logits: np.ndarray, draft: np.ndarray, T: float, u_acc: np.ndarray,
+                         u_sample: np.ndarray, exclude_rejected: bool = True):
+    """One sequence of speculative sampling at temperature T > 0.
+
+    The pages name the property (an exact sample from the target at T) and
+    "the same acceptance rule as DSpark" without writing it out; the plainest
+    reading is the standard speculative-sampling rule.  This drafter proposes
+    greedily, so its proposal distribution q_i is one-hot at draft[i] and the
+    rule reads:
+
+      p_i  = softmax(logits[i] / T)
+      draft i (in order) is accepted iff u_acc[i] < min(1, p_i(x_i) / q_i(x_i)) = p_i(x_i)
+      n    = number of leading accepted drafts
+      corr = a draw from the residual max(0, p_n - q_n) (p_n without x_n,
+             renormalised) if n < D; a draw from p_D if n = D < R; -1 if
+             n = D = R
+      emitted / next_tok as in verify_accept.
+
+    The one categorical draw uses the Gumbel-max trick over u_sample[V] (one
+    uniform per vocabulary entry; the residual excludes x_n).  Random numbers
+    are inputs.  Accept probabilities are float64; the draw is decided in
+    float32 (gumbel_scores).  exclude_rejected=False is a deliberately wrong
+    variant kept for the negative-control test.
+
+    Pinned: T -> 0 equals verify_accept; emitted-token frequencies against
+    p_0 and p_1 by chi-square (a wrong residual fails).
+    Returns n, corr, emitted, next_tok, and diagnostics (accept probabilities,
+    the u - p margins, the top-2 score gap of the draw)."""
+    z = np.asarray(logits)
+    R, V = z.shape
+    x = np.asarray(draft, dtype=np.int64)
+    Dn = len(x)
+    p_acc = np.array([softmax_t(z[i], T)[x[i]] for i in range(Dn)], dtype=F64)
+    n = 0
+    while n < Dn and float(u_acc[n]) < p_acc[n]:
+        n += 1
+    row = n if n < Dn else (Dn if Dn < R else -1)
+    gap = np.inf
+    if row < 0:
+        corr = -1
+    else:
+        sc = gumbel_scores(z[row], T, u_sample).astype(F64)
+        if n < Dn and exclude_rejected:
+            sc[x[n]] = -np.inf
+        corr = int(argmax_lowest(sc))
+        srt = np.sort(sc)
+        gap = float(srt[-1] - srt[-2])
+    emitted = np.full(R, -1, dtype=np.int32)
+    emitted[:n] = x[:n]
+    if corr >= 0:
+        emitted[n] = corr
+        next_tok = corr
+    else:
+        next_tok = int(x[n - 1]) if n > 0 else -1
+    diag = {"p_accept": p_acc, "u_minus_p": np.asarray(u_acc[:Dn], dtype=F64) - p_acc, "row": row,
+            "score_gap": gap}
+    return n, corr, emitted, next_tok, diag
+
+
 def commit_rows(n: int, rows: int) -> int:
     """Rows of the verified block whose target hidden state enters the
     drafter's context: block inputs 0..n (the last token plus the n accepted
