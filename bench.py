@@ -279,6 +279,14 @@ def run_ours(args, rank, world, local_rank):
             g_fused = None
     VREP = 100
     g_verify = capture(lambda: api.dflash_verify_accept(logits, draft, n_out, corr, emitted, nxt, vws), VREP)
+    # temperature speculative-sampling accept on the same rows (T = 0.8,
+    # uniforms drawn once on the device)
+    u_acc = torch.rand((b, cfg.B - 1), device=dev).clamp_(1e-7, 1 - 1e-7)
+    u_smp = torch.rand((b, cfg.V), device=dev).clamp_(1e-7, 1 - 1e-7)
+    sws = torch.zeros(api.dflash_verify_sample_workspace_size(b, cfg.R, cfg.V), dtype=torch.uint8, device=dev)
+    s_n, s_c = torch.empty_like(n_out), torch.empty_like(corr)
+    g_sample = capture(lambda: api.dflash_verify_accept_sample(logits, draft, 0.8, u_acc, u_smp, s_n, s_c,
+                                                               ws=sws), VREP)
     M1 = b * (cfg.B - 1)
     lm_idx = torch.empty(M1, dtype=torch.int32, device=dev)
     lmws = torch.zeros(4096, dtype=torch.uint8, device=dev)
@@ -308,6 +316,7 @@ def run_ours(args, rank, world, local_rank):
     _, draft_ms = timed(g_draft, K, Wm)
     fused_ms = timed(g_fused, K, Wm)[1] if g_fused is not None else None
     _, ver_ms = timed(g_verify, max(3, K // 5), 2)
+    _, smp_ms = timed(g_sample, max(3, K // 5), 2)
     _, lm_ms = timed(g_lm, K, Wm)
     assert api.dflash_get_status() == 0, "device status flagged during the timed region"
 
@@ -369,6 +378,7 @@ def run_ours(args, rank, world, local_rank):
         "step_roofline": {"bytes": step_bytes, "frac_of_measured": step_bytes / (dms * 1e-3) / 1e9 / hbm,
                           "frac_of_8TBps": step_bytes / (dms * 1e-3) / 1e9 / 8000.0},
         "verify_accept_blocks_per_s": b / (statistics.median(ver_ms) / VREP / 1e3),
+        "verify_sample_blocks_per_s": b / (statistics.median(smp_ms) / VREP / 1e3),
         "roofline": {"kernel": "lmhead_kernel (bf16 GEMV + fused argmax)", "bound": "hbm", "achieved": lm_gbs,
                      "peak": hbm, "unit": "GB/s", "frac": lm_gbs / hbm, "traffic": traffic,
                      "peak_kind": peak_kind, "algorithmic_bytes_per_launch": lm_bytes},

@@ -27,7 +27,8 @@ EXPORTS = [
     "dflash_version", "dflash_status_string", "dflash_workspace_size", "dflash_pack_w8a16",
     "dflash_w8a16_linear_workspace_size", "dflash_w8a16_linear", "dflash_draft_block", "dflash_draft_block_fused",
     "dflash_lmhead_workspace_size", "dflash_lmhead_argmax", "dflash_verify_workspace_size",
-    "dflash_verify_accept", "dflash_verify_accept_noalloc", "dflash_kv_commit", "dflash_get_status",
+    "dflash_verify_accept", "dflash_verify_accept_noalloc", "dflash_verify_sample_workspace_size",
+    "dflash_verify_accept_sample", "dflash_kv_commit", "dflash_get_status",
 ]
 
 
@@ -90,6 +91,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dflash_verify_workspace_size": ([I32, I32, I64, PSZ], I32),
         "dflash_verify_accept": ([P, P, I32, I32, I32, I64, P, P, P, P, P, SZ, P], I32),
         "dflash_verify_accept_noalloc": ([P, P, I32, I32, I32, I64, P, P, P, P, P], I32),
+        "dflash_verify_sample_workspace_size": ([I32, I32, I64, PSZ], I32),
+        "dflash_verify_accept_sample": ([P, P, I32, I32, I32, I64, ctypes.c_float, P, P, P, P, P, P, P, SZ, P],
+                                        I32),
         "dflash_kv_commit": ([ctypes.POINTER(Weights), ctypes.POINTER(KV), P, I32, P, P, SZ, P], I32),
         "dflash_get_status": ([ctypes.POINTER(ctypes.c_int32), I32], I32),
     }
@@ -203,6 +207,29 @@ def dflash_verify_accept(logits, draft, n_out, corr_out, emitted=None, next_tok=
     _check("dflash_verify_accept", load_library().dflash_verify_accept(
         logits.data_ptr(), draft.data_ptr(), b, R, D, V, n_out.data_ptr(), corr_out.data_ptr(), _ptr(emitted),
         _ptr(next_tok), ws.data_ptr(), ws.numel(), _stream(stream)))
+
+
+def dflash_verify_sample_workspace_size(b: int, R: int, V: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("dflash_verify_sample_workspace_size",
+           load_library().dflash_verify_sample_workspace_size(b, R, V, ctypes.byref(n)))
+    return n.value
+
+
+def dflash_verify_accept_sample(logits, draft, temperature: float, u_accept, u_sample, n_out, corr_out,
+                                emitted=None, next_tok=None, ws=None, stream=None):
+    """Temperature speculative-sampling accept.  logits fp32 [b][R][V], draft
+    int32 [b][D], u_accept fp32 [b][D], u_sample fp32 [b][V] (uniforms in
+    (0, 1)), all device tensors."""
+    torch = _torch()
+    b, R, V = logits.shape
+    D = draft.shape[1]
+    if ws is None:
+        ws = torch.zeros(dflash_verify_sample_workspace_size(b, R, V), dtype=torch.uint8, device=logits.device)
+    _check("dflash_verify_accept_sample", load_library().dflash_verify_accept_sample(
+        logits.data_ptr(), draft.data_ptr(), b, R, D, V, float(temperature), u_accept.data_ptr(),
+        u_sample.data_ptr(), n_out.data_ptr(), corr_out.data_ptr(), _ptr(emitted), _ptr(next_tok),
+        ws.data_ptr(), ws.numel(), _stream(stream)))
 
 
 def dflash_verify_accept_noalloc(logits, draft, n_out, corr_out, emitted=None, next_tok=None, stream=None):

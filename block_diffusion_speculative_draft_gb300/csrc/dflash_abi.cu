@@ -558,6 +558,25 @@ int32_t dflash_verify_accept_noalloc(const float* logits, const int32_t* draft, 
                                        static_cast<cudaStream_t>(stream)));
 }
 
+int32_t dflash_verify_sample_workspace_size(int32_t b, int32_t R, int64_t V, size_t* bytes) {
+  if (!bytes || b < 1 || R < 1 || R > 64 || V < 1) return DFLASH_EINVAL;
+  *bytes = sample_ws_bytes(b, R, V);
+  return DFLASH_OK;
+}
+
+int32_t dflash_verify_accept_sample(const float* logits, const int32_t* draft, int32_t b, int32_t R, int32_t D,
+                                    int64_t V, float temperature, const float* u_accept, const float* u_sample,
+                                    int32_t* n_out, int32_t* corr_out, int32_t* emitted_out, int32_t* next_tok_out,
+                                    void* ws, size_t ws_bytes, void* stream) {
+  if (!logits || !draft || !u_accept || !u_sample || !n_out || !corr_out) return DFLASH_EINVAL;
+  if (b < 1 || R < 1 || R > 64 || D < 1 || D > R || V < 1 || V > ((int64_t)1 << 31) - 1) return DFLASH_EINVAL;
+  if (!(temperature > 0.f) || !(temperature < INFINITY)) return DFLASH_EINVAL;
+  if ((int64_t)b * R > 65535) return DFLASH_EUNSUPPORTED;
+  if (!ws || ws_bytes < sample_ws_bytes(b, R, V)) return DFLASH_EWORKSPACE;
+  return map_err(verify_sample(logits, draft, b, R, D, V, temperature, u_accept, u_sample, n_out, corr_out,
+                               emitted_out, next_tok_out, ws, static_cast<cudaStream_t>(stream), false));
+}
+
 int32_t dflash_kv_commit(const dflash_weights* w, const dflash_kv* kv, const uint16_t* hid, int32_t rows_per_seq,
                          const int32_t* n, void* ws, size_t ws_bytes, void* stream) {
   if (int r = check_weights(w)) return r;

@@ -131,6 +131,33 @@ cudaError_t final_norm(const float* x, int b, int B, int H, const float* gamma, 
                        float* hidden_out, cudaStream_t st, bool pdl);
 cudaError_t commit_len_update(int* len, const int* nacc, int b, int rows_per_seq, int cap, cudaStream_t st,
                               bool pdl, int* status);
+// --- temperature speculative-sampling accept (k_sample.cu) ---
+struct SampleArgs {
+  const float* logits;    // [b][R][V]
+  const int* draft;       // [b][D]
+  const float* u_acc;     // [b][D] uniforms in (0, 1)
+  const float* u_sample;  // [b][V] uniforms in (0, 1)
+  int b, R, D;
+  int64_t V;
+  float T;
+  int P, P2;              // vocabulary slices per row (stats) / per sequence (pick)
+  int64_t chunk, chunk2;  // slice lengths
+  int* tickets;           // [2b] zero between calls
+  float2* part;           // [b R][P] (max, exp-sum) of z / T per slice
+  float* zx;              // [b R] z / T of each row's draft token
+  int* sel;               // [b][2] row to sample (-1: none), token it excludes
+  unsigned long long* keys;  // [b][P2]
+  int* n_out;
+  int* corr_out;
+  int* emitted;
+  int* next_tok;
+};
+int sample_parts(int b, int R, int64_t V);
+int sample_parts2(int b, int64_t V);
+size_t sample_ws_bytes(int b, int R, int64_t V);
+cudaError_t verify_sample(const float* logits, const int* draft, int b, int R, int D, int64_t V, float T,
+                          const float* u_acc, const float* u_sample, int* n_out, int* corr_out, int* emitted,
+                          int* next_tok, void* ws, cudaStream_t st, bool pdl);
 size_t verify_ws_bytes(int b, int R, int64_t V);
 cudaError_t verify_accept(const float* logits, const int* draft, int b, int R, int D, int64_t V, int* n_out,
                           int* corr_out, int* emitted, int* next_tok, void* ws, cudaStream_t st, bool pdl);

@@ -275,6 +275,39 @@ DFLASH_API int32_t dflash_verify_accept_noalloc(const float* logits,
                                                 int32_t* next_tok_out,
                                                 void* stream);
 
+/* Workspace bytes for dflash_verify_accept_sample. */
+DFLASH_API int32_t dflash_verify_sample_workspace_size(int32_t b, int32_t R, int64_t V,
+                                                       size_t* bytes);
+
+/* Temperature speculative-sampling accept (mlx-dspark v0.0.3 release notes,
+ * "Highlights": with temperature T > 0 the loop stays lossless, each emitted
+ * token an exact sample from the target at T, "via the same acceptance rule
+ * as DSpark").  The pages do not write the rule out; this is the standard
+ * speculative-sampling rule for this drafter's greedy (one-hot) proposals.
+ * For each sequence j, with p_r = softmax(logits[j][r] / T):
+ *   draft i, in order, is accepted iff u_accept[j][i] < p_i(draft[j][i])
+ *   n    = number of leading accepted drafts
+ *   corr = a draw from p_n with draft[j][n] removed (renormalised) if n < D,
+ *          a draw from p_D if n = D < R, else -1
+ *   emitted / next_tok as in dflash_verify_accept.
+ * The draw is argmax_v logits[j][row][v] / T - log(-log u_sample[j][v])
+ * (Gumbel-max, decided in fp32, lowest index on ties).  The random numbers
+ * are inputs: u_accept [b][D] and u_sample [b][V] fp32 on the device, every
+ * value in the open interval (0, 1); values outside it give unspecified
+ * tokens.  temperature: finite, > 0.  Accept probabilities are formed in
+ * fp32 (max and exp-sum per vocabulary slice, merged in a fixed order).
+ * Other arguments, layouts and errors as in dflash_verify_accept; ws holds
+ * dflash_verify_sample_workspace_size bytes, zero-filled once (every call
+ * leaves its counters zero).  A draft token outside [0, V) has probability 0
+ * (rejected). */
+DFLASH_API int32_t dflash_verify_accept_sample(const float* logits, const int32_t* draft,
+                                               int32_t b, int32_t R, int32_t D, int64_t V,
+                                               float temperature, const float* u_accept,
+                                               const float* u_sample, int32_t* n_out,
+                                               int32_t* corr_out, int32_t* emitted_out,
+                                               int32_t* next_tok_out, void* ws,
+                                               size_t ws_bytes, void* stream);
+
 /* Draft-KV commit with rollback of the rejected suffix (mlx-dspark v0.0.3,
  * "Notes": KV rollback; dflash-mlx "What It Does": conditioning on target
  * hidden states).  hid: [b][rows_per_seq][k*H] fp16 target hidden rows of the

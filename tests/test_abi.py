@@ -74,6 +74,15 @@ def test_bad_arguments_rejected_on_host(lib):
     x = ctypes.c_void_p(16)
     assert lib.dflash_verify_accept(x, x, 1, 4, 5, 100, x, x, P, P, x, 1 << 20, P) == -1
     assert lib.dflash_pack_w8a16(x, 0, 100, 128, 0, x, x, P) == -2
+    # sampling accept: temperature must be finite and > 0, uniforms present,
+    # workspace large enough
+    ws_need = api.dflash_verify_sample_workspace_size(1, 4, 100)
+    assert ws_need > 0
+    for T in (0.0, -1.0, float("inf"), float("nan")):
+        assert lib.dflash_verify_accept_sample(x, x, 1, 4, 3, 100, T, x, x, x, x, P, P, x, ws_need, P) == -1
+    assert lib.dflash_verify_accept_sample(x, x, 1, 4, 3, 100, 1.0, P, x, x, x, P, P, x, ws_need, P) == -1
+    assert lib.dflash_verify_accept_sample(x, x, 1, 4, 5, 100, 1.0, x, x, x, x, P, P, x, ws_need, P) == -1
+    assert lib.dflash_verify_accept_sample(x, x, 1, 4, 3, 100, 1.0, x, x, x, x, P, P, x, ws_need - 1, P) == -5
 
 
 def test_weights_struct_checked_before_launch(lib):
