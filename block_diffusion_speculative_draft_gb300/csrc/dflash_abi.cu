@@ -152,6 +152,11 @@ WS carve(const dflash_config& c, int b, int rps, uint8_t* base) {
 
 int map_err(cudaError_t e) { return e == cudaSuccess ? DFLASH_OK : DFLASH_ECUDA; }
 
+// Every launch, the first of a call included, allows programmatic dependent
+// launch: each kernel reads nothing but constant weights before its
+// griddepcontrol.wait, so it may start while the stream's previous kernel
+// (of this call or of an earlier one) is still finishing.
+
 W8Args base_args(const dflash_w8& w, int M, int epi) {
   W8Args a;
   memset(&a, 0, sizeof(a));
@@ -231,7 +236,7 @@ int32_t dflash_w8a16_linear(const dflash_w8* w, const uint16_t* x, int64_t M, fl
   W8Args a = base_args(*w, (int)M, EPI_STORE_F32);
   a.out_f32 = y;
   a.ldo = (int)w->N;
-  return map_err(w8_gemm(a, reinterpret_cast<const __half*>(x), static_cast<cudaStream_t>(stream), false));
+  return map_err(w8_gemm(a, reinterpret_cast<const __half*>(x), static_cast<cudaStream_t>(stream), true));
 }
 
 int32_t dflash_w8a16_linear_workspace_size(int64_t M, int64_t N, int64_t K, size_t* bytes) {
@@ -398,7 +403,7 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
   if (lm_rows > 128) lm_rows = 128;
   const uint32_t lm_pf_bytes = (uint32_t)(lm_rows * row_bytes);
   e = embed_rmsnorm(reinterpret_cast<const __nv_bfloat16*>(w->embed), last_tok, c.mask_id, c.V, b, c.B, c.H,
-                    w->gamma_in, c.eps, s.x, s.u, st, false, status);
+                    w->gamma_in, c.eps, s.x, s.u, st, true, status);
   if (e != cudaSuccess) return DFLASH_ECUDA;
   for (int l = 0; l < c.L; ++l) {
     // [q|k|v] = W8(qkv) u ; per-head QK-RMSNorm + neox RoPE in the epilogue
@@ -524,7 +529,7 @@ int32_t dflash_lmhead_argmax(const uint16_t* h, const uint16_t* w, int64_t M, in
   if (!status) return DFLASH_ECUDA;
   return map_err(lmhead_argmax(reinterpret_cast<const __nv_bfloat16*>(h), reinterpret_cast<const __nv_bfloat16*>(w),
                                (int)M, (int)V, (int)H, idx_out, maxlogit_out, logits_out, ws,
-                               static_cast<cudaStream_t>(stream), false, status));
+                               static_cast<cudaStream_t>(stream), true, status));
 }
 
 int32_t dflash_verify_workspace_size(int32_t b, int32_t R, int64_t V, size_t* bytes) {
@@ -542,7 +547,7 @@ int32_t dflash_verify_accept(const float* logits, const int32_t* draft, int32_t 
   if (!ws || ws_bytes < verify_ws_bytes(b, R, V)) return DFLASH_EWORKSPACE;
   if ((V & 3) == 0 && !aligned16(logits)) return DFLASH_EINVAL;
   return map_err(verify_accept(logits, draft, b, R, D, V, n_out, corr_out, emitted_out, next_tok_out, ws,
-                               static_cast<cudaStream_t>(stream), false));
+                               static_cast<cudaStream_t>(stream), true));
 }
 
 int32_t dflash_verify_accept_noalloc(const float* logits, const int32_t* draft, int32_t b, int32_t R, int32_t D,
@@ -574,7 +579,7 @@ int32_t dflash_verify_accept_sample(const float* logits, const int32_t* draft, i
   if ((int64_t)b * R > 65535) return DFLASH_EUNSUPPORTED;
   if (!ws || ws_bytes < sample_ws_bytes(b, R, V)) return DFLASH_EWORKSPACE;
   return map_err(verify_sample(logits, draft, b, R, D, V, temperature, u_accept, u_sample, n_out, corr_out,
-                               emitted_out, next_tok_out, ws, static_cast<cudaStream_t>(stream), false));
+                               emitted_out, next_tok_out, ws, static_cast<cudaStream_t>(stream), true));
 }
 
 int32_t dflash_kv_commit(const dflash_weights* w, const dflash_kv* kv, const uint16_t* hid, int32_t rows_per_seq,
@@ -604,7 +609,7 @@ int32_t dflash_kv_commit(const dflash_weights* w, const dflash_kv* kv, const uin
   af.g_next = w->gamma_hid;
   af.ss_out = s.ss;
   af.nss_out = c.H / 128;
-  if ((e = w8_gemm(af, reinterpret_cast<const __half*>(hid), st, false)) != cudaSuccess) return DFLASH_ECUDA;
+  if ((e = w8_gemm(af, reinterpret_cast<const __half*>(hid), st, true)) != cudaSuccess) return DFLASH_ECUDA;
   // K = rope(knorm(W_k c)), V = W_v c for every layer: the K/V rows of each
   // layer's qkv projection, up to kLayersPerLaunch layers in one launch
   for (int l0 = 0; l0 < c.L; l0 += kLayersPerLaunch) {

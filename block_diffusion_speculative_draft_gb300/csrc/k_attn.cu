@@ -6,7 +6,9 @@
 //
 // One CTA per (context split, kv head, sequence).  The B block rows times the
 // nq/nkv query heads that share a kv head form one query tile (64 rows for
-// B = 16, group 4), so every K/V byte is read once per kv head.  Long contexts
+// B = 16, group 4), so every K/V byte is read once per kv head.  One compute
+// warp per 16 query rows; as many helper warps again (up to 10 warps in all)
+// share the copies and the split merge, which are latency-bound.  Long contexts
 // are split along the keys (flash-decoding; the pages' long-context verify
 // likewise uses a two-pass attention, dflash-mlx summary, "기술적 도전":
 // JIT SDPA 2-pass for N >= 1024): the splits of one (sequence, kv head) form
@@ -48,8 +50,8 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
   const int ns = gridDim.x;
   const int grp = a.nq / a.nkv;
   const int rows = a.B * grp;
-  const int nw = blockDim.x >> 5;
-  const int rows_pad = nw * 16;
+  const int nwc = a.nwc;
+  const int rows_pad = nwc * 16;
   uint8_t* sQ = smem;
   uint8_t* sK = sQ + rows_pad * RB;        // [2][64][D]
   uint8_t* sV = sK + 2 * kKT * RB;         // [2][64][D]
@@ -129,6 +131,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
     cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();
+    if (warp < nwc) {
     if (it == 0) {
       const uint32_t qb = smem_u32(sQ);
 #pragma unroll
@@ -223,6 +226,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
         mma_f16(o[2 * dp + 1], pf[kk], b2, b3);
       }
     }
+    }
     __syncthreads();
   }
   pdl_trigger();
@@ -235,6 +239,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
     lse[r] = lrow[r] > 0.f ? mrow[r] + log2f(lrow[r]) : -INFINITY;
   }
   if (ns == 1) {
+    if (warp < nwc)
 #pragma unroll
     for (int i = 0; i < D / 8; ++i)
 #pragma unroll
@@ -260,6 +265,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
   const uint32_t rObase = smem_u32(rO), rLbase = smem_u32(rL);
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
+    if (warp >= nwc) break;
     const int rho = warp * 16 + g8 + 8 * h;
     if (rho >= rows) continue;
     const int own = ((rho + 1) * ns - 1) / rows;
@@ -344,6 +350,8 @@ cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
   const int rows = a.B * (a.nq / a.nkv);
   const int nw = (rows + 15) / 16;
   const int rows_pad = nw * 16;
+  a.nwc = nw;
+  const int nthr = (2 * nw < 10 ? 2 * nw : (nw > 10 ? nw : 10)) * 32;
   const void* fn = a.d == 128 ? (const void*)attn_kernel<128> : (const void*)attn_kernel<64>;
   // one 64-key tile per split while the longest possible context allows it,
   // so the (latency-bound) pass is as short as the split count permits
@@ -361,7 +369,7 @@ cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
   };
   size_t smem = smem_for(ns);
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (ns > kPortable && !attn_cluster_fits(fn, ns, nw * 32, smem)) {
+  if (ns > kPortable && !attn_cluster_fits(fn, ns, nthr, smem)) {
     ns = kPortable;
     smem = smem_for(ns);
     cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -369,7 +377,7 @@ cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
   a.max_splits = ns;
   dim3 grid(ns, a.nkv, a.b);
   void* args[] = {&a};
-  return launch_kc(fn, grid, dim3(nw * 32), smem, st, pdl, dim3(ns, 1, 1), args);
+  return launch_kc(fn, grid, dim3(nthr), smem, st, pdl, dim3(ns, 1, 1), args);
 }
 
 }  // namespace dfl

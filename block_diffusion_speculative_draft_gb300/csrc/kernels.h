@@ -114,6 +114,7 @@ struct AttnArgs {
   int b, B, nq, nkv, d, cap;
   int max_splits;
   int* status;
+  int nwc;  // compute warps (16 query rows each); the rest help with loads and the merge
   // L2 prefetch issued while the kernel would otherwise leave HBM idle:
   // pieces [pf_i0, pf_i1) of base + i * pf_stride, pf_bytes each (or none)
   const uint8_t* pf_base;
