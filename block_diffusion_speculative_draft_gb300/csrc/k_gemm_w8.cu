@@ -337,7 +337,19 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
       float rf = 0.f;
       if (m < a.M) {
         float sum = 0.f;
-        for (int i = 0; i < a.nss_in; ++i) sum += a.ss_in[(size_t)m * a.nss_in + i];
+        const float* row = a.ss_in + (size_t)m * a.nss_in;
+        if ((a.nss_in & 3) == 0 && a.nss_in <= 64) {
+          // every partial in flight at once (one round trip), summed in order
+          float4 v[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            if (4 * q < a.nss_in) v[q] = reinterpret_cast<const float4*>(row)[q];
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            if (4 * q < a.nss_in) sum += ((v[q].x + v[q].y) + (v[q].z + v[q].w));
+        } else {
+          for (int i = 0; i < a.nss_in; ++i) sum += row[i];
+        }
         rf = rsqrtf(sum / a.K + a.eps);
       }
       s_rr[threadIdx.x] = rf;
