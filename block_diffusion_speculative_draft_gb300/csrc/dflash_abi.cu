@@ -599,7 +599,6 @@ int32_t dflash_kv_commit(const dflash_weights* w, const dflash_kv* kv, const uin
   if (!status) return DFLASH_ECUDA;
   const int Mc = b * rows_per_seq;
   const size_t layer_kv = (size_t)b * c.nkv * kv->cap * c.d;
-  cudaError_t e;
   // c = RMSNorm(W8(fc) h; gamma_hid)
   // the epilogue writes u = y * gamma_hid and the row sums of squares; the
   // K/V GEMMs apply the RMSNorm factor to their results
@@ -609,7 +608,7 @@ int32_t dflash_kv_commit(const dflash_weights* w, const dflash_kv* kv, const uin
   af.g_next = w->gamma_hid;
   af.ss_out = s.ss;
   af.nss_out = c.H / 128;
-  if ((e = w8_gemm(af, reinterpret_cast<const __half*>(hid), st, true)) != cudaSuccess) return DFLASH_ECUDA;
+  if (w8_gemm(af, reinterpret_cast<const __half*>(hid), st, true) != cudaSuccess) return DFLASH_ECUDA;
   // K = rope(knorm(W_k c)), V = W_v c for every layer: the K/V rows of each
   // layer's qkv projection, up to kLayersPerLaunch layers in one launch
   for (int l0 = 0; l0 < c.L; l0 += kLayersPerLaunch) {
@@ -640,7 +639,7 @@ int32_t dflash_kv_commit(const dflash_weights* w, const dflash_kv* kv, const uin
     a.cap = kv->cap;
     a.ss_in = s.ss;
     a.nss_in = c.H / 128;
-    if ((e = w8_gemm(a, s.u, st, true)) != cudaSuccess) return DFLASH_ECUDA;
+    if (w8_gemm(a, s.u, st, true) != cudaSuccess) return DFLASH_ECUDA;
   }
   return map_err(commit_len_update(kv->len, n, b, rows_per_seq, kv->cap, st, true, status));
 }
