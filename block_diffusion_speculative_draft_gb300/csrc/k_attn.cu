@@ -356,6 +356,11 @@ cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
   // one 64-key tile per split while the longest possible context allows it,
   // so the (latency-bound) pass is as short as the split count permits
   int ns = (a.cap + a.B + kKT - 1) / kKT;
+  // no more splits than keep about two CTAs per SM busy when the batch and
+  // the kv heads already fill the GPU (a grid of several waves costs more than
+  // longer splits)
+  const int fill = (2 * kNumSMs + a.b * a.nkv - 1) / (a.b * a.nkv);
+  if (ns > fill) ns = fill;
   if (ns > kMaxSplits) ns = kMaxSplits;
   if (ns < 1) ns = 1;
   auto smem_for = [&](int n) {
