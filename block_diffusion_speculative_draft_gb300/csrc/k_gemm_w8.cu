@@ -12,7 +12,10 @@
 //    (the packer lays each tile out in MMA-fragment order, so a copy needs no
 //    tensor map and every consumer lane reads 16 contiguous bytes), and the
 //    matching 128-column activation slice with a 2-D TMA load (128-byte
-//    swizzle, rows past M zero-filled), into a 4-stage mbarrier ring;
+//    swizzle, rows past M zero-filled), into a 4-stage mbarrier ring (3
+//    stages for 64-row chunks, which keeps two CTAs per SM);
+//  * activation rows are taken 16, 32 or 64 at a time per CTA; chunks of
+//    one weight tile are adjacent in launch order and share it through L2;
 //  * consumer warps turn biased int8 into fp16 exactly in registers and issue
 //    m16n8k16 MMAs with fp32 accumulation; the scale is applied after the
 //    K reduction;
@@ -34,22 +37,22 @@ namespace dfl {
 
 namespace {
 
-constexpr int kStages = 4;
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
 template <int MT>
 struct Geo {
   static constexpr int MCH = MT * 8;          // activation rows per chunk
+  static constexpr int NST = MT >= 8 ? 3 : 4;  // ring stages (3 keeps two 64-row CTAs per SM)
   static constexpr int ABYTES = 2 * MCH * 128;  // two [MCH][64] fp16 halves
   static constexpr int STAGE = kTileBytes + ABYTES;
   static constexpr int TSTRIDE = 132;  // epilogue tile row stride (floats)
   static constexpr int TBYTES = (MCH * TSTRIDE * 4 + 1023) / 1024 * 1024;
-  static_assert(2 * TBYTES <= kStages * STAGE, "epilogue tiles must fit in the ring");
+  static_assert(2 * TBYTES <= NST * STAGE, "epilogue tiles must fit in the ring");
   // side data after the barriers: row scales, gamma, next gamma, per-row
   // positions, per-row norm factors
   static constexpr int SIDE = 128 * 4 + 128 * 4 + 128 * 4 + MCH * 4 + MCH * 4;
-  static constexpr size_t SMEM = 1024 + kStages * (size_t)STAGE + 2 * kStages * 8 + 64 + SIDE;
+  static constexpr size_t SMEM = 1024 + NST * (size_t)STAGE + 2 * NST * 8 + 64 + SIDE;
 };
 
 // packed row -> logical row
@@ -241,9 +244,9 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
   using G = Geo<MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * G::STAGE);
-  uint64_t* empty = full + kStages;
-  float* s_sc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(empty + kStages) + 64);  // [128]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::NST * G::STAGE);
+  uint64_t* empty = full + G::NST;
+  float* s_sc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(empty + G::NST) + 64);  // [128]
   float* s_gam = s_sc + 128;                                                                 // [128]
   float* s_gn = s_gam + 128;                                                                 // [128]
   int* s_pos = reinterpret_cast<int*>(s_gn + 128);                                           // [MCH]
@@ -273,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < G::NST; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
@@ -295,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
       prefetch_tmap(&xmap);
       const uint8_t* wsrc = wq + ((size_t)((a.row0 >> 7) + nt) * KT + kt0) * kTileBytes;
       const uint64_t pol = policy_evict_first();
-      const int pre = nk < kStages ? nk : kStages;
+      const int pre = nk < G::NST ? nk : G::NST;
       for (int i = 0; i < pre; ++i) {
         mbar_arrive_expect_tx(&full[i], G::STAGE);
         bulk_g2s_hint(smem + i * G::STAGE, wsrc + (size_t)i * kTileBytes, kTileBytes, &full[i], pol);
@@ -307,8 +310,8 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
         tma_load_2d(sa + G::MCH * 128, &xmap, (kt0 + i) * kTile + 64, z * G::MCH, &full[i]);
       }
       for (int i = pre; i < nk; ++i) {
-        const int slot = i % kStages;
-        if (!mbar_wait(&empty[slot], ((i / kStages) - 1) & 1, a.status)) break;
+        const int slot = i % G::NST;
+        if (!mbar_wait(&empty[slot], ((i / G::NST) - 1) & 1, a.status)) break;
         mbar_arrive_expect_tx(&full[slot], G::STAGE);
         uint8_t* st = smem + slot * G::STAGE;
         bulk_g2s_hint(st, wsrc + (size_t)i * kTileBytes, kTileBytes, &full[slot], pol);
@@ -375,8 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
     const int g_tok_lo = (lane & 7) + ((lane >> 4) << 3);
     const int ch_hi = (lane >> 3) & 1;
     for (int i = 0; i < nk; ++i) {
-      const int slot = i % kStages;
-      if (!mbar_wait(&full[slot], (i / kStages) & 1, a.status)) break;
+      const int slot = i % G::NST;
+      if (!mbar_wait(&full[slot], (i / G::NST) & 1, a.status)) break;
       const uint8_t* wl = smem + slot * G::STAGE + (warp * 8 * 32 + lane) * 16;
       const uint32_t abase = smem_u32(smem + slot * G::STAGE + kTileBytes);
 #pragma unroll
@@ -551,7 +554,7 @@ int w8_pick_splits(int units, int KT) {
   return s;
 }
 
-static int pick_mt(int M) { return M <= 16 ? 2 : 4; }
+static int pick_mt(int M) { return M <= 16 ? 2 : (M <= 32 ? 4 : 8); }
 
 // How many clusters of (1, s, 1) CTAs can be resident at once: clusters are
 // placed within one GPC, so sizes that do not divide a GPC's CTA slots leave
@@ -595,8 +598,9 @@ cudaError_t w8_gemm(const W8Args& a0, const __half* x, cudaStream_t st, bool pdl
   const int mch = mt * 8;
   const int chunks = (a.M + mch - 1) / mch;
   const int ntiles = a.nrows / kTile * (a.nl > 0 ? a.nl : 1);
-  const void* fn = mt == 2 ? (const void*)w8_gemm_kernel<2> : (const void*)w8_gemm_kernel<4>;
-  const size_t smem = mt == 2 ? Geo<2>::SMEM : Geo<4>::SMEM;
+  const void* fn = mt == 2 ? (const void*)w8_gemm_kernel<2>
+                  : mt == 4 ? (const void*)w8_gemm_kernel<4> : (const void*)w8_gemm_kernel<8>;
+  const size_t smem = mt == 2 ? Geo<2>::SMEM : mt == 4 ? Geo<4>::SMEM : Geo<8>::SMEM;
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const int units = chunks * ntiles;
   a.splits = w8_pick_splits(units, a.K / kTile);
