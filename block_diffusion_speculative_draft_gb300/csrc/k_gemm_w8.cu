@@ -14,8 +14,8 @@
 //    matching 128-column activation slice with a 2-D TMA load (128-byte
 //    swizzle, rows past M zero-filled), into a 4-stage mbarrier ring (3
 //    stages for 64-row chunks, which keeps two CTAs per SM);
-//  * activation rows are taken 16, 32 or 64 at a time per CTA; chunks of
-//    one weight tile are adjacent in launch order and share it through L2;
+//  * activation rows are taken 16, 32 or 64 at a time per CTA (one chunk
+//    per grid z index); larger M runs several chunks of the same tiles;
 //  * consumer warps turn biased int8 into fp16 exactly in registers and issue
 //    m16n8k16 MMAs with fp32 accumulation; the scale is applied after the
 //    K reduction;
