@@ -8,7 +8,8 @@
 // nq/nkv query heads that share a kv head form one query tile (64 rows for
 // B = 16, group 4), so every K/V byte is read once per kv head.  One compute
 // warp per 16 query rows; as many helper warps again (up to 10 warps in all)
-// share the copies and the split merge, which are latency-bound.  Long contexts
+// share the copies and the split merge, which are latency-bound, and, when a
+// split spans several tiles, compute the second key half of every tile.  Long contexts
 // are split along the keys (flash-decoding; the pages' long-context verify
 // likewise uses a two-pass attention, dflash-mlx summary, "기술적 도전":
 // JIT SDPA 2-pass for N >= 1024): the splits of one (sequence, kv head) form
@@ -41,7 +42,7 @@ __device__ __forceinline__ void split_range(int total, int sp, int ns, int& k0, 
   k1 = min(total, k0 + chunk);
 }
 
-template <int D>
+template <int D, int KH>
 __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
   constexpr int RB = D * 2;  // bytes per row
   extern __shared__ uint8_t smem_raw[];
@@ -126,108 +127,160 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
   uint32_t qf[D / 16][4];
 
+  // KH = 2: warp w computes row block w % nwc over key half w / nwc of every
+  // tile, each half with its own online softmax, merged once after the last
+  // tile; KH = 1: one warp per row block over all 64 keys of a tile
+  constexpr int KK = kKT / KH;  // keys per warp and tile
+  constexpr int NN = KK / 8;    // n8 score tiles per warp
+  const int rb = warp % nwc, half = warp / nwc;
+  const bool cw = warp < nwc * KH;
   for (int it = 0; it < ntile; ++it) {
     if (it + 1 < ntile) load_kv((it + 1) & 1, k0 + (it + 1) * kKT, 2);
     cp_async_commit();
     cp_async_wait<1>();
     __syncthreads();
-    if (warp < nwc) {
-    if (it == 0) {
-      const uint32_t qb = smem_u32(sQ);
+    if (cw) {
+      if (it == 0) {
+        const uint32_t qb = smem_u32(sQ);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          int row = rb * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          int ch = 2 * ks + (lane >> 4);
+          ldsm_x4(qb + row * RB + ((ch ^ (row & 7)) << 4), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+        }
+      }
+      const int buf = it & 1;
+      const uint32_t kb = smem_u32(sK + buf * kKT * RB);
+      const uint32_t vb = smem_u32(sV + buf * kKT * RB);
+      // S = Q K^T : 16 rows x KK keys per warp
+      float s[NN][4];
+#pragma unroll
+      for (int n = 0; n < NN; ++n)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) s[n][e] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < D / 16; ++ks) {
-        int row = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        int ch = 2 * ks + (lane >> 4);
-        ldsm_x4(qb + row * RB + ((ch ^ (row & 7)) << 4), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+#pragma unroll
+        for (int n16 = 0; n16 < NN / 2; ++n16) {
+          int key = half * KK + n16 * 16 + (lane & 7) + ((lane >> 4) << 3);
+          int ch = 2 * ks + ((lane >> 3) & 1);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(kb + key * RB + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+          mma_f16(s[2 * n16], qf[ks], b0, b1);
+          mma_f16(s[2 * n16 + 1], qf[ks], b2, b3);
+        }
       }
-    }
-    const int buf = it & 1;
-    const uint32_t kb = smem_u32(sK + buf * kKT * RB);
-    const uint32_t vb = smem_u32(sV + buf * kKT * RB);
-    // S = Q K^T : 16 rows x 64 keys per warp
-    float s[8][4];
+      // scale, mask, online softmax (rows g8 and g8 + 8 of this warp); a half
+      // may see no valid key yet: its max stays -inf and contributes nothing
+      const int kbase = k0 + it * kKT + half * KK;
+      float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
+      for (int n = 0; n < NN; ++n)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) s[n][e] = 0.f;
+        for (int e = 0; e < 4; ++e) {
+          int key = kbase + n * 8 + 2 * t4 + (e & 1);
+          float v = key < k1 ? s[n][e] * sl2 : -INFINITY;
+          s[n][e] = v;
+          mx[e >> 1] = fmaxf(mx[e >> 1], v);
+        }
 #pragma unroll
-    for (int ks = 0; ks < D / 16; ++ks) {
-#pragma unroll
-      for (int n16 = 0; n16 < 4; ++n16) {
-        int key = n16 * 16 + (lane & 7) + ((lane >> 4) << 3);
-        int ch = 2 * ks + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(kb + key * RB + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
-        mma_f16(s[2 * n16], qf[ks], b0, b1);
-        mma_f16(s[2 * n16 + 1], qf[ks], b2, b3);
+      for (int r = 0; r < 2; ++r) {
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
       }
-    }
-    // scale, mask, online softmax (rows g8 and g8 + 8 of this warp)
-    const int kbase = k0 + it * kKT;
-    float mx[2] = {-INFINITY, -INFINITY};
+      float corr[2], mnew[2], rs[2] = {0.f, 0.f};
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
+      for (int r = 0; r < 2; ++r) {
+        mnew[r] = fmaxf(mrow[r], mx[r]);
+        corr[r] = mnew[r] == -INFINITY ? 1.f : exp2f(mrow[r] - mnew[r]);
+        mrow[r] = mnew[r];
+      }
+      uint32_t pf[NN / 2][4];  // P as the A operand of P.V, k16 steps over KK keys
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        int key = kbase + n * 8 + 2 * t4 + (e & 1);
-        float v = key < k1 ? s[n][e] * sl2 : -INFINITY;
-        s[n][e] = v;
-        mx[e >> 1] = fmaxf(mx[e >> 1], v);
+      for (int n = 0; n < NN; ++n) {
+        const float q0 = mnew[0] == -INFINITY ? 0.f : mnew[0];
+        const float q1 = mnew[1] == -INFINITY ? 0.f : mnew[1];
+        float p0 = exp2f(s[n][0] - q0);
+        float p1 = exp2f(s[n][1] - q0);
+        float p2 = exp2f(s[n][2] - q1);
+        float p3 = exp2f(s[n][3] - q1);
+        rs[0] += p0 + p1;
+        rs[1] += p2 + p3;
+        __half2 h01 = __floats2half2_rn(p0, p1);
+        __half2 h23 = __floats2half2_rn(p2, p3);
+        pf[n >> 1][(n & 1) * 2 + 0] = *reinterpret_cast<uint32_t*>(&h01);
+        pf[n >> 1][(n & 1) * 2 + 1] = *reinterpret_cast<uint32_t*>(&h23);
       }
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
-      mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-    }
-    float corr[2], mnew[2], rs[2] = {0.f, 0.f};
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      mnew[r] = fmaxf(mrow[r], mx[r]);
-      corr[r] = exp2f(mrow[r] - mnew[r]);
-      mrow[r] = mnew[r];
-    }
-    uint32_t pf[4][4];  // P as the A operand of P.V, 4 k16 steps over 64 keys
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      float p0 = exp2f(s[n][0] - mnew[0]);
-      float p1 = exp2f(s[n][1] - mnew[0]);
-      float p2 = exp2f(s[n][2] - mnew[1]);
-      float p3 = exp2f(s[n][3] - mnew[1]);
-      rs[0] += p0 + p1;
-      rs[1] += p2 + p3;
-      __half2 h01 = __floats2half2_rn(p0, p1);
-      __half2 h23 = __floats2half2_rn(p2, p3);
-      pf[n >> 1][(n & 1) * 2 + 0] = *reinterpret_cast<uint32_t*>(&h01);
-      pf[n >> 1][(n & 1) * 2 + 1] = *reinterpret_cast<uint32_t*>(&h23);
-    }
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      rs[r] += __shfl_xor_sync(0xffffffffu, rs[r], 1);
-      rs[r] += __shfl_xor_sync(0xffffffffu, rs[r], 2);
-      lrow[r] = lrow[r] * corr[r] + rs[r];
-    }
-#pragma unroll
-    for (int i = 0; i < D / 8; ++i) {
-      o[i][0] *= corr[0];
-      o[i][1] *= corr[0];
-      o[i][2] *= corr[1];
-      o[i][3] *= corr[1];
-    }
-    // O += P V
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk) {
-#pragma unroll
-      for (int dp = 0; dp < D / 16; ++dp) {
-        int key = kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-        int ch = 2 * dp + (lane >> 4);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(vb + key * RB + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
-        mma_f16(o[2 * dp], pf[kk], b0, b1);
-        mma_f16(o[2 * dp + 1], pf[kk], b2, b3);
+      for (int r = 0; r < 2; ++r) {
+        rs[r] += __shfl_xor_sync(0xffffffffu, rs[r], 1);
+        rs[r] += __shfl_xor_sync(0xffffffffu, rs[r], 2);
+        lrow[r] = lrow[r] * corr[r] + rs[r];
       }
-    }
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i) {
+        o[i][0] *= corr[0];
+        o[i][1] *= corr[0];
+        o[i][2] *= corr[1];
+        o[i][3] *= corr[1];
+      }
+      // O += P V
+#pragma unroll
+      for (int kk = 0; kk < NN / 2; ++kk) {
+#pragma unroll
+        for (int dp = 0; dp < D / 16; ++dp) {
+          int key = half * KK + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          int ch = 2 * dp + (lane >> 4);
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(vb + key * RB + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+          mma_f16(o[2 * dp], pf[kk], b0, b1);
+          mma_f16(o[2 * dp + 1], pf[kk], b2, b3);
+        }
+      }
     }
     __syncthreads();
+  }
+  if (KH == 2) {
+    // merge the key halves of each row block: half 1 hands (max, sum, O) over
+    // through shared memory (the K/V buffers are free once the copies land)
+    constexpr int XS = D + 4;  // row stride (floats)
+    cp_async_wait<0>();
+    __syncthreads();
+    float* xo = reinterpret_cast<float*>(sK);  // [nwc][16][XS]
+    float* xm = xo + (size_t)nwc * 16 * XS;    // [nwc][16]
+    float* xl = xm + nwc * 16;                 // [nwc][16]
+    if (cw && half == 1) {
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          xo[(rb * 16 + g8 + ((e >> 1) << 3)) * XS + i * 8 + 2 * t4 + (e & 1)] = o[i][e];
+      if (t4 == 0) {
+        xm[rb * 16 + g8] = mrow[0];
+        xm[rb * 16 + g8 + 8] = mrow[1];
+        xl[rb * 16 + g8] = lrow[0];
+        xl[rb * 16 + g8 + 8] = lrow[1];
+      }
+    }
+    __syncthreads();
+    if (cw && half == 0) {
+      float c0[2], c1[2];
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const float m1 = xm[rb * 16 + g8 + 8 * r], l1 = xl[rb * 16 + g8 + 8 * r];
+        const float mn = fmaxf(mrow[r], m1);
+        c0[r] = mrow[r] == -INFINITY ? 0.f : exp2f(mrow[r] - mn);
+        c1[r] = m1 == -INFINITY ? 0.f : exp2f(m1 - mn);
+        lrow[r] = lrow[r] * c0[r] + l1 * c1[r];
+        mrow[r] = mn;
+      }
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          o[i][e] = o[i][e] * c0[e >> 1] +
+                    xo[(rb * 16 + g8 + ((e >> 1) << 3)) * XS + i * 8 + 2 * t4 + (e & 1)] * c1[e >> 1];
+    }
   }
   pdl_trigger();
 
@@ -352,7 +405,11 @@ cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
   const int rows_pad = nw * 16;
   a.nwc = nw;
   const int nthr = (2 * nw < 10 ? 2 * nw : (nw > 10 ? nw : 10)) * 32;
-  const void* fn = a.d == 128 ? (const void*)attn_kernel<128> : (const void*)attn_kernel<64>;
+  auto kernel_for = [&](bool kh2) {
+    return a.d == 128 ? (kh2 ? (const void*)attn_kernel<128, 2> : (const void*)attn_kernel<128, 1>)
+                      : (kh2 ? (const void*)attn_kernel<64, 2> : (const void*)attn_kernel<64, 1>);
+  };
+  const void* fn = kernel_for(false);
   // one 64-key tile per split while the longest possible context allows it,
   // so the (latency-bound) pass is as short as the split count permits
   int ns = (a.cap + a.B + kKT - 1) / kKT;
@@ -378,6 +435,14 @@ cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
     ns = kPortable;
     smem = smem_for(ns);
     cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  }
+  // helper warps take the second key half of every tile when a split has
+  // several tiles (one tile: the extra merge costs more than it saves)
+  const int tiles = ((a.cap + a.B + ns - 1) / ns + kKT - 1) / kKT;
+  if (nthr >= 2 * nw * 32 && tiles >= 2) {
+    fn = kernel_for(true);
+    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (ns > kPortable) cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   }
   a.max_splits = ns;
   dim3 grid(ns, a.nkv, a.b);
