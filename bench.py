@@ -172,10 +172,15 @@ def cores() -> int:
         return os.cpu_count() or 1
 
 
+def pick_config(args):
+    """The named workload (--config), else the default Qwen3-4B shape."""
+    return configs.BY_NAME[args.config] if getattr(args, "config", None) else DEFAULT_CFG
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    cfg = DEFAULT_CFG
+    cfg = pick_config(args)
     W = synth.drafter_weights(cfg)
     C = cfg.ctx[0]
     hid = synth.target_hidden(cfg.seed, "ctx0", C, cfg.k * cfg.H)
@@ -216,7 +221,7 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    cfg = DEFAULT_CFG
+    cfg = pick_config(args)
     b = cfg.b
     W = synth.drafter_weights(cfg)
     model = api.DeviceDrafter(cfg, W, dev)
@@ -409,6 +414,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--config", default=None, choices=sorted(configs.BY_NAME),
+                    help="another workload of the parity suite (default: the Qwen3-4B-shaped one)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
