@@ -444,7 +444,6 @@ cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
     cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (ns > kPortable) cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   }
-  a.max_splits = ns;
   dim3 grid(ns, a.nkv, a.b);
   void* args[] = {&a};
   return launch_kc(fn, grid, dim3(nthr), smem, st, pdl, dim3(ns, 1, 1), args);

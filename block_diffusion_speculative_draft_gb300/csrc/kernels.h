@@ -112,7 +112,6 @@ struct AttnArgs {
   const int* len;
   __half* out;  // [M][nq][d]
   int b, B, nq, nkv, d, cap;
-  int max_splits;
   int* status;
   int nwc;  // compute warps (16 query rows each); the rest help with loads and the merge
   // L2 prefetch issued while the kernel would otherwise leave HBM idle:

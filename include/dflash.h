@@ -193,6 +193,9 @@ DFLASH_API int32_t dflash_w8a16_linear(const dflash_w8* w, const uint16_t* x, in
  * last_tok: [b] int32.  draft_out: [b][B-1] int32.
  * hidden_out (nullable): [b][B-1][H] fp32, h before bf16 rounding.
  * logits_out (nullable): [b][B-1][V] fp32.
+ * When both are null the lm-head's input is bf16(x * gamma_final) without
+ * the final RMSNorm's positive per-row factor, which leaves each row's
+ * argmax unchanged (up to bf16 rounding of near ties).
  * The cache is read, never written: the block's own K/V live in the
  * workspace, so rejecting drafts needs no cache rollback. */
 DFLASH_API int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv,
