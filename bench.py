@@ -115,11 +115,13 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def launches_per_step(cfg) -> int:
+def launches_per_step(cfg, folded: bool = False) -> int:
     # draft: embed+norm, per layer qkv/attn/o/gu/down (the RMSNorms between
     # them, and the final one, are applied inside the GEMM epilogues), lm-head
     draft = 5 * cfg.L + 2
     verify = 1
+    if folded:  # commit folded into the draft: its fc GEMM and the length update
+        return draft + verify + 2
     commit = 2 + (cfg.L + 7) // 8  # fc, K/V of up to 8 layers per launch, length update
     return draft + verify + commit
 
@@ -253,6 +255,13 @@ def run_ours(args, rank, world, local_rank):
         api.dflash_verify_accept(logits, draft, n_out, corr, emitted, nxt, vws)
         api.dflash_kv_commit(model, kv, blk, n_out, ws)
 
+    def step_folded():
+        # the same work per step with the commit of the previous verify's
+        # accepted rows folded into this step's draft pass
+        kv.len.copy_(len0)
+        api.dflash_commit_draft_block(model, kv, blk, n_out, t0, draft, ws)
+        api.dflash_verify_accept(logits, draft, n_out, corr, emitted, nxt, vws)
+
     def draft_only():
         api.dflash_draft_block(model, kv, t0, draft, ws)
 
@@ -260,6 +269,7 @@ def run_ours(args, rank, world, local_rank):
     s.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s):
         for _ in range(3):
+            step_folded()
             step()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
@@ -273,6 +283,7 @@ def run_ours(args, rank, world, local_rank):
         return g
 
     g_step = capture(step)
+    g_folded = capture(step_folded)
     g_draft = capture(draft_only)
     g_fused = None
     if cfg.M <= 32:
@@ -318,6 +329,7 @@ def run_ours(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clk:
         total_ms, per_ms = timed(g_step, K, Wm)
     clocks = clk.summary()
+    fold_total, _ = timed(g_folded, K, Wm)
     _, draft_ms = timed(g_draft, K, Wm)
     fused_ms = timed(g_fused, K, Wm)[1] if g_fused is not None else None
     _, ver_ms = timed(g_verify, max(3, K // 5), 2)
@@ -376,6 +388,10 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": cfg.name, "b": b, "B": cfg.B, "ctx": [int(c) for c in ctx], "L": cfg.L,
                    "H": cfg.H, "V": cfg.V, "l2": "inputs larger than L2: weights+lm-head "
                    f"{step_bytes / 1e9:.2f} GB streamed per step", "parallelism": f"replicas x{world}"},
+        "step": "draft + verify-accept + commit of the accepted rows (separate calls)",
+        "step_commit_folded": {"blocks_per_s": whole_job_rate(world, b, K, fold_total),
+                               "ms_per_step": fold_total / K,
+                               "gpu_launches_per_step": launches_per_step(cfg, folded=True)},
         "draft_step_us": {"median": dms * 1e3, "p10": float(np.percentile(draft_ms, 10)) * 1e3,
                           "p90": float(np.percentile(draft_ms, 90)) * 1e3},
         "draft_step_weight_GBps": step_bytes / (dms * 1e-3) / 1e9,

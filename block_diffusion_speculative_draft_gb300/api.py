@@ -28,7 +28,7 @@ EXPORTS = [
     "dflash_w8a16_linear_workspace_size", "dflash_w8a16_linear", "dflash_draft_block", "dflash_draft_block_fused",
     "dflash_lmhead_workspace_size", "dflash_lmhead_argmax", "dflash_verify_workspace_size",
     "dflash_verify_accept", "dflash_verify_accept_noalloc", "dflash_verify_sample_workspace_size",
-    "dflash_verify_accept_sample", "dflash_kv_commit", "dflash_get_status",
+    "dflash_verify_accept_sample", "dflash_kv_commit", "dflash_commit_draft_block", "dflash_get_status",
 ]
 
 
@@ -95,6 +95,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dflash_verify_accept_sample": ([P, P, I32, I32, I32, I64, ctypes.c_float, P, P, P, P, P, P, P, SZ, P],
                                         I32),
         "dflash_kv_commit": ([ctypes.POINTER(Weights), ctypes.POINTER(KV), P, I32, P, P, SZ, P], I32),
+        "dflash_commit_draft_block": ([ctypes.POINTER(Weights), ctypes.POINTER(KV), P, I32, P, P, P, P, P, P, SZ, P],
+                                      I32),
         "dflash_get_status": ([ctypes.POINTER(ctypes.c_int32), I32], I32),
     }
     for name, (args, res) in sig.items():
@@ -264,6 +266,16 @@ def dflash_kv_commit(model: "DeviceDrafter", kv: "KVCache", hid, n, ws, stream=N
     _check("dflash_kv_commit", load_library().dflash_kv_commit(
         ctypes.byref(model.c), ctypes.byref(kv.c), hid.data_ptr(), rps, n.data_ptr(), ws.data_ptr(), ws.numel(),
         _stream(stream)))
+
+
+def dflash_commit_draft_block(model: "DeviceDrafter", kv: "KVCache", hid, n, last_tok, draft_out, ws, hidden=None,
+                              logits=None, stream=None):
+    """dflash_kv_commit(hid, n) and dflash_draft_block(last_tok) in one pass.
+    hid fp16 [b][rows_per_seq][k*H], n int32 [b], last_tok int32 [b]."""
+    rps = hid.shape[1]
+    _check("dflash_commit_draft_block", load_library().dflash_commit_draft_block(
+        ctypes.byref(model.c), ctypes.byref(kv.c), hid.data_ptr(), rps, n.data_ptr(), last_tok.data_ptr(),
+        draft_out.data_ptr(), _ptr(hidden), _ptr(logits), ws.data_ptr(), ws.numel(), _stream(stream)))
 
 
 def dflash_get_status(clear: bool = True) -> int:

@@ -120,7 +120,7 @@ int step_nslots_for(const dflash_config& c, int G) {
 // single zero-fill of the whole buffer initialises them.
 WS carve(const dflash_config& c, int b, int rps, uint8_t* base) {
   WS w;
-  const int M = b * c.B, Mc = b * rps, Mx = M > Mc ? M : Mc;
+  const int M = b * c.B, Mc = b * rps;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     uint8_t* p = base ? base + off : nullptr;
@@ -133,14 +133,14 @@ WS carve(const dflash_config& c, int b, int rps, uint8_t* base) {
   w.skeys = (unsigned long long*)take(step ? 32 * sizeof(unsigned long long) : 0);
   w.sbar = (unsigned*)take(step ? 2 * sizeof(unsigned) : 0);
   w.x = (float*)take((size_t)M * c.H * 4);
-  w.u = (__half*)take((size_t)Mx * c.H * 2);
+  w.u = (__half*)take((size_t)(M + Mc) * c.H * 2);  // block rows, then commit rows
   w.q = (__half*)take((size_t)M * c.nq * c.d * 2);
   w.kb = (__half*)take((size_t)M * c.nkv * c.d * 2);
   w.vb = (__half*)take((size_t)M * c.nkv * c.d * 2);
   w.ao = (__half*)take((size_t)M * c.nq * c.d * 2);
   w.g = (__half*)take((size_t)M * c.F * 2);
   w.h = (__nv_bfloat16*)take((size_t)b * (c.B - 1) * c.H * 2);
-  w.ss = (float*)take((size_t)Mx * (c.H / 128) * 4);
+  w.ss = (float*)take((size_t)(M + Mc) * (c.H / 128) * 4);
   w.spart_bytes = step ? (size_t)step_ntiles_max(c) * step_nslots_for(c, 2 * kNumSMs) * 32 * 128 * sizeof(float) : 0;
   w.spart = (float*)take(w.spart_bytes);
   const size_t na = step ? (size_t)b * c.nkv * kStepMaxSplits * step_rows_pad(c) : 0;
@@ -275,9 +275,14 @@ static int check_kv(const dflash_kv* kv) {
   return DFLASH_OK;
 }
 
+// A draft pass, optionally with a commit folded in (hid non-null): the
+// commit's context rows ride along in each layer's QKV projection, so their
+// K/V reach the cache without a separate launch and the block is drafted
+// against the grown context, exactly as a commit followed by a draft.
 static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, const int32_t* last_tok,
                                 int32_t* draft_out, float* hidden_out, float* logits_out, void* ws, size_t ws_bytes,
-                                void* stream, bool fused) {
+                                void* stream, bool fused, const uint16_t* hid = nullptr, int rps = 0,
+                                const int32_t* ncommit = nullptr) {
   if (int r = check_weights(w)) return r;
   if (int r = check_kv(kv)) return r;
   if (!last_tok || !draft_out) return DFLASH_EINVAL;
@@ -285,9 +290,16 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
   const dflash_config& c = w->cfg;
   const int b = kv->b;
   if ((int64_t)b * c.B > 4096) return DFLASH_EUNSUPPORTED;
-  WS need = carve(c, b, c.B, nullptr);
+  const bool commit = hid != nullptr;
+  if (commit) {
+    if (!ncommit || !aligned16(hid)) return DFLASH_EINVAL;
+    if (rps < 1 || rps > 256 || (int64_t)b * rps > 4096) return DFLASH_EINVAL;
+    if (fused) return DFLASH_EUNSUPPORTED;
+  }
+  const int rps_ws = commit ? rps : c.B;
+  WS need = carve(c, b, rps_ws, nullptr);
   if (!ws || ws_bytes < need.total) return DFLASH_EWORKSPACE;
-  WS s = carve(c, b, c.B, static_cast<uint8_t*>(ws));
+  WS s = carve(c, b, rps_ws, static_cast<uint8_t*>(ws));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int* status = status_ptr();
   if (!status) return DFLASH_ECUDA;
@@ -402,12 +414,25 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
   size_t lm_rows = kLmPrefetchBytes / ((size_t)lm_first * row_bytes);
   if (lm_rows > 128) lm_rows = 128;
   const uint32_t lm_pf_bytes = (uint32_t)(lm_rows * row_bytes);
+  const int Mc = commit ? b * rps : 0;
+  const int nss = c.H / 128;
+  if (commit) {
+    // c = RMSNorm(W8(fc) h; gamma_hid), deferred: u rows [M, M + Mc) = y * gamma_hid
+    W8Args af = base_args(w->fc, Mc, EPI_STORE_F32);
+    af.ldo = c.H;
+    af.xg_out = s.u + (size_t)M * c.H;
+    af.g_next = w->gamma_hid;
+    af.ss_out = s.ss + (size_t)M * nss;
+    af.nss_out = nss;
+    if (w8_gemm(af, reinterpret_cast<const __half*>(hid), st, true) != cudaSuccess) return DFLASH_ECUDA;
+  }
+  // with a commit every activation row of the first QKV is in the deferred form
   e = embed_rmsnorm(reinterpret_cast<const __nv_bfloat16*>(w->embed), last_tok, c.mask_id, c.V, b, c.B, c.H,
-                    w->gamma_in, c.eps, s.x, s.u, st, true, status);
+                    w->gamma_in, c.eps, s.x, s.u, commit ? s.ss : nullptr, st, true, status);
   if (e != cudaSuccess) return DFLASH_ECUDA;
   for (int l = 0; l < c.L; ++l) {
     // [q|k|v] = W8(qkv) u ; per-head QK-RMSNorm + neox RoPE in the epilogue
-    W8Args a = base_args(w->qkv[l], M, EPI_QKV);
+    W8Args a = base_args(w->qkv[l], M + Mc, EPI_QKV);
     fill_inv_freq(a, c.rope_theta, c.d);
     a.out_h = s.q;
     a.kout = s.kb;
@@ -423,9 +448,16 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
     a.rows_per_seq = c.B;
     a.b = b;
     a.cap = kv->cap;
-    if (l > 0) {  // layer 0 reads the embedding, normalised by its own kernel
+    if (l > 0 || commit) {  // else layer 0 reads the embedding, normalised by its own kernel
       a.ss_in = s.ss;
-      a.nss_in = c.H / 128;
+      a.nss_in = nss;
+    }
+    if (commit) {
+      a.mc0 = M;
+      a.c_nacc = ncommit;
+      a.c_rps = rps;
+      a.ck = reinterpret_cast<__half*>(kv->k) + l * layer_kv;
+      a.cv = reinterpret_cast<__half*>(kv->v) + l * layer_kv;
     }
     if ((e = w8_gemm(a, s.u, st, true)) != cudaSuccess) return DFLASH_ECUDA;
     // block attention over [context || block]
@@ -444,6 +476,10 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
     at.d = c.d;
     at.cap = kv->cap;
     at.status = status;
+    if (commit) {
+      at.nacc = ncommit;
+      at.rps = rps;
+    }
     // HBM is nearly idle during attention: pull a prefix of each vocabulary
     // tile that starts an lm-head CTA's stream into L2 (a share per layer),
     // so the lm-head reads that part from L2
@@ -498,6 +534,8 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
     return DFLASH_ECUDA;
   e = lmhead_argmax(s.h, reinterpret_cast<const __nv_bfloat16*>(w->lm_head), b * (c.B - 1), c.V, c.H, draft_out,
                     nullptr, logits_out, s.lm, st, true, status);
+  if (e != cudaSuccess) return DFLASH_ECUDA;
+  if (commit) e = commit_len_update(kv->len, ncommit, b, rps, kv->cap, st, true, status);
   return map_err(e);
 }
 
@@ -510,6 +548,14 @@ int32_t dflash_draft_block_fused(const dflash_weights* w, const dflash_kv* kv, c
                                  int32_t* draft_out, float* hidden_out, float* logits_out, void* ws, size_t ws_bytes,
                                  void* stream) {
   return draft_block_impl(w, kv, last_tok, draft_out, hidden_out, logits_out, ws, ws_bytes, stream, true);
+}
+
+int32_t dflash_commit_draft_block(const dflash_weights* w, const dflash_kv* kv, const uint16_t* hid,
+                                  int32_t rows_per_seq, const int32_t* n, const int32_t* last_tok, int32_t* draft_out,
+                                  float* hidden_out, float* logits_out, void* ws, size_t ws_bytes, void* stream) {
+  if (!hid) return DFLASH_EINVAL;
+  return draft_block_impl(w, kv, last_tok, draft_out, hidden_out, logits_out, ws, ws_bytes, stream, false, hid,
+                          rows_per_seq, n);
 }
 
 int32_t dflash_lmhead_workspace_size(int64_t M, size_t* bytes) {

@@ -62,22 +62,28 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
   // The context K/V and its length are inputs of the whole draft pass (no
   // kernel of the pass writes them), so the first tile's context keys are
   // fetched before waiting for the kernel that produces q and the block K/V.
+  // (a commit folded into this pass appends rows [Lold, L), written by this
+  // layer's QKV kernel: those are read only after the wait)
   int L = a.len[j];
   if (L < 0) L = 0;
   if (L > a.cap) L = a.cap;
+  const int Lold = L;
+  if (a.nacc) L += commit_count(a.len[j], a.nacc[j], a.rps, a.cap);
   const int total = L + a.B;
   int k0, k1;
   split_range(total, sp, ns, k0, k1);
 
-  // part 0: context keys t < L only; 1: block keys and the zero fill; 2: all
+  // part 0: context keys t < Lold only; 1: the rest (appended context rows,
+  // block keys, zero fill); 2: all
   auto load_kv = [&](int buf, int t0, int part) {
     for (int c = threadIdx.x; c < kKT * (D / 8); c += blockDim.x) {
       int r = c / (D / 8), ch = c % (D / 8);
       int t = t0 + r;
       bool ok = t < k1;
       const bool ctx = ok && t < L;
-      if (part == 0 && !ctx) continue;
-      if (part == 1 && ctx) continue;
+      const bool old_ctx = ok && t < Lold;
+      if (part == 0 && !old_ctx) continue;
+      if (part == 1 && old_ctx) continue;
       const __half* ks = a.kc;
       const __half* vs = a.vc;
       if (ok) {

@@ -181,6 +181,8 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
     const int m = z * G::MCH + tok;
     const int p = pos[tok];
     if (m >= a.M || p < 0) continue;
+    const bool crow = a.epi == EPI_QKV && a.c_nacc && m >= a.mc0;  // folded commit row
+    if (crow && kind == 0) continue;                              // its q is not needed
     const int seq = m / a.rows_per_seq;
     float v[4];
 #pragma unroll
@@ -215,7 +217,7 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
         rope_rot(v[2], v[3], p, a.inv_hi[lane], a.inv_lo[lane]);
       }
     }
-    if (a.epi == EPI_QKV) {
+    if (a.epi == EPI_QKV && !crow) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         int row = prow0 + lane + 32 * i;
@@ -224,15 +226,18 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
         else if (kind == 1) kout[(size_t)m * kd + (row - qd)] = hv;
         else vout[(size_t)m * kd + (row - qd - kd)] = hv;
       }
-    } else {  // EPI_KVCOMMIT: cache [b][nkv][cap][d]
+    } else {  // a committed context row: cache [b][nkv][cap][d]
+      const int cseq = crow ? (m - a.mc0) / a.c_rps : seq;
+      __half* ck = crow ? a.ck : kout;
+      __half* cv = crow ? a.cv : vout;
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         int row = prow0 + lane + 32 * i - qd;  // within k|v rows
         int isv = row >= kd;
         int rr = isv ? row - kd : row;
         int h = rr / a.d, e = rr - h * a.d;
-        size_t off = (((size_t)seq * a.nkv + h) * a.cap + p) * a.d + e;
-        (isv ? vout : kout)[off] = __float2half_rn(v[i]);
+        size_t off = (((size_t)cseq * a.nkv + h) * a.cap + p) * a.d + e;
+        (isv ? cv : ck)[off] = __float2half_rn(v[i]);
       }
     }
   }
@@ -362,15 +367,20 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
       const int t = threadIdx.x, m = z * G::MCH + t;
       int p = -1;
       if (m < a.M) {
-        const int seq = m / a.rows_per_seq, slot = m - seq * a.rows_per_seq;
-        int L0 = a.len[seq];
         if (a.epi == EPI_KVCOMMIT) {
-          const int nn = a.nacc[seq];
-          const int cnt = min(nn + 1, a.rows_per_seq);
-          const bool ok = nn >= -1 && nn <= a.rows_per_seq && L0 >= 0 && L0 + max(cnt, 0) <= a.cap;
-          p = (ok && slot < cnt) ? L0 + slot : -1;
-        } else {
-          p = (L0 < 0 ? 0 : L0) + slot;
+          const int seq = m / a.rows_per_seq, slot = m - seq * a.rows_per_seq;
+          const int L0 = a.len[seq];
+          p = slot < commit_count(L0, a.nacc[seq], a.rows_per_seq, a.cap) ? L0 + slot : -1;
+        } else if (a.c_nacc && m >= a.mc0) {  // a context row of the folded commit
+          const int mc = m - a.mc0, seq = mc / a.c_rps, slot = mc - seq * a.c_rps;
+          const int L0 = a.len[seq];
+          p = slot < commit_count(L0, a.c_nacc[seq], a.c_rps, a.cap) ? L0 + slot : -1;
+        } else {  // a block row: after the context (grown by the folded commit)
+          const int seq = m / a.rows_per_seq, slot = m - seq * a.rows_per_seq;
+          const int L0 = a.len[seq];
+          int base = L0 < 0 ? 0 : L0;
+          if (a.c_nacc) base += commit_count(L0, a.c_nacc[seq], a.c_rps, a.cap);
+          p = base + slot;
         }
       }
       s_pos[t] = p;

@@ -137,7 +137,7 @@ __device__ __forceinline__ void store_f16_row(__half* ur, int H, const float4 (&
 __global__ void __launch_bounds__(kNormThreads) embed_rmsnorm_kernel(const __nv_bfloat16* E, const int* last_tok,
                                                                     int mask_id, int V, int B, int H,
                                                                     const float* gamma, float eps, float* x,
-                                                                    __half* u, int* status) {
+                                                                    __half* u, float* ss_out, int* status) {
   __shared__ float sh[32];
   pdl_wait();
   const int m = blockIdx.x;
@@ -160,7 +160,23 @@ __global__ void __launch_bounds__(kNormThreads) embed_rmsnorm_kernel(const __nv_
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < kNormVec; ++i) ss += v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
-  float inv = rsqrtf(block_sum(ss, sh) / H + eps);
+  float inv = 1.f;
+  if (ss_out) {
+    // deferred RMSNorm: per-128-column sums of squares; for a given i one
+    // warp holds one column tile (n4 is a multiple of 32)
+#pragma unroll
+    for (int i = 0; i < kNormVec; ++i) {
+      const int c0 = (threadIdx.x & ~31) + i * kNormThreads;
+      if (c0 < n4) {
+        float q = v[i].x * v[i].x + v[i].y * v[i].y + v[i].z * v[i].z + v[i].w * v[i].w;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) q += __shfl_xor_sync(0xffffffffu, q, o);
+        if ((threadIdx.x & 31) == 0) ss_out[(size_t)m * (H >> 7) + (c0 >> 5)] = q;
+      }
+    }
+  } else {
+    inv = rsqrtf(block_sum(ss, sh) / H + eps);
+  }
   pdl_trigger();
   float4* xr = reinterpret_cast<float4*>(x + (size_t)m * H);
 #pragma unroll
@@ -337,9 +353,9 @@ int verify_parts(int b, int R, int64_t V) {
 }  // namespace
 
 cudaError_t embed_rmsnorm(const __nv_bfloat16* E, const int* last_tok, int mask_id, int V, int b, int B, int H,
-                          const float* gamma, float eps, float* x, __half* u, cudaStream_t st, bool pdl,
-                          int* status) {
-  void* args[] = {&E, &last_tok, &mask_id, &V, &B, &H, &gamma, &eps, &x, &u, &status};
+                          const float* gamma, float eps, float* x, __half* u, float* ss_out, cudaStream_t st,
+                          bool pdl, int* status) {
+  void* args[] = {&E, &last_tok, &mask_id, &V, &B, &H, &gamma, &eps, &x, &u, &ss_out, &status};
   return launch_k((const void*)embed_rmsnorm_kernel, dim3(b * B), dim3(kNormThreads), 0, st, pdl, args);
 }
 

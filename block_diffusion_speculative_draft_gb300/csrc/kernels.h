@@ -62,6 +62,15 @@ struct W8Args {
   // the argmax over each row's logits does not see.
   __nv_bfloat16* hb_out;
   int hb_rps;
+  // A commit folded into the draft's QKV projection (EPI_QKV only; c_nacc
+  // null: none): rows m >= mc0 are target-context rows, c_rps per sequence,
+  // whose K/V go into this layer's cache ck / cv at len + slot for the
+  // committed slots; the block's rows sit after the new length.
+  int mc0;
+  const int* c_nacc;
+  int c_rps;
+  __half* ck;
+  __half* cv;
   // Several layers' projections in one launch (the K/V rows of every
   // layer's qkv for a commit): tile columns [i ntl, (i + 1) ntl) of the grid
   // belong to layer i < nl and use lq/ls/lk/lv/lgk[i] in place of
@@ -114,6 +123,10 @@ struct AttnArgs {
   int b, B, nq, nkv, d, cap;
   int* status;
   int nwc;  // compute warps (16 query rows each); the rest help with loads and the merge
+  // a commit folded into this pass (null: none): the context grows by
+  // commit_count(len, nacc, rps, cap) rows, written by this layer's QKV kernel
+  const int* nacc;
+  int rps;
   // L2 prefetch issued while the kernel would otherwise leave HBM idle:
   // pieces [pf_i0, pf_i1) of base + i * pf_stride, pf_bytes each (or none)
   const uint8_t* pf_base;
@@ -124,9 +137,20 @@ struct AttnArgs {
 cudaError_t attention(const AttnArgs& a, cudaStream_t st, bool pdl);
 
 // --- small kernels (k_small.cu) ---
+// ss_out null: u = RMSNorm(x; gamma).  Else the deferred form: u = x * gamma
+// and ss_out[m][H/128] = sums of squares per 128-column tile.
 cudaError_t embed_rmsnorm(const __nv_bfloat16* E, const int* last_tok, int mask_id, int V, int b, int B, int H,
-                          const float* gamma, float eps, float* x, __half* u, cudaStream_t st, bool pdl,
-                          int* status);
+                          const float* gamma, float eps, float* x, __half* u, float* ss_out, cudaStream_t st,
+                          bool pdl, int* status);
+
+// Rows of a sequence a commit appends: min(n + 1, rps), or 0 when n is out
+// of [-1, rps], the length is negative or the rows would pass cap (the
+// length-update kernel flags those cases).
+__device__ __forceinline__ int commit_count(int len, int n, int rps, int cap) {
+  int c = n + 1 < rps ? n + 1 : rps;
+  if (c < 0) c = 0;
+  return (n >= -1 && n <= rps && len >= 0 && len + c <= cap) ? c : 0;
+}
 cudaError_t final_norm(const float* x, int b, int B, int H, const float* gamma, float eps, __nv_bfloat16* h,
                        float* hidden_out, cudaStream_t st, bool pdl);
 cudaError_t commit_len_update(int* len, const int* nacc, int b, int rows_per_seq, int cap, cudaStream_t st,

@@ -311,6 +311,21 @@ DFLASH_API int32_t dflash_verify_accept_sample(const float* logits, const int32_
                                                int32_t* next_tok_out, void* ws,
                                                size_t ws_bytes, void* stream);
 
+/* Commit and draft in one pass: the same results as dflash_kv_commit(w, kv,
+ * hid, rows_per_seq, n, ...) followed by dflash_draft_block(w, kv, last_tok,
+ * ...) on the same stream (up to fp32 summation order).  The committed rows'
+ * K/V projections ride along in each layer's QKV GEMM of the draft, so the
+ * K/V weights are read once and the separate K/V launch disappears; the
+ * block is drafted against the grown context and len[] is advanced at the
+ * end.  Arguments and errors are the union of the two calls'; ws is sized by
+ * dflash_workspace_size(cfg, b, rows_per_seq).  Multi-kernel path only. */
+DFLASH_API int32_t dflash_commit_draft_block(const dflash_weights* w, const dflash_kv* kv,
+                                             const uint16_t* hid, int32_t rows_per_seq,
+                                             const int32_t* n, const int32_t* last_tok,
+                                             int32_t* draft_out, float* hidden_out,
+                                             float* logits_out, void* ws, size_t ws_bytes,
+                                             void* stream);
+
 /* Draft-KV commit with rollback of the rejected suffix (mlx-dspark v0.0.3,
  * "Notes": KV rollback; dflash-mlx "What It Does": conditioning on target
  * hidden states).  hid: [b][rows_per_seq][k*H] fp16 target hidden rows of the
