@@ -604,7 +604,9 @@ static int max_active_clusters(const void* fn, size_t smem, int s) {
 
 cudaError_t w8_gemm(const W8Args& a0, const __half* x, cudaStream_t st, bool pdl) {
   W8Args a = a0;
-  const int mt = pick_mt(a.M);
+  // a QKV with a folded commit runs block rows and context rows as separate
+  // 16-row chunks (they share the weight tiles through L2)
+  const int mt = a.c_nacc ? 2 : pick_mt(a.M);
   const int mch = mt * 8;
   const int chunks = (a.M + mch - 1) / mch;
   const int ntiles = a.nrows / kTile * (a.nl > 0 ? a.nl : 1);
