@@ -95,6 +95,14 @@ def test_tiny_commit_and_draft(fused):
     _check_draft(cfg, W, model, kv, ws, hids, ctx, fused=fused)
 
 
+def test_tiny_long_context_multi_tile_splits():
+    # a 1000-row context gives attention splits of several 64-key tiles, the
+    # path where helper warps compute the second key half of every tile
+    cfg = TINY.with_ctx((1000,))
+    W, model, ctx, kv, ws, hids = _setup(cfg, 64)
+    _check_draft(cfg, W, model, kv, ws, hids, ctx)
+
+
 def test_tiny_prefill_chunk_sizes_agree():
     # the same context committed 5 rows or 64 rows at a time gives one cache
     cfg = TINY.with_ctx((37,))
