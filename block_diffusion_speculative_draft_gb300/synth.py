@@ -62,6 +62,24 @@ def w8_grid(seed: int, name: str, N: int, K: int) -> Tuple[np.ndarray, np.ndarra
     return q, s
 
 
+def w4_grid(seed: int, name: str, N: int, K: int) -> Tuple[np.ndarray, np.ndarray]:
+    """int4 grid q[N][K] in [-7, 7] (absmax 7 in every 128-column group) and
+    fp16 scales s[N][K / 128]; magnitudes comparable to w8_grid's."""
+    rng = rng_for(seed, "w4", name)
+    G = K // 128
+    q = rng.integers(-7, 8, size=(N, K), dtype=np.int8)
+    col = rng.integers(0, 128, size=(N, G)) + 128 * np.arange(G)[None, :]
+    sign = np.where(rng.integers(0, 2, size=(N, G)) == 1, 7, -7).astype(np.int8)
+    q[np.arange(N)[:, None], col] = sign
+    s = rng.lognormal(mean=-3.1, sigma=0.3, size=(N, G)).astype(np.float16)
+    return q, s
+
+
+def w4_float(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """The synthetic float weight on each group's int4 grid, as fp32."""
+    return q.astype(np.float32) * np.repeat(s.astype(np.float32), 128, axis=1)
+
+
 def w8_float(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     """The synthetic float weight on each row's int8 grid, as fp32."""
     return q.astype(np.float32) * s.astype(np.float32)[:, None]
@@ -151,8 +169,9 @@ def verify_logits(seed: int, name: str, draft: np.ndarray, R: int, V: int,
     return lg
 
 
-def drafter_weights(cfg, with_float: bool = False) -> Dict[str, object]:
-    """All drafter tensors for a workload (host numpy arrays).
+def drafter_weights(cfg, with_float: bool = False, bits: int = 8) -> Dict[str, object]:
+    """All drafter tensors for a workload (host numpy arrays); bits = 4 draws
+    the projections on int4 grids with per-128-column group scales.
 
     W8 matrices are stored as (q, s) in their logical row order:
       qkv  [(nq + 2 nkv) d][H]  rows: q heads, then k heads, then v heads
@@ -163,12 +182,13 @@ def drafter_weights(cfg, with_float: bool = False) -> Dict[str, object]:
     """
     sd, L, H, d, F = cfg.seed, cfg.L, cfg.H, cfg.d, cfg.F
     W: Dict[str, object] = {}
-    W["fc"] = w8_grid(sd, "fc", H, cfg.k * H)
+    grid = w4_grid if bits == 4 else w8_grid
+    W["fc"] = grid(sd, "fc", H, cfg.k * H)
     for l in range(L):
-        W[f"qkv{l}"] = w8_grid(sd, f"qkv{l}", cfg.nqkv, H)
-        W[f"o{l}"] = w8_grid(sd, f"o{l}", H, cfg.nq * d)
-        W[f"gu{l}"] = w8_grid(sd, f"gu{l}", 2 * F, H)
-        W[f"down{l}"] = w8_grid(sd, f"down{l}", H, F)
+        W[f"qkv{l}"] = grid(sd, f"qkv{l}", cfg.nqkv, H)
+        W[f"o{l}"] = grid(sd, f"o{l}", H, cfg.nq * d)
+        W[f"gu{l}"] = grid(sd, f"gu{l}", 2 * F, H)
+        W[f"down{l}"] = grid(sd, f"down{l}", H, F)
     W["gamma_hid"] = gamma(sd, "hid", (H,))
     W["gamma_in"] = gamma(sd, "in", (L, H))
     W["gamma_post"] = gamma(sd, "post", (L, H))

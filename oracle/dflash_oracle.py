@@ -73,6 +73,41 @@ def pack_w8a16(w: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
     return q, s
 
 
+GROUP4 = 128  # columns per int4 scale group
+
+
+def dequant_w4(q: np.ndarray, s: np.ndarray) -> np.ndarray:
+    """w[n][k] = q[n][k] * s[n][k / 128]: int4 values (in [-7, 7]) with one
+    fp16 scale per output row and 128-column group.  A 4-bit drafter is the
+    pages' default (mlx-dspark v0.0.3 release notes, "Notes": drafter
+    quantisation does not affect acceptance, 4-bit stays the default); the
+    symmetric format and the group size are this build's reading.  Pinned:
+    exact (q * s fits in fp32)."""
+    sg = np.repeat(np.asarray(s, dtype=np.float16).astype(F64), GROUP4, axis=1)
+    return q.astype(F64) * sg
+
+
+def pack_w4a16(w: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """Symmetric int4 quantisation of w[N][K] (fp32), K a multiple of 128.
+
+    s[n][g] = fp16(absmax over row n, columns [128 g, 128 g + 128) / 7), the
+    division in fp32 rounded to nearest even; q = clamp(rint(w / s), -7, 7)
+    with the division in fp32 using the rounded s; groups whose s is 0 get
+    q = 0.  Pinned: round trip on the int4 grid is exact; |w - q s| <= s/2;
+    max|q| = 7 in every group."""
+    w32 = np.asarray(w, dtype=np.float32)
+    N, K = w32.shape
+    g = w32.reshape(N, K // GROUP4, GROUP4)
+    amax = np.abs(g).max(axis=2)
+    s = (amax / np.float32(7.0)).astype(np.float32).astype(np.float16)
+    s32 = s.astype(np.float32)[:, :, None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.rint(g / s32)
+    r = np.where(s32 == 0, np.float32(0), r)
+    q = np.clip(r, -7, 7).astype(np.int8).reshape(N, K)
+    return q, s
+
+
 # ----------------------------------------------------------------------------
 # norms and rotary embedding
 # ----------------------------------------------------------------------------
@@ -145,7 +180,8 @@ def attention_gqa(q: np.ndarray, k: np.ndarray, v: np.ndarray) -> np.ndarray:
 class Drafter:
     """Dequantised float64 view of a drafter's tensors (lazy per matrix).
 
-    W maps names to (q, s) pairs for W8 matrices in logical row order
+    W maps names to (q, s) pairs for W8 matrices (s per row) or W4
+    matrices (s per row and 128-column group) in logical row order
     (qkv rows: q heads | k heads | v heads; gu rows: gate F | up F) and to
     arrays for gammas and the bf16 embedding / lm-head bit patterns."""
 
@@ -157,7 +193,7 @@ class Drafter:
         if name in self._cache:
             return self._cache[name]
         q, s = self.W[name]
-        w = dequant_w8(q, s)
+        w = dequant_w4(q, s) if np.ndim(s) == 2 else dequant_w8(q, s)
         if self.cache:
             self._cache[name] = w
         return w

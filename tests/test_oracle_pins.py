@@ -69,6 +69,60 @@ def test_pack_negative_control(monkeypatch):
     assert np.any(err > s.astype(np.float64)[:, None] * 0.5 * (1 + 1e-6))
 
 
+# ---------------------------------------------------------------- W4A16 -----
+def test_dequant_w4_is_exact_and_grouped():
+    # int4 x fp16 is exact in fp32; the scale of column k is group k // 128
+    q, s = synth.w4_grid(13, "pin4", 16, 512)
+    w64 = O.dequant_w4(q, s)
+    w32 = q.astype(np.float32) * np.repeat(s.astype(np.float32), 128, axis=1)
+    assert np.array_equal(w64, w32.astype(np.float64))
+    q1 = np.zeros((2, 256), np.int8)
+    q1[1, 127] = 3
+    q1[1, 128] = 5
+    s1 = np.array([[1.0, 1.0], [0.5, 2.0]], np.float16)
+    w = O.dequant_w4(q1, s1)
+    assert w[1, 127] == 1.5 and w[1, 128] == 10.0 and np.count_nonzero(w) == 2
+
+
+def test_pack_w4_round_trip_on_int4_grid():
+    # every synthetic group has absmax exactly 7 * s, so packing is lossless
+    q, s = synth.w4_grid(14, "pin4", 48, 384)
+    assert np.abs(q).max() == 7
+    q2, s2 = O.pack_w4a16(synth.w4_float(q, s))
+    assert np.array_equal(q2, q)
+    assert np.array_equal(s2.view(np.uint16), s.view(np.uint16))
+
+
+def test_pack_w4_error_bound_and_range():
+    rng = np.random.default_rng(5)
+    w = (rng.standard_normal((64, 384)) * rng.lognormal(-2, 1, (64, 1))).astype(np.float32)
+    w[3, 128:256] = 0.0  # an all-zero group
+    q, s = O.pack_w4a16(w)
+    assert s.shape == (64, 3)
+    assert np.all(np.abs(q.astype(np.int32)) <= 7)
+    assert s[3, 1] == 0 and not q[3, 128:256].any()
+    sg = np.repeat(s.astype(np.float32), 128, axis=1)
+    nz = sg > 0
+    err = np.abs(w.astype(np.float64) - O.dequant_w4(q, s))
+    assert np.all(err[nz] <= sg[nz] * (0.5 + 1e-6) + 1e-30)
+    # each group's maximum maps to +-7 (or +-6 after fp16 rounding of s up)
+    g = np.abs(q.reshape(64, 3, 128)).max(axis=2)
+    assert np.all(g[s > 0] >= 6)
+
+
+def test_pack_w4_negative_control(monkeypatch):
+    # one scale per row instead of per group loses the small groups' precision
+    rng = np.random.default_rng(6)
+    w = rng.standard_normal((8, 256)).astype(np.float32)
+    w[:, 128:] *= 1e-3
+    q, s = O.pack_w4a16(w)
+    ok = np.abs(w.astype(np.float64) - O.dequant_w4(q, s))
+    s_row = np.repeat(s.max(axis=1, keepdims=True), 2, axis=1)
+    bad = np.abs(w.astype(np.float64) - O.dequant_w4(np.clip(np.rint(
+        w / np.repeat(s_row.astype(np.float32), 128, axis=1)), -7, 7).astype(np.int8), s_row))
+    assert np.max(bad[:, 128:]) > 5 * np.max(ok[:, 128:])
+
+
 def test_linear_orientation():
     # a single nonzero weight q[n0][k0] routes input channel k0 to output n0
     x = np.arange(1, 13, dtype=np.float64).reshape(2, 6)
