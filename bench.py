@@ -371,6 +371,19 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
 
+    # the same draft step with int4 projections (W4A16, group scales in the
+    # packed tiles); the cache and inputs are the ones above
+    W4 = synth.drafter_weights(cfg, bits=4)
+    m4 = api.DeviceDrafter(cfg, W4, dev, bits=4)
+    del W4
+    draft4 = torch.empty_like(draft)
+    api.dflash_draft_block(m4, kv, t0, draft4, ws)
+    torch.cuda.synchronize()
+    g_draft4 = capture(lambda: api.dflash_draft_block(m4, kv, t0, draft4, ws))
+    _, draft4_ms = timed(g_draft4, K, Wm)
+    assert api.dflash_get_status() == 0, "device status flagged during the int4 draft timing"
+    del g_draft4, m4
+
     hbm, peak_kind = peaks()
     ms_step = total_ms / K
     value = whole_job_rate(world, b, K, total_ms)
@@ -395,6 +408,10 @@ def run_ours(args, rank, world, local_rank):
         "draft_step_us": {"median": dms * 1e3, "p10": float(np.percentile(draft_ms, 10)) * 1e3,
                           "p90": float(np.percentile(draft_ms, 90)) * 1e3},
         "draft_step_weight_GBps": step_bytes / (dms * 1e-3) / 1e9,
+        "draft_step_w4a16": {"median_us": statistics.median(draft4_ms) * 1e3,
+                             "bytes": cfg.step_bytes_w4(list(ctx)),
+                             "frac_of_measured": cfg.step_bytes_w4(list(ctx))
+                             / (statistics.median(draft4_ms) * 1e-3) / 1e9 / hbm},
         "draft_step_fused_kernel_us": None if fused_ms is None else statistics.median(fused_ms) * 1e3,
         "step_roofline": {"bytes": step_bytes, "frac_of_measured": step_bytes / (dms * 1e-3) / 1e9 / hbm,
                           "frac_of_8TBps": step_bytes / (dms * 1e-3) / 1e9 / 8000.0},

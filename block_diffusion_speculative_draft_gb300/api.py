@@ -25,6 +25,7 @@ DEV_KV_CAPACITY, DEV_BAD_TOKEN, DEV_BAD_LENGTH, DEV_WAIT_TIMEOUT = 0x1, 0x2, 0x4
 
 EXPORTS = [
     "dflash_version", "dflash_status_string", "dflash_workspace_size", "dflash_pack_w8a16",
+    "dflash_w4a16_packed_bytes", "dflash_pack_w4a16",
     "dflash_w8a16_linear_workspace_size", "dflash_w8a16_linear", "dflash_draft_block", "dflash_draft_block_fused",
     "dflash_lmhead_workspace_size", "dflash_lmhead_argmax", "dflash_verify_workspace_size",
     "dflash_verify_accept", "dflash_verify_accept_noalloc", "dflash_verify_sample_workspace_size",
@@ -48,7 +49,7 @@ class Config(ctypes.Structure):
 
 class W8(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("s", ctypes.c_void_p), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
-                ("layout", ctypes.c_int32)]
+                ("layout", ctypes.c_int32), ("bits", ctypes.c_int32)]
 
 
 class Weights(ctypes.Structure):
@@ -82,6 +83,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dflash_status_string": ([I32], ctypes.c_char_p),
         "dflash_workspace_size": ([ctypes.POINTER(Config), I32, I32, PSZ], I32),
         "dflash_pack_w8a16": ([P, I32, I64, I64, I32, P, P, P], I32),
+        "dflash_w4a16_packed_bytes": ([I64, I64, PSZ], I32),
+        "dflash_pack_w4a16": ([P, I32, I64, I64, I32, P, P, P], I32),
         "dflash_w8a16_linear_workspace_size": ([I64, I64, I64, PSZ], I32),
         "dflash_w8a16_linear": ([ctypes.POINTER(W8), P, I64, P, P, SZ, P], I32),
         "dflash_draft_block": ([ctypes.POINTER(Weights), ctypes.POINTER(KV), P, P, P, P, P, SZ, P], I32),
@@ -99,6 +102,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
                                       I32),
         "dflash_get_status": ([ctypes.POINTER(ctypes.c_int32), I32], I32),
     }
+    if set(sig) != set(EXPORTS):  # every export is called with declared argument types
+        raise RuntimeError(f"binding signatures out of step with exports: {set(sig) ^ set(EXPORTS)}")
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
         fn.argtypes = args
@@ -155,8 +160,25 @@ def dflash_pack_w8a16(w, layout: int = LAYOUT_PLAIN, stream=None):
     return q, s
 
 
-def w8_desc(q, s, N: int, K: int, layout: int = LAYOUT_PLAIN) -> W8:
-    return W8(q.data_ptr(), s.data_ptr(), N, K, layout)
+def dflash_pack_w4a16(w, layout: int = LAYOUT_PLAIN, stream=None):
+    """Pack a device weight w[N][K] to int4 with per-128-column group scales;
+    returns (q, s): q uint8 tiles (scales included), s fp16 [N][K/128]."""
+    torch = _torch()
+    lib = load_library()
+    dt = {torch.float32: DTYPE_F32, torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16}[w.dtype]
+    N, K = w.shape
+    w = w.contiguous()
+    n = ctypes.c_size_t(0)
+    _check("dflash_w4a16_packed_bytes", lib.dflash_w4a16_packed_bytes(N, K, ctypes.byref(n)))
+    q = torch.empty(n.value, dtype=torch.uint8, device=w.device)
+    s = torch.empty((N, K // 128), dtype=torch.float16, device=w.device)
+    _check("dflash_pack_w4a16", lib.dflash_pack_w4a16(
+        w.data_ptr(), dt, N, K, layout, q.data_ptr(), s.data_ptr(), _stream(stream)))
+    return q, s
+
+
+def w8_desc(q, s, N: int, K: int, layout: int = LAYOUT_PLAIN, bits: int = 8) -> W8:
+    return W8(q.data_ptr(), s.data_ptr() if s is not None else None, N, K, layout, bits)
 
 
 def dflash_w8a16_linear(desc: W8, x, ws=None, stream=None):
@@ -291,26 +313,33 @@ def to_c_config(cfg) -> Config:
 
 
 class DeviceDrafter:
-    """A drafter's tensors resident on the GPU, packed by dflash_pack_w8a16.
+    """A drafter's tensors resident on the GPU, packed by dflash_pack_w8a16
+    (bits 8) or dflash_pack_w4a16 (bits 4).
 
-    `W` is the host dict from synth.drafter_weights (int8 grids + fp16 scales,
-    fp32 gammas, bf16 tables).  Each W8 matrix is uploaded as its fp32 float
-    weight and packed on the device, one matrix at a time."""
+    `W` is the host dict from synth.drafter_weights (int8 or int4 grids +
+    fp16 scales, fp32 gammas, bf16 tables).  Each matrix is uploaded as its
+    fp32 float weight and packed on the device, one matrix at a time."""
 
-    def __init__(self, cfg, W: Dict[str, object], device="cuda"):
+    def __init__(self, cfg, W: Dict[str, object], device="cuda", bits: int = 8):
         torch = _torch()
         self.cfg = cfg
         self.keep: List[object] = []
         dev = torch.device(device)
         from . import synth
 
+        self.bits = bits
+
         def pack(name, layout=LAYOUT_PLAIN):
             q, s = W[name]
-            w = torch.from_numpy(synth.w8_float(q, s)).to(dev)
-            qd, sd = dflash_pack_w8a16(w, layout)
+            if bits == 4:
+                w = torch.from_numpy(synth.w4_float(q, s)).to(dev)
+                qd, sd = dflash_pack_w4a16(w, layout)
+            else:
+                w = torch.from_numpy(synth.w8_float(q, s)).to(dev)
+                qd, sd = dflash_pack_w8a16(w, layout)
             del w
             self.keep += [qd, sd]
-            return W8(qd.data_ptr(), sd.data_ptr(), q.shape[0], q.shape[1], layout)
+            return W8(qd.data_ptr(), sd.data_ptr(), q.shape[0], q.shape[1], layout, bits)
 
         def up(a, dtype=None):
             t = torch.from_numpy(np.ascontiguousarray(a)).to(dev)

@@ -80,6 +80,11 @@ class DrafterConfig:
         return (self.layer_weight_bytes() + self.scale_bytes()
                 + self.lmhead_bytes() + self.kv_read_bytes(ctx))
 
+    def step_bytes_w4(self, ctx: List[int]) -> int:
+        # int4 codes (half a byte per weight) + one fp16 scale per 128 weights
+        lw = self.layer_weight_bytes()
+        return lw // 2 + lw // 64 + self.lmhead_bytes() + self.kv_read_bytes(ctx)
+
     def commit_weight_bytes(self) -> int:
         fc = self.H * self.k * self.H + 2 * self.H
         kv = self.L * (2 * self.nkv * self.d * self.H + 2 * 2 * self.nkv * self.d)

@@ -61,7 +61,8 @@ int check_cfg(const dflash_config* c) {
 }
 
 int check_w8(const dflash_w8& w, int64_t N, int64_t K, int layout) {
-  if (!w.q || !w.s) return DFLASH_EINVAL;
+  if (w.bits != 0 && w.bits != 8 && w.bits != 4) return DFLASH_EINVAL;
+  if (!w.q || (w.bits != 4 && !w.s)) return DFLASH_EINVAL;
   if (w.N != N || w.K != K || w.layout != layout) return DFLASH_EINVAL;
   if (!aligned16(w.q)) return DFLASH_EINVAL;
   return DFLASH_OK;
@@ -165,6 +166,7 @@ W8Args base_args(const dflash_w8& w, int M, int epi) {
   a.N = (int)w.N;
   a.K = (int)w.K;
   a.layout = w.layout;
+  a.bits = w.bits == 4 ? 4 : 8;
   a.row0 = 0;
   a.nrows = (int)w.N;
   a.M = M;
@@ -224,6 +226,25 @@ int32_t dflash_pack_w8a16(const void* w, int32_t w_dtype, int64_t N, int64_t K, 
                          static_cast<cudaStream_t>(stream)));
 }
 
+int32_t dflash_w4a16_packed_bytes(int64_t N, int64_t K, size_t* bytes) {
+  if (!bytes || N < 1 || K < 1) return DFLASH_EINVAL;
+  if (N % 128 || K % 128) return DFLASH_EUNSUPPORTED;
+  *bytes = (size_t)(N / 128) * (size_t)(K / 128) * (size_t)kW4TileBytes;
+  return DFLASH_OK;
+}
+
+int32_t dflash_pack_w4a16(const void* w, int32_t w_dtype, int64_t N, int64_t K, int32_t layout, void* q_out,
+                          uint16_t* s_out, void* stream) {
+  if (!w || !q_out || !s_out) return DFLASH_EINVAL;
+  if (w_dtype < 0 || w_dtype > 2 || N < 1 || K < 1) return DFLASH_EINVAL;
+  if (layout != DFLASH_LAYOUT_PLAIN && layout != DFLASH_LAYOUT_GATEUP) return DFLASH_EINVAL;
+  if (N % 128 || K % 128) return DFLASH_EUNSUPPORTED;
+  if (layout == DFLASH_LAYOUT_GATEUP && (N / 2) % 64) return DFLASH_EUNSUPPORTED;
+  if (!aligned16(q_out)) return DFLASH_EINVAL;
+  return map_err(w4_pack(w, w_dtype, N, K, layout, static_cast<uint8_t*>(q_out), reinterpret_cast<__half*>(s_out),
+                         static_cast<cudaStream_t>(stream)));
+}
+
 int32_t dflash_w8a16_linear(const dflash_w8* w, const uint16_t* x, int64_t M, float* y, void* ws, size_t ws_bytes,
                             void* stream) {
   (void)ws;
@@ -264,6 +285,12 @@ static int check_weights(const dflash_weights* w) {
     if (int r = check_w8(w->gu[l], 2 * (int64_t)c.F, c.H, DFLASH_LAYOUT_GATEUP)) return r;
     if (int r = check_w8(w->down[l], c.H, c.F, DFLASH_LAYOUT_PLAIN)) return r;
   }
+  // one weight format per drafter (batched launches span several layers)
+  const int bits = w->fc.bits == 4 ? 4 : 8;
+  for (int l = 0; l < c.L; ++l) {
+    for (const dflash_w8* m : {&w->qkv[l], &w->o[l], &w->gu[l], &w->down[l]})
+      if ((m->bits == 4 ? 4 : 8) != bits) return DFLASH_EINVAL;
+  }
   return DFLASH_OK;
 }
 
@@ -290,6 +317,7 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
   const dflash_config& c = w->cfg;
   const int b = kv->b;
   if ((int64_t)b * c.B > 4096) return DFLASH_EUNSUPPORTED;
+  if (fused && w->fc.bits == 4) return DFLASH_EUNSUPPORTED;  // the single-kernel step is int8 only
   const bool commit = hid != nullptr;
   if (commit) {
     if (!ncommit || !aligned16(hid)) return DFLASH_EINVAL;

@@ -40,12 +40,22 @@ namespace {
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
-template <int MT>
+// packed int4 tile: 8 KB of fragment-ordered nibbles, then the 128 rows'
+// fp16 scales of the tile's 128-column group
+constexpr int kTile4Bytes = (int)kW4TileBytes;
+
+template <int MT, int BITS = 8>
 struct Geo {
   static constexpr int MCH = MT * 8;          // activation rows per chunk
-  static constexpr int NST = MT >= 8 ? 3 : 4;  // ring stages (3 keeps two 64-row CTAs per SM)
+  // ring stages: int8 3 / 4 (3 keeps two 64-row CTAs per SM); int4 tiles are
+  // half the bytes, so a deeper ring keeps as many weight bytes in flight
+  // (every variant stays under 110 KB: two CTAs per SM)
+  static constexpr int NST = BITS == 8 ? (MT >= 8 ? 3 : 4) : (MT >= 8 ? 4 : (MT >= 4 ? 6 : 8));
   static constexpr int ABYTES = 2 * MCH * 128;  // two [MCH][64] fp16 halves
-  static constexpr int STAGE = kTileBytes + ABYTES;
+  static constexpr int WBYTES = BITS == 8 ? kTileBytes : kTile4Bytes;  // weight bytes per stage
+  static constexpr int WSLOT = (WBYTES + 1023) / 1024 * 1024;          // activations 1 KB aligned
+  static constexpr int STAGE = WSLOT + ABYTES;
+  static constexpr int TX = WBYTES + ABYTES;  // bytes a stage's copies deliver
   static constexpr int TSTRIDE = 132;  // epilogue tile row stride (floats)
   static constexpr int TBYTES = (MCH * TSTRIDE * 4 + 1023) / 1024 * 1024;
   static_assert(2 * TBYTES <= NST * STAGE, "epilogue tiles must fit in the ring");
@@ -53,6 +63,7 @@ struct Geo {
   // positions, per-row norm factors
   static constexpr int SIDE = 128 * 4 + 128 * 4 + 128 * 4 + MCH * 4 + MCH * 4;
   static constexpr size_t SMEM = 1024 + NST * (size_t)STAGE + 2 * NST * 8 + 64 + SIDE;
+  static_assert(SMEM <= 112 * 1024, "two CTAs per SM");
 };
 
 // packed row -> logical row
@@ -243,10 +254,34 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
   }
 }
 
-template <int MT>
+// int4 nibbles (biased by 8) of one 32-bit word to the four half2 registers
+// of an m16k16 A fragment: nibble k sits at bits 4k; nibbles (0, 4), (1, 5),
+// (2, 6), (3, 7) form registers 0..3.  The magic-number conversion puts a
+// nibble into an fp16 mantissa under exponent 2^10 (1024 + n, or 1024 + 16 n
+// for the high nibble of a byte, scaled back by 1/16) and removes the bias by
+// one subtraction; every step is exact.
+__device__ __forceinline__ void biased_u4x8_to_half2x4(uint32_t w, uint32_t (&r)[4]) {
+  const uint32_t lo0 = (w & 0x000F000Fu) | 0x64006400u;
+  const uint32_t hi0 = (w & 0x00F000F0u) | 0x64006400u;
+  const uint32_t lo1 = ((w >> 8) & 0x000F000Fu) | 0x64006400u;
+  const uint32_t hi1 = ((w >> 8) & 0x00F000F0u) | 0x64006400u;
+  const __half2 sub = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));  // 1032
+  const __half2 sixteenth = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));  // 1/16
+  const __half2 sub16 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));  // -72
+  __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&lo0), sub);
+  __half2 b = __hfma2(*reinterpret_cast<const __half2*>(&hi0), sixteenth, sub16);
+  __half2 c = __hsub2(*reinterpret_cast<const __half2*>(&lo1), sub);
+  __half2 d = __hfma2(*reinterpret_cast<const __half2*>(&hi1), sixteenth, sub16);
+  r[0] = *reinterpret_cast<uint32_t*>(&a);
+  r[1] = *reinterpret_cast<uint32_t*>(&b);
+  r[2] = *reinterpret_cast<uint32_t*>(&c);
+  r[3] = *reinterpret_cast<uint32_t*>(&d);
+}
+
+template <int MT, int BITS>
 __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                const W8Args a) {
-  using G = Geo<MT>;
+  using G = Geo<MT, BITS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::NST * G::STAGE);
@@ -301,27 +336,27 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
     // ---------------- producer ----------------
     if (lane == 0) {
       prefetch_tmap(&xmap);
-      const uint8_t* wsrc = wq + ((size_t)((a.row0 >> 7) + nt) * KT + kt0) * kTileBytes;
+      const uint8_t* wsrc = wq + ((size_t)((a.row0 >> 7) + nt) * KT + kt0) * G::WBYTES;
       const uint64_t pol = policy_evict_first();
       const int pre = nk < G::NST ? nk : G::NST;
       for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(&full[i], G::STAGE);
-        bulk_g2s_hint(smem + i * G::STAGE, wsrc + (size_t)i * kTileBytes, kTileBytes, &full[i], pol);
+        mbar_arrive_expect_tx(&full[i], G::TX);
+        bulk_g2s_hint(smem + i * G::STAGE, wsrc + (size_t)i * G::WBYTES, G::WBYTES, &full[i], pol);
       }
       pdl_wait();
       for (int i = 0; i < pre; ++i) {
-        uint8_t* sa = smem + i * G::STAGE + kTileBytes;
+        uint8_t* sa = smem + i * G::STAGE + G::WSLOT;
         tma_load_2d(sa, &xmap, (kt0 + i) * kTile, z * G::MCH, &full[i]);
         tma_load_2d(sa + G::MCH * 128, &xmap, (kt0 + i) * kTile + 64, z * G::MCH, &full[i]);
       }
       for (int i = pre; i < nk; ++i) {
         const int slot = i % G::NST;
         if (!mbar_wait(&empty[slot], ((i / G::NST) - 1) & 1, a.status)) break;
-        mbar_arrive_expect_tx(&full[slot], G::STAGE);
+        mbar_arrive_expect_tx(&full[slot], G::TX);
         uint8_t* st = smem + slot * G::STAGE;
-        bulk_g2s_hint(st, wsrc + (size_t)i * kTileBytes, kTileBytes, &full[slot], pol);
-        tma_load_2d(st + kTileBytes, &xmap, (kt0 + i) * kTile, z * G::MCH, &full[slot]);
-        tma_load_2d(st + kTileBytes + G::MCH * 128, &xmap, (kt0 + i) * kTile + 64, z * G::MCH, &full[slot]);
+        bulk_g2s_hint(st, wsrc + (size_t)i * G::WBYTES, G::WBYTES, &full[slot], pol);
+        tma_load_2d(st + G::WSLOT, &xmap, (kt0 + i) * kTile, z * G::MCH, &full[slot]);
+        tma_load_2d(st + G::WSLOT + G::MCH * 128, &xmap, (kt0 + i) * kTile + 64, z * G::MCH, &full[slot]);
       }
     }
     pdl_trigger();
@@ -330,7 +365,8 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
     {  // weights-side data first (independent of the preceding kernel)
       const int r = threadIdx.x;  // 0..127
       const int prow = a.row0 + nt * kTile + r;
-      s_sc[r] = __half2float(wsc[logical_row(prow, a.layout, a.N)]);
+      // int4 weights carry their group scales in the tile (applied per stage)
+      s_sc[r] = BITS == 8 ? __half2float(wsc[logical_row(prow, a.layout, a.N)]) : 1.f;
       if (a.epi == EPI_QKV || a.epi == EPI_KVCOMMIT) {
         const int qd = a.nq * a.d;
         const float* gsrc = (a.row0 + nt * kTile) < qd ? a.gq : gk;
@@ -390,27 +426,70 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
     for (int i = 0; i < nk; ++i) {
       const int slot = i % G::NST;
       if (!mbar_wait(&full[slot], (i / G::NST) & 1, a.status)) break;
-      const uint8_t* wl = smem + slot * G::STAGE + (warp * 8 * 32 + lane) * 16;
-      const uint32_t abase = smem_u32(smem + slot * G::STAGE + kTileBytes);
+      const uint32_t abase = smem_u32(smem + slot * G::STAGE + G::WSLOT);
+      if constexpr (BITS == 8) {
+        const uint8_t* wl = smem + slot * G::STAGE + (warp * 8 * 32 + lane) * 16;
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        uint4 wq = *reinterpret_cast<const uint4*>(wl + ks * 32 * 16);
-        uint32_t af[2][4];
-        biased_u8x4_to_half2x2(wq.x, af[0][0], af[0][1]);
-        biased_u8x4_to_half2x2(wq.y, af[0][2], af[0][3]);
-        biased_u8x4_to_half2x2(wq.z, af[1][0], af[1][1]);
-        biased_u8x4_to_half2x2(wq.w, af[1][2], af[1][3]);
-        const uint32_t hbase = abase + (ks >> 2) * (G::MCH * 128);
-        const int ch = ((ks & 3) << 1) + ch_hi;
+        for (int ks = 0; ks < 8; ++ks) {
+          uint4 wq = *reinterpret_cast<const uint4*>(wl + ks * 32 * 16);
+          uint32_t af[2][4];
+          biased_u8x4_to_half2x2(wq.x, af[0][0], af[0][1]);
+          biased_u8x4_to_half2x2(wq.y, af[0][2], af[0][3]);
+          biased_u8x4_to_half2x2(wq.z, af[1][0], af[1][1]);
+          biased_u8x4_to_half2x2(wq.w, af[1][2], af[1][3]);
+          const uint32_t hbase = abase + (ks >> 2) * (G::MCH * 128);
+          const int ch = ((ks & 3) << 1) + ch_hi;
 #pragma unroll
-        for (int p = 0; p < MT / 2; ++p) {
-          const int tok = p * 16 + g_tok_lo;
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(hbase + tok * 128 + ((ch ^ (tok & 7)) << 4), b0, b1, b2, b3);
-          mma_f16(acc[0][2 * p], af[0], b0, b1);
-          mma_f16(acc[1][2 * p], af[1], b0, b1);
-          mma_f16(acc[0][2 * p + 1], af[0], b2, b3);
-          mma_f16(acc[1][2 * p + 1], af[1], b2, b3);
+          for (int p = 0; p < MT / 2; ++p) {
+            const int tok = p * 16 + g_tok_lo;
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(hbase + tok * 128 + ((ch ^ (tok & 7)) << 4), b0, b1, b2, b3);
+            mma_f16(acc[0][2 * p], af[0], b0, b1);
+            mma_f16(acc[1][2 * p], af[1], b0, b1);
+            mma_f16(acc[0][2 * p + 1], af[0], b2, b3);
+            mma_f16(acc[1][2 * p + 1], af[1], b2, b3);
+          }
+        }
+      } else {
+        // int4: this k-tile is one scale group, so its partial sums are
+        // scaled per row before joining the accumulators
+        const uint8_t* wl = smem + slot * G::STAGE + (warp * 8 * 32 + lane) * 8;
+        float tacc[2][MT][4];
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+#pragma unroll
+          for (int jj = 0; jj < MT; ++jj)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) tacc[x][jj][e] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint2 wq = *reinterpret_cast<const uint2*>(wl + ks * 32 * 8);
+          uint32_t af[2][4];
+          biased_u4x8_to_half2x4(wq.x, af[0]);
+          biased_u4x8_to_half2x4(wq.y, af[1]);
+          const uint32_t hbase = abase + (ks >> 2) * (G::MCH * 128);
+          const int ch = ((ks & 3) << 1) + ch_hi;
+#pragma unroll
+          for (int p = 0; p < MT / 2; ++p) {
+            const int tok = p * 16 + g_tok_lo;
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(hbase + tok * 128 + ((ch ^ (tok & 7)) << 4), b0, b1, b2, b3);
+            mma_f16(tacc[0][2 * p], af[0], b0, b1);
+            mma_f16(tacc[1][2 * p], af[1], b0, b1);
+            mma_f16(tacc[0][2 * p + 1], af[0], b2, b3);
+            mma_f16(tacc[1][2 * p + 1], af[1], b2, b3);
+          }
+        }
+        const __half* gsc = reinterpret_cast<const __half*>(smem + slot * G::STAGE + 8192);
+        const int g = lane >> 2;
+#pragma unroll
+        for (int mg = 0; mg < 2; ++mg) {
+          const float s_lo = __half2float(gsc[warp * 32 + mg * 16 + g]);
+          const float s_hi = __half2float(gsc[warp * 32 + mg * 16 + g + 8]);
+#pragma unroll
+          for (int jj = 0; jj < MT; ++jj)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[mg][jj][e] += tacc[mg][jj][e] * (e < 2 ? s_lo : s_hi);
         }
       }
       __syncwarp();
@@ -550,6 +629,69 @@ __global__ void pack_q_kernel(const void* w, int64_t N, int64_t K, int layout, c
   reinterpret_cast<uint4*>(q)[chunk] = make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+// int4 group scales: s[n][g] = fp16(absmax of row n over columns
+// [128 g, 128 g + 128) / 7), one warp per (row, group)
+template <typename T>
+__global__ void pack4_scale_kernel(const void* w, int64_t N, int64_t K, __half* s) {
+  const int64_t G = K / kTile;
+  const int64_t item = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (item >= N * G) return;
+  const int64_t row = item / G, grp = item - row * G;
+  const int lane = threadIdx.x & 31;
+  float m = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(ld_w<T>(w, row * K + grp * kTile + lane + 32 * e)));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) s[item] = __float2half_rn(m / 7.0f);
+}
+
+// one thread per 8-byte lane chunk of a packed int4 tile:
+// tile (nt, kt) -> [warp 4][kstep 8][lane 32][frag(2w) word | frag(2w+1) word],
+// then 128 fp16 scales (group kt of the tile's packed rows).  In a fragment
+// word nibble k holds element (row g + 8 (k & 1), column 2t + (k >> 2) +
+// 8 ((k >> 1) & 1)) as q + 8, so nibbles (k, k + 4) are register k's halves.
+template <typename T>
+__global__ void pack4_q_kernel(const void* w, int64_t N, int64_t K, int layout, const __half* s, uint8_t* q) {
+  const int64_t chunk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (chunk >= N * K / 16) return;
+  const int64_t KT = K / kTile;
+  const int64_t tile = chunk >> 10;
+  const int within = (int)(chunk & 1023);
+  const int wq = within >> 8, ks = (within >> 5) & 7, ln = within & 31;
+  const int64_t nt = tile / KT, kt = tile - nt * KT;
+  const int g = ln >> 2, t = ln & 3;
+  auto lrow_of = [&](int64_t prow) {
+    if (layout != 1) return prow;
+    const int64_t tl = prow >> 7, rr = prow & 127;
+    return rr < 64 ? tl * 64 + rr : (N >> 1) + tl * 64 + (rr - 64);
+  };
+  uint32_t word[2];
+#pragma unroll
+  for (int f = 0; f < 2; ++f) {
+    const int mg = 2 * wq + f;
+    uint32_t wd = 0u;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int r = g + (k & 1) * 8;
+      const int c = 2 * t + (k >> 2) + ((k >> 1) & 1) * 8;
+      const int64_t lrow = lrow_of(nt * kTile + mg * 16 + r);
+      const float sc = __half2float(s[lrow * KT + kt]);
+      int qv = 0;
+      if (sc != 0.f) {
+        float r_ = rintf(ld_w<T>(w, lrow * K + kt * kTile + ks * 16 + c) / sc);
+        qv = (int)fminf(fmaxf(r_, -7.f), 7.f);
+      }
+      wd |= (uint32_t)(qv + 8) << (4 * k);
+    }
+    word[f] = wd;
+  }
+  uint8_t* tb = q + tile * kTile4Bytes;
+  reinterpret_cast<uint2*>(tb)[within] = make_uint2(word[0], word[1]);
+  if (within < kTile)
+    reinterpret_cast<__half*>(tb + 8192)[within] = s[lrow_of(nt * kTile + within) * KT + kt];
+}
+
 }  // namespace
 
 int w8_pick_splits(int units, int KT) {
@@ -610,9 +752,13 @@ cudaError_t w8_gemm(const W8Args& a0, const __half* x, cudaStream_t st, bool pdl
   const int mch = mt * 8;
   const int chunks = (a.M + mch - 1) / mch;
   const int ntiles = a.nrows / kTile * (a.nl > 0 ? a.nl : 1);
-  const void* fn = mt == 2 ? (const void*)w8_gemm_kernel<2>
-                  : mt == 4 ? (const void*)w8_gemm_kernel<4> : (const void*)w8_gemm_kernel<8>;
-  const size_t smem = mt == 2 ? Geo<2>::SMEM : mt == 4 ? Geo<4>::SMEM : Geo<8>::SMEM;
+  const bool w4 = a.bits == 4;
+  const void* fn = w4 ? (mt == 2 ? (const void*)w8_gemm_kernel<2, 4>
+                         : mt == 4 ? (const void*)w8_gemm_kernel<4, 4> : (const void*)w8_gemm_kernel<8, 4>)
+                      : (mt == 2 ? (const void*)w8_gemm_kernel<2, 8>
+                         : mt == 4 ? (const void*)w8_gemm_kernel<4, 8> : (const void*)w8_gemm_kernel<8, 8>);
+  const size_t smem = w4 ? (mt == 2 ? Geo<2, 4>::SMEM : mt == 4 ? Geo<4, 4>::SMEM : Geo<8, 4>::SMEM)
+                         : (mt == 2 ? Geo<2>::SMEM : mt == 4 ? Geo<4>::SMEM : Geo<8>::SMEM);
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const int units = chunks * ntiles;
   a.splits = w8_pick_splits(units, a.K / kTile);
@@ -642,6 +788,25 @@ cudaError_t w8_pack(const void* w, int w_dtype, int64_t N, int64_t K, int layout
   } else {
     pack_scale_kernel<__nv_bfloat16><<<g1, b1, 0, st>>>(w, N, K, s_out);
     pack_q_kernel<__nv_bfloat16><<<g2, 256, 0, st>>>(w, N, K, layout, s_out, q_out);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t w4_pack(const void* w, int w_dtype, int64_t N, int64_t K, int layout, uint8_t* q_out, __half* s_out,
+                    cudaStream_t st) {
+  const int64_t items = N * (K / kTile);
+  dim3 g1((unsigned)((items + 7) / 8));
+  const int64_t nchunks = N * K / 16;
+  dim3 g2((unsigned)((nchunks + 255) / 256));
+  if (w_dtype == 0) {
+    pack4_scale_kernel<float><<<g1, 256, 0, st>>>(w, N, K, s_out);
+    pack4_q_kernel<float><<<g2, 256, 0, st>>>(w, N, K, layout, s_out, q_out);
+  } else if (w_dtype == 1) {
+    pack4_scale_kernel<__half><<<g1, 256, 0, st>>>(w, N, K, s_out);
+    pack4_q_kernel<__half><<<g2, 256, 0, st>>>(w, N, K, layout, s_out, q_out);
+  } else {
+    pack4_scale_kernel<__nv_bfloat16><<<g1, 256, 0, st>>>(w, N, K, s_out);
+    pack4_q_kernel<__nv_bfloat16><<<g2, 256, 0, st>>>(w, N, K, layout, s_out, q_out);
   }
   return cudaGetLastError();
 }

@@ -24,8 +24,9 @@ enum Epi : int {
 
 struct W8Args {
   const uint8_t* q;  // packed tiles
-  const __half* s;   // logical-order scales
+  const __half* s;   // logical-order scales (int8 weights only)
   int N, K, layout;
+  int bits;  // 8: int8 tiles + per-row scales; 4: int4 tiles carrying their group scales
   int row0;   // first packed row used (multiple of 128)
   int nrows;  // packed rows used (multiple of 128)
   int M;      // activation rows
@@ -102,6 +103,11 @@ int w8_pick_splits(int units, int KT);
 cudaError_t w8_gemm(const W8Args& a, const __half* x, cudaStream_t st, bool pdl);
 cudaError_t w8_pack(const void* w, int w_dtype, int64_t N, int64_t K, int layout, uint8_t* q_out, __half* s_out,
                     cudaStream_t st);
+// int4 packing: s_out [N][K/128] group scales in logical order, q_out the
+// packed tiles of kW4TileBytes each (nibbles + the tile's rows' scales)
+cudaError_t w4_pack(const void* w, int w_dtype, int64_t N, int64_t K, int layout, uint8_t* q_out, __half* s_out,
+                    cudaStream_t st);
+constexpr int64_t kW4TileBytes = 8192 + 256;
 
 // --- lm-head GEMM + argmax (k_lmhead.cu) ---
 size_t lmhead_ws_bytes(int64_t M);

@@ -95,14 +95,21 @@ typedef struct dflash_config {
   float eps;        /* RMSNorm epsilon                                    */
 } dflash_config;
 
-/* A packed W8A16 matrix (output of dflash_pack_w8a16): logical weight
- * W[N][K] = q[N][K] * s[N].  `q` is N*K bytes in the library's tiled layout,
- * `s` is N fp16 scales in logical row order.  Borrowed device pointers. */
+/* A packed weight matrix, int8 or int4 codes with fp16 scales.
+ *  bits 8 (or 0), output of dflash_pack_w8a16: W[N][K] = q[N][K] * s[N];
+ *    `q` is N*K bytes in the library's tiled layout, `s` is N fp16 scales in
+ *    logical row order.
+ *  bits 4, output of dflash_pack_w4a16: W[N][K] = q[N][K] * s[N][K/128]
+ *    with q in [-7, 7]; `q` is dflash_w4a16_packed_bytes(N, K) bytes of
+ *    tiles that carry their own scales, so `s` is not read and may be NULL.
+ * Borrowed device pointers.  All matrices of one dflash_weights use the same
+ * `bits`. */
 typedef struct dflash_w8 {
   const void* q;
   const uint16_t* s;
   int64_t N, K;
   int32_t layout; /* DFLASH_LAYOUT_* */
+  int32_t bits;   /* 8 (or 0) or 4 */
 } dflash_w8;
 
 /* Drafter weights.  qkv/o/gu/down point to HOST arrays of L descriptors
@@ -168,12 +175,34 @@ DFLASH_API int32_t dflash_pack_w8a16(const void* w, int32_t w_dtype, int64_t N, 
                           int32_t layout, void* q_out, uint16_t* s_out,
                           void* stream);
 
+/* Bytes of the packed tiles of an int4 matrix: (N/128)(K/128) tiles of
+ * 8448 bytes (8192 of codes, then the tile's 128 rows' fp16 scales).
+ * N, K multiples of 128 (else DFLASH_EUNSUPPORTED). */
+DFLASH_API int32_t dflash_w4a16_packed_bytes(int64_t N, int64_t K, size_t* bytes);
+
+/* Symmetric int4 quantisation with one scale per row and 128-column group
+ * (W4A16; a 4-bit drafter is the default of mlx-dspark v0.0.3, release
+ * notes "Notes"; the symmetric [-7, 7] format and the group size of 128 are
+ * this library's choice) of w[N][K] (device, w_dtype DFLASH_DTYPE_*):
+ *   s[n][g] = fp16_rn(max_{k in group g} |w[n][k]| / 7)  (fp32 division)
+ *   q[n][k] = clamp(rint(w[n][k] / s[n][k/128]), -7, 7)  (fp32 division;
+ *             0 where the scale is 0)
+ * q_out (16-byte aligned, dflash_w4a16_packed_bytes(N, K) bytes) receives
+ * the tiles, s_out (device, N*K/128 fp16) the scales in logical order; both
+ * caller-owned.  s_out is only a by-product once packing has finished (the
+ * tiles hold a copy).  Layouts, shape limits and errors as dflash_pack_w8a16.
+ * Asynchronous on `stream`. */
+DFLASH_API int32_t dflash_pack_w4a16(const void* w, int32_t w_dtype, int64_t N, int64_t K,
+                          int32_t layout, void* q_out, uint16_t* s_out,
+                          void* stream);
+
 /* Workspace bytes for dflash_w8a16_linear. */
 DFLASH_API int32_t dflash_w8a16_linear_workspace_size(int64_t M, int64_t N, int64_t K,
                                            size_t* bytes);
 
 /* The W8A16 projection alone (the kernel every drafter matmul runs on):
- * y[m][n] = s[n] * sum_k x[m][k] q[n][k] with fp16 activations x [M][K]
+ * y[m][n] = s[n] * sum_k x[m][k] q[n][k] (int4: sum over groups g of
+ * s[n][g] * sum_{k in g} x[m][k] q[n][k]) with fp16 activations x [M][K]
  * (16-byte aligned), fp32 accumulation, fp32 output y [M][N] in logical row
  * order (mirror-sd README, "The Story", Phase 3).  M in [1, 4096]. */
 DFLASH_API int32_t dflash_w8a16_linear(const dflash_w8* w, const uint16_t* x, int64_t M,
