@@ -26,6 +26,12 @@
 //    epilogue for that slice; no partial ever touches global memory;
 //  * programmatic dependent launch: the weight copies of the first stages are
 //    issued before griddepcontrol.wait, overlapping the previous kernel's tail.
+// The same kernel runs int4 weights (W4A16; a 4-bit drafter is the default of
+// mlx-dspark v0.0.3, release notes "Notes"): symmetric codes in [-7, 7] with
+// one fp16 scale per row and 128-column group, packed as 8448-byte tiles
+// (fragment-ordered nibbles + the tile's group scales).  A k-tile is one
+// group, so each stage's partial sums are scaled per row as they join the
+// accumulators, and the ring is deeper to keep as many bytes in flight.
 #include <map>
 #include <mutex>
 #include <tuple>
