@@ -160,18 +160,29 @@ def dflash_pack_w8a16(w, layout: int = LAYOUT_PLAIN, stream=None):
     return q, s
 
 
-def dflash_pack_w4a16(w, layout: int = LAYOUT_PLAIN, stream=None):
+def dflash_w4a16_packed_bytes(N: int, K: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("dflash_w4a16_packed_bytes", load_library().dflash_w4a16_packed_bytes(N, K, ctypes.byref(n)))
+    return n.value
+
+
+def dflash_pack_w4a16(w, layout: int = LAYOUT_PLAIN, stream=None, q=None, s=None):
     """Pack a device weight w[N][K] to int4 with per-128-column group scales;
-    returns (q, s): q uint8 tiles (scales included), s fp16 [N][K/128]."""
+    returns (q, s): q uint8 tiles (scales included), s fp16 [N][K/128].  `q`
+    and `s` may be given (contiguous device buffers of those sizes), e.g. a
+    128-row-aligned slice of a larger matrix's tiles."""
     torch = _torch()
     lib = load_library()
     dt = {torch.float32: DTYPE_F32, torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16}[w.dtype]
     N, K = w.shape
     w = w.contiguous()
-    n = ctypes.c_size_t(0)
-    _check("dflash_w4a16_packed_bytes", lib.dflash_w4a16_packed_bytes(N, K, ctypes.byref(n)))
-    q = torch.empty(n.value, dtype=torch.uint8, device=w.device)
-    s = torch.empty((N, K // 128), dtype=torch.float16, device=w.device)
+    nbytes = dflash_w4a16_packed_bytes(N, K)
+    if q is None:
+        q = torch.empty(nbytes, dtype=torch.uint8, device=w.device)
+    if s is None:
+        s = torch.empty((N, K // 128), dtype=torch.float16, device=w.device)
+    if q.numel() < nbytes or s.numel() < N * (K // 128) or not (q.is_contiguous() and s.is_contiguous()):
+        raise ValueError("dflash_pack_w4a16: output buffers too small or not contiguous")
     _check("dflash_pack_w4a16", lib.dflash_pack_w4a16(
         w.data_ptr(), dt, N, K, layout, q.data_ptr(), s.data_ptr(), _stream(stream)))
     return q, s
@@ -181,8 +192,8 @@ def w8_desc(q, s, N: int, K: int, layout: int = LAYOUT_PLAIN, bits: int = 8) -> 
     return W8(q.data_ptr(), s.data_ptr() if s is not None else None, N, K, layout, bits)
 
 
-def dflash_w8a16_linear(desc: W8, x, ws=None, stream=None):
-    """y[M][N] fp32 = W8(desc) applied to fp16 x[M][K]."""
+def dflash_w8a16_linear(desc: W8, x, ws=None, stream=None, y=None):
+    """y[M][N] fp32 = W8(desc) applied to fp16 x[M][K] (y may be given)."""
     torch = _torch()
     lib = load_library()
     M = x.shape[0]
@@ -191,7 +202,10 @@ def dflash_w8a16_linear(desc: W8, x, ws=None, stream=None):
            lib.dflash_w8a16_linear_workspace_size(M, desc.N, desc.K, ctypes.byref(n)))
     if ws is None or ws.numel() < n.value:
         ws = torch.zeros(max(n.value, 256), dtype=torch.uint8, device=x.device)
-    y = torch.empty((M, desc.N), dtype=torch.float32, device=x.device)
+    if y is None:
+        y = torch.empty((M, desc.N), dtype=torch.float32, device=x.device)
+    elif y.numel() < M * desc.N or not y.is_contiguous() or y.dtype != torch.float32:
+        raise ValueError("dflash_w8a16_linear: y must be contiguous fp32 with M*N elements")
     _check("dflash_w8a16_linear", lib.dflash_w8a16_linear(
         ctypes.byref(desc), x.data_ptr(), M, y.data_ptr(), ws.data_ptr(), ws.numel(), _stream(stream)))
     return y

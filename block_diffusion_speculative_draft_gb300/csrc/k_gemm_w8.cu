@@ -350,6 +350,9 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
         bulk_g2s_hint(smem + i * G::STAGE, wsrc + (size_t)i * G::WBYTES, G::WBYTES, &full[i], pol);
       }
       pdl_wait();
+      // the activations were written by the previous kernel with generic
+      // stores; order this thread's tensor (async-proxy) reads after them
+      fence_proxy_async_global();
       for (int i = 0; i < pre; ++i) {
         uint8_t* sa = smem + i * G::STAGE + G::WSLOT;
         tma_load_2d(sa, &xmap, (kt0 + i) * kTile, z * G::MCH, &full[i]);

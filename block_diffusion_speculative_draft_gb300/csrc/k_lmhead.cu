@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_kernel(const __grid_consta
         tma_load_2d_hint(smem + i * G::STAGE, &wmap, ks * 64, tile * 128, &full[i], pol);
       }
       pdl_wait();
+      fence_proxy_async_global();  // h was written with generic stores: order the tensor reads after them
       for (int i = 0; i < pre; ++i) {
         int ks = i % KS;
         tma_load_2d(smem + i * G::STAGE + kWBox, &hmap, ks * 64, z * G::MCH, &full[i]);
