@@ -100,3 +100,61 @@ def test_weights_struct_checked_before_launch(lib):
     kv = api.KV(256, 256, 256, 1, 64)
     assert lib.dflash_draft_block(ctypes.byref(W), ctypes.byref(kv), fake, fake, None, None, fake, 1 << 30,
                                   None) == -1
+
+
+def test_int4_entry_points_checked_on_host(lib):
+    from block_diffusion_speculative_draft_gb300 import api
+    n = ctypes.c_size_t(0)
+    assert lib.dflash_w4a16_packed_bytes(128, 256, ctypes.byref(n)) == 0 and n.value == 2 * 8448
+    assert api.dflash_w4a16_packed_bytes(256, 384) == 2 * 3 * 8448
+    assert lib.dflash_w4a16_packed_bytes(100, 128, ctypes.byref(n)) == -2
+    assert lib.dflash_w4a16_packed_bytes(128, 128, None) == -1
+    P, x = None, ctypes.c_void_p(256)
+    assert lib.dflash_pack_w4a16(P, 0, 128, 128, 0, x, x, P) == -1
+    assert lib.dflash_pack_w4a16(x, 0, 128, 128, 0, x, P, P) == -1
+    assert lib.dflash_pack_w4a16(x, 3, 128, 128, 0, x, x, P) == -1          # unknown dtype
+    assert lib.dflash_pack_w4a16(x, 0, 128, 100, 0, x, x, P) == -2          # K not a multiple of 128
+    assert lib.dflash_pack_w4a16(x, 0, 128, 128, 0, ctypes.c_void_p(264), x, P) == -1  # q_out misaligned
+
+
+def _tiny_weights(api, c, bits=8, fc_bits=None, s_ptr=256):
+    def d(N, K, layout=0, b=bits):
+        return api.W8(256, s_ptr, N, K, layout, b)
+    L = c.L
+    arr = lambda N, K, layout=0: (api.W8 * L)(*[d(N, K, layout) for _ in range(L)])
+    qkv, o = arr(c.nqkv, c.H), arr(c.H, c.nq * c.d)
+    gu, down = arr(2 * c.F, c.H, 1), arr(c.H, c.F)
+    P = lambda a: ctypes.cast(a, ctypes.POINTER(api.W8))
+    W = api.Weights(api.to_c_config(c), d(c.H, c.k * c.H, 0, bits if fc_bits is None else fc_bits),
+                    P(qkv), P(o), P(gu), P(down), 256, 256, 256, 256, 256, 256, 256, 256)
+    return W, (qkv, o, gu, down)
+
+
+def test_weight_bits_checked_before_launch(lib):
+    """bits must be 0, 8 or 4 and the same for every matrix; int4 matrices
+    need no scale pointer; the single-kernel step refuses int4.  Every case
+    returns on the host (a workspace that is too small is the last check
+    before any launch)."""
+    from block_diffusion_speculative_draft_gb300 import api
+    from block_diffusion_speculative_draft_gb300.configs import TINY as c
+    fake = ctypes.c_void_p(256)
+    kv = api.KV(256, 256, 256, 1, 64)
+
+    def draft(W, fn=lib.dflash_draft_block):
+        return fn(ctypes.byref(W), ctypes.byref(kv), fake, fake, None, None, None, 0, None)
+
+    for bits in (0, 8, 4):
+        W, keep = _tiny_weights(api, c, bits)
+        assert draft(W) == -5, bits                      # valid: only the workspace is missing
+    W, keep = _tiny_weights(api, c, 4, s_ptr=None)
+    assert draft(W) == -5                                # int4 needs no scale array
+    W, keep = _tiny_weights(api, c, 8, s_ptr=None)
+    assert draft(W) == -1                                # int8 does
+    W, keep = _tiny_weights(api, c, 5)
+    assert draft(W) == -1
+    W, keep = _tiny_weights(api, c, 4, fc_bits=8)
+    assert draft(W) == -1                                # mixed widths
+    W, keep = _tiny_weights(api, c, 4)
+    assert draft(W, lib.dflash_draft_block_fused) == -2  # single-kernel step is int8 only
+    W, keep = _tiny_weights(api, c, 8)
+    assert draft(W, lib.dflash_draft_block_fused) == -5

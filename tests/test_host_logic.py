@@ -1,0 +1,81 @@
+"""Host-side logic that the GPU runs depend on, checked on the CPU: the
+algorithmic byte counts the roofline divides by, the stand-in target's row
+chunks, and the test helper that decodes packed int4 tiles (so that the GPU
+packer's bit-exact test compares against a correct reading of the layout)."""
+import numpy as np
+
+from oracle import dflash_oracle as O
+from block_diffusion_speculative_draft_gb300.configs import QWEN3_4B, TINY, ALL
+from block_diffusion_speculative_draft_gb300 import workload as WL
+from tests.gpu_util import unpack_tiled_q4
+
+
+def test_step_bytes_by_hand():
+    c = QWEN3_4B
+    # per layer: q|k|v (32 + 2 * 8 heads of 128) x 2560, o 2560 x 4096,
+    # gate|up 2 * 9728 x 2560, down 2560 x 9728, one byte per int8 weight
+    per_layer = 2560 * 6144 + 2560 * 4096 + 2 * 9728 * 2560 + 2560 * 9728
+    weights = 5 * per_layer
+    scales = 2 * 5 * (6144 + 2560 + 2 * 9728 + 2560)
+    lm = 2 * 151936 * 2560
+    kv = 5 * 512 * 8 * 128 * 2 * 2
+    assert c.step_bytes([512]) == weights + scales + lm + kv == 1293332480
+    assert c.step_bytes_w4([512]) == weights // 2 + weights // 64 + lm + kv == 1048596480
+
+
+def test_standin_chunks_cover_the_vocabulary():
+    for cfg in ALL:
+        ch = WL.standin_chunks(cfg)
+        assert ch[0][0] == 0 and ch[-1][1] == cfg.V
+        assert all(a[1] == b[0] for a, b in zip(ch, ch[1:]))
+        assert all((r1 - r0) % 128 == 0 and r1 - r0 <= WL.STANDIN_CHUNK for r0, r1 in ch)
+    assert WL.standin_chunks(TINY) == [(0, 4096)]
+
+
+def _pack4_by_element(q, s, layout):
+    """The packed int4 layout written element by element: tile (nt, kt) of
+    8448 bytes; lane chunk (warp w, k-step ks, lane l) at 8 (256 w + 32 ks + l)
+    holds two words, word f for m-group 2w + f; nibble k of a word is element
+    (row g + 8 (k & 1), column 2t + (k >> 2) + 8 ((k >> 1) & 1)) of the lane's
+    fragment (g = l / 4, t = l % 4), stored as q + 8; the tile's 128 packed
+    rows' scales follow at byte 8192."""
+    N, K = q.shape
+    KT = K // 128
+    buf = np.zeros((N // 128) * KT * 8448, np.uint8)
+
+    def lrow(pr):
+        if layout != 1:
+            return pr
+        tl, rr = pr >> 7, pr & 127
+        return tl * 64 + rr if rr < 64 else N // 2 + tl * 64 + rr - 64
+
+    for nt in range(N // 128):
+        for kt in range(KT):
+            base = (nt * KT + kt) * 8448
+            for r in range(128):
+                buf[base + 8192 + 2 * r:base + 8194 + 2 * r] = np.array([s[lrow(nt * 128 + r), kt]], "<f2").view(np.uint8)
+            for w in range(4):
+                for ks in range(8):
+                    for ln in range(32):
+                        g, t = ln // 4, ln % 4
+                        words = []
+                        for f in range(2):
+                            wd = 0
+                            for k in range(8):
+                                row = lrow(nt * 128 + (2 * w + f) * 16 + g + 8 * (k & 1))
+                                col = kt * 128 + ks * 16 + 2 * t + (k >> 2) + 8 * ((k >> 1) & 1)
+                                wd |= (int(q[row, col]) + 8) << (4 * k)
+                            words.append(wd)
+                        off = base + 8 * (256 * w + 32 * ks + ln)
+                        buf[off:off + 8] = np.array(words, "<u4").view(np.uint8)
+    return buf
+
+
+def test_int4_tile_decoder_reads_the_layout():
+    rng = np.random.default_rng(3)
+    w = rng.standard_normal((256, 256)).astype(np.float32)
+    q, s = O.pack_w4a16(w)
+    for layout in (0, 1):
+        q2, s2 = unpack_tiled_q4(_pack4_by_element(q, s, layout), 256, 256, layout)
+        assert np.array_equal(q2, q)
+        assert np.array_equal(s2.view(np.uint16), s.view(np.uint16))
