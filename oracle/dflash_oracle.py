@@ -24,8 +24,13 @@ Sources (web pages on DFlash; cited by page title and section):
 
 Where the pages are silent the plainest reading is taken and the docstring of
 the function that takes it says so.  Parity status of each function is stated
-in its docstring; the whole-drafter composition (norm placement, context path,
-RoPE base, eps) is "parity unpinned" by the pages.
+in its docstring.  The whole-drafter composition has no worked example in the
+pages; it is pinned by invariants instead (a layer with zero output
+projections is the identity, context order does not matter, greedy
+speculative decoding reproduces plain greedy decoding).  The conventions it
+takes where the pages are silent (norm placement on the context path, RoPE
+base, eps) are readings no pin can fix: for those choices parity is
+"parity unpinned".
 """
 from __future__ import annotations
 

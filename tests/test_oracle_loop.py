@@ -105,3 +105,60 @@ def test_draft_block_structure(setup):
     # the context conditions every slot
     out3 = O.draft_block(D, 3, [k[:10] for k in Ks], [v[:10] for v in Vs])
     assert np.all(np.abs(out3["logits"] - out["logits"]).max(axis=1) > 0)
+
+
+def _zero(W, name):
+    q, s = W[name]
+    W[name] = (np.zeros_like(q), s)
+
+
+def _one_layer_from(W2, l):
+    """A 1-layer weight dict holding layer l of a 2-layer one."""
+    W1 = {k: v for k, v in W2.items() if not k[-1].isdigit()}
+    for m in ("qkv", "o", "gu", "down"):
+        W1[f"{m}0"] = W2[f"{m}{l}"]
+    for gname in ("gamma_in", "gamma_post", "gamma_q", "gamma_k"):
+        W1[gname] = W2[gname][l:l + 1]
+    return W1
+
+
+@pytest.mark.parametrize("zeroed", [0, 1])
+def test_zero_branch_layer_is_the_identity(zeroed):
+    # a layer whose o and down projections are zero adds nothing to the
+    # residual stream, so a 2-layer drafter with one such layer equals the
+    # 1-layer drafter made of the other layer -- exactly (pins the residual
+    # wiring, the layer order and which gammas / K/V each layer uses)
+    cfg2 = dataclasses.replace(MICRO, L=2, seed=91)
+    W2 = synth.drafter_weights(cfg2)
+    _zero(W2, f"o{zeroed}")
+    _zero(W2, f"down{zeroed}")
+    keep = 1 - zeroed
+    W1 = _one_layer_from(W2, keep)
+    D2, D1 = O.Drafter(cfg2, W2), O.Drafter(MICRO, W1)
+    hid = synth.target_hidden(5, "idl", 24, MICRO.k * MICRO.H)
+    K2, V2 = O.context_kv(D2, hid)
+    K1, V1 = O.context_kv(D1, hid)
+    a = O.draft_block(D2, 11, K2, V2)
+    b = O.draft_block(D1, 11, K1, V1)
+    assert np.array_equal(a["logits"], b["logits"]) and np.array_equal(a["draft"], b["draft"])
+    # negative control: without the zeroing the 2-layer drafter differs
+    W2b = synth.drafter_weights(cfg2)
+    D2b = O.Drafter(cfg2, W2b)
+    Kb, Vb = O.context_kv(D2b, hid)
+    assert np.abs(O.draft_block(D2b, 11, Kb, Vb)["logits"] - b["logits"]).max() > 1e-3
+
+
+def test_context_order_does_not_matter(setup):
+    # context keys carry their positions inside K (RoPE applied at commit), and
+    # the block attends to all of them without a mask: permuting the context
+    # rows (K and V together) leaves the draft unchanged
+    W, D, *_ = setup
+    hid = synth.target_hidden(5, "perm", 30, MICRO.k * MICRO.H)
+    Ks, Vs = O.context_kv(D, hid)
+    perm = np.random.default_rng(4).permutation(30)
+    a = O.draft_block(D, 7, Ks, Vs)
+    b = O.draft_block(D, 7, [k[perm] for k in Ks], [v[perm] for v in Vs])
+    assert np.allclose(a["logits"], b["logits"], rtol=1e-12, atol=1e-12)
+    # negative control: permuting K alone (breaking the K/V pairing) changes it
+    c = O.draft_block(D, 7, [k[perm] for k in Ks], Vs)
+    assert np.abs(c["logits"] - a["logits"]).max() > 1e-6
