@@ -194,12 +194,12 @@ def run_reference(args, rank, world):
         return synth.verify_logits(cfg.seed, "verify", draft[None], cfg.R, cfg.V, nacc)[0]
 
     steps = max(1, args.steps)
-    budget = 150.0  # seconds of oracle work for the whole arm
+    cap_s = 150.0  # seconds of oracle work for the whole arm
     warm = oracle_step_time(cfg, W, hid, t0, blk, logits_fn, 1)
-    nwarm = max(0, min(args.warmup, int(0.3 * budget / max(warm[0], 1e-3))) - 1)
+    nwarm = max(0, min(args.warmup, int(0.3 * cap_s / max(warm[0], 1e-3))) - 1)
     if nwarm:
         oracle_step_time(cfg, W, hid, t0, blk, logits_fn, nwarm)
-    run = max(1, min(steps, int(0.7 * budget / max(warm[0], 1e-3))))
+    run = max(1, min(steps, int(0.7 * cap_s / max(warm[0], 1e-3))))
     ts = oracle_step_time(cfg, W, hid, t0, blk, logits_fn, run)
     per = statistics.median(ts)
     value = cfg.b / per

@@ -88,7 +88,7 @@ struct W8Args {
   float inv_lo[64];
 };
 
-// Tensor-map encoder from the driver (resolved once through the runtime).
+// Tensor-map encoder of the CUDA driver API (resolved once through the runtime).
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);
 

@@ -280,7 +280,7 @@ DFLASH_API int32_t dflash_verify_accept(const float* logits, const int32_t* draf
                              int32_t* emitted_out, int32_t* next_tok_out,
                              void* ws, size_t ws_bytes, void* stream);
 
-/* Allocation-free verify-accept.  The paper has no counterpart to this call;
+/* Allocation-free verify-accept.  The pages describe no counterpart to this call;
  * it exists for callers that cannot allocate device memory themselves (for
  * example code running inside a stream capture that forbids allocation,
  * embedders whose memory is fully pre-reserved by another allocator, or

@@ -86,7 +86,7 @@ def dequant_w4(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     fp16 scale per output row and 128-column group.  A 4-bit drafter is the
     pages' default (mlx-dspark v0.0.3 release notes, "Notes": drafter
     quantisation does not affect acceptance, 4-bit stays the default); the
-    symmetric format and the group size are this build's reading.  Pinned:
+    symmetric format and the group size are a reading (the pages give neither).  Pinned:
     exact (q * s fits in fp32)."""
     sg = np.repeat(np.asarray(s, dtype=np.float16).astype(F64), GROUP4, axis=1)
     return q.astype(F64) * sg
