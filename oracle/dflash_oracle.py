@@ -45,7 +45,8 @@ F64 = np.float64
 # storage decoding (inputs arrive rounded to their storage types)
 # ----------------------------------------------------------------------------
 def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
-    """bf16 bit patterns (uint16) -> float64 (exact)."""
+    """bf16 bit patterns (uint16) -> float64 (exact).  Pinned on patterns
+    decoded by hand (normal, subnormal, signed zero, largest finite, inf)."""
     u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
     return u.view(np.float32).astype(F64)
 
@@ -262,6 +263,10 @@ def argmax_lowest(x: np.ndarray) -> np.ndarray:
 
 
 def top2_margin(x: np.ndarray) -> np.ndarray:
+    """Gap between the largest and the second-largest entry of each row
+    (counting repeats, so a tied maximum gives 0).  The GPU's draft tokens
+    are compared with the oracle's only where this gap exceeds 1e-2.  Pinned
+    on hand-worked rows (ties, all-negative rows)."""
     part = np.partition(x, -2, axis=-1)
     return part[..., -1] - part[..., -2]
 
@@ -319,7 +324,9 @@ def draft_block(D: Drafter, t0: int, ctxK: List[np.ndarray], ctxV: List[np.ndarr
 
 def lmhead_logits(h: np.ndarray, w_bits: np.ndarray, chunk: int = 16384) -> np.ndarray:
     """logits = h W_lm^T with the target's shared bf16 lm-head [dspark
-    "Highlights": the drafter reuses the target's embedding and lm-head]."""
+    "Highlights": the drafter reuses the target's embedding and lm-head],
+    computed over vocabulary chunks.  Pinned on hand-built tables whose
+    vocabulary spans several chunk boundaries."""
     h = np.asarray(h, dtype=F64)
     V = w_bits.shape[0]
     out = np.empty((h.shape[0], V), dtype=F64)
@@ -331,7 +338,8 @@ def lmhead_logits(h: np.ndarray, w_bits: np.ndarray, chunk: int = 16384) -> np.n
 
 def lmhead_argmax(h_bits: np.ndarray, w_bits: np.ndarray):
     """argmax over the vocabulary of bf16 h[M][H] . bf16 W[V][H]^T, lowest
-    index on ties; also the maximum logit and the top-2 margin."""
+    index on ties; also the maximum logit and the top-2 margin.  Pinned on a
+    hand-worked 9-row table with a tied maximum."""
     lg = lmhead_logits(bf16_to_f64(h_bits), w_bits)
     return argmax_lowest(lg).astype(np.int32), lg.max(axis=-1), top2_margin(lg), lg
 
