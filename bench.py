@@ -9,6 +9,12 @@ weights, prompts or datasets exist here); they stand in for the pages'
 Qwen3-class drafters and prompt suites.  The committed context length is
 reset before every step so every step sees the same context.
 
+The default workload is the 27B-class drafter of the mirror-sd README's
+"Results" table (5 layers, hidden 5120, block 32) with 4096 committed
+context rows; the draft step is also timed at 64 and 2048 rows, the table's
+other contexts.  The headline runs in the library's early-launch mode (one
+stream on a dedicated GPU); the stream-order mode is timed beside it.
+
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle as it
 stands on the host cores instead.
 """
@@ -32,7 +38,8 @@ import numpy as np  # noqa: E402
 from block_diffusion_speculative_draft_gb300 import configs, synth  # noqa: E402
 
 METRIC = "draft-step µs & weight GB/s vs ~8 TB/s HBM; verify-accept blocks/s (1×GB300)"
-DEFAULT_CFG = configs.QWEN3_4B
+DEFAULT_CFG = configs.DENSE_27B.with_ctx((4096,))
+CTX_SWEEP = configs.DENSE_27B_CTX_SWEEP
 FALLBACK_HBM_GBS = 6800.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch from one ncu capture
@@ -175,23 +182,35 @@ def cores() -> int:
 
 
 def pick_config(args):
-    """The named workload (--config), else the default Qwen3-4B shape."""
+    """The named workload (--config), else the default 27B-class drafter at
+    4096 context rows."""
     return configs.BY_NAME[args.config] if getattr(args, "config", None) else DEFAULT_CFG
+
+
+def config_dict(cfg, ctx, world: int) -> dict:
+    """The `config` object both arms print for a workload."""
+    step_bytes = cfg.step_bytes(list(ctx))
+    return {"workload": cfg.name, "b": cfg.b, "B": cfg.B, "ctx": [int(c) for c in ctx], "L": cfg.L,
+            "H": cfg.H, "V": cfg.V,
+            "l2": f"inputs larger than L2: {step_bytes / 1e9:.2f} GB of weights, lm-head and KV streamed per step",
+            "parallelism": f"replicas x{world}"}
 
 
 def run_reference(args, rank, world):
     if rank != 0:
         return
+    from block_diffusion_speculative_draft_gb300.workload import contexts
     cfg = pick_config(args)
     W = synth.drafter_weights(cfg)
-    C = cfg.ctx[0]
+    ctx = contexts(cfg)
+    C = int(ctx[0])
     hid = synth.target_hidden(cfg.seed, "ctx0", C, cfg.k * cfg.H)
-    blk = synth.target_hidden(cfg.seed, "blk", cfg.B, cfg.k * cfg.H)
-    t0 = int(synth.tokens(cfg.seed, "t0", 1, cfg.V)[0])
-    nacc = synth.accept_lengths(cfg.seed, "acc", 1, cfg.B - 1, cfg.accept_mean)
+    blk = synth.target_hidden(cfg.seed, "blk0", cfg.B, cfg.k * cfg.H)
+    t0 = int(synth.tokens(cfg.seed, "t0", cfg.b, cfg.V)[0])
+    nacc = synth.accept_lengths(cfg.seed, "acc", cfg.b, cfg.B - 1, cfg.accept_mean)
 
     def logits_fn(draft):
-        return synth.verify_logits(cfg.seed, "verify", draft[None], cfg.R, cfg.V, nacc)[0]
+        return synth.verify_logits(cfg.seed, "verify", draft[None], cfg.R, cfg.V, nacc[:1])[0]
 
     steps = max(1, args.steps)
     cap_s = 150.0  # seconds of oracle work for the whole arm
@@ -202,20 +221,56 @@ def run_reference(args, rank, world):
     run = max(1, min(steps, int(0.7 * cap_s / max(warm[0], 1e-3))))
     ts = oracle_step_time(cfg, W, hid, t0, blk, logits_fn, run)
     per = statistics.median(ts)
-    value = cfg.b / per
+    value = 1.0 / per  # one sequence per oracle step
     out = {"metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": world, "steps": run,
            "warmup": 1 + nwarm, "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
-           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": cfg.name, "b": cfg.b, "B": cfg.B, "ctx": C},
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_dict(cfg, ctx, world),
            "impl": "reference",
            "cpu_baseline": {"value": value, "unit": "blocks/s", "cores": cores(), "kind": "oracle",
-                            "sample": f"{run} oracle step(s) (draft + verify-accept + commit) of one "
-                                      f"sequence of {cfg.name}; {steps} requested"},
+                            "sample": f"{run} oracle step(s) (draft + verify-accept + commit) of sequence 0 of "
+                                      f"{cfg.name}; {steps} requested"},
            "e2e": {"value": value, "unit": "blocks/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 
 
 # -------------------------------------------------------------- GPU leg ----
+def timed_graph(torch, g, K, W_, world, dev):
+    """K replays of a CUDA graph after W_ warm-up replays: (total ms over the
+    slowest rank, per-replay ms).  Events on the current stream, a barrier and
+    a synchronize on both sides."""
+    for _ in range(W_):
+        g.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    evs[0].record()
+    for i in range(K):
+        g.replay()
+        evs[i + 1].record()
+    torch.cuda.synchronize()
+    per = [evs[i].elapsed_time(evs[i + 1]) for i in range(K)]
+    return max_over_ranks(evs[0].elapsed_time(evs[K]), world, dev), per
+
+
+def capture(torch, fn, reps=1):
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()  # one eager run: kernel attributes and caches are set before capture
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    return g
+
+
+def med_us(ms_list) -> float:
+    return statistics.median(ms_list) * 1e3
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     from block_diffusion_speculative_draft_gb300 import api
@@ -224,24 +279,39 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     cfg = pick_config(args)
-    b = cfg.b
+    b, B = cfg.b, cfg.B
+    K, Wm = args.steps, max(3, args.warmup)
+    hbm, peak_kind = peaks()
     W = synth.drafter_weights(cfg)
     model = api.DeviceDrafter(cfg, W, dev)
     ctx = contexts(cfg)
-    kv = api.KVCache(cfg, b, int(ctx.max()) + 2 * cfg.B, dev)
-    ws = api.workspace(cfg, b, cfg.B, dev)
-    commit_contexts(api, torch, cfg, model, kv, ws, ctx, cfg.B, dev)
+    # context sweep: (label, committed length per sequence); the default
+    # workload also times the pages' other contexts, any other workload its own
+    if b == 1 and args.config is None:
+        sweep = [(str(C), [C]) for C in sorted(set(int(c) for c in CTX_SWEEP) | {int(ctx[0])})]
+    else:
+        sweep = [("ctx", [int(c) for c in ctx])]
+    cmax = max(max(lens) for _, lens in sweep)
+    # one cache holding the largest context: context row j depends only on
+    # target row j and position j, so a shorter context is the same cache
+    # with a smaller committed length
+    kv = api.KVCache(cfg, b, cmax + 2 * B, dev)
+    ws = api.workspace(cfg, b, B, dev)
+    full_ctx = np.maximum(ctx, cmax) if len(sweep) > 1 else ctx
+    head_label = str(int(ctx[0])) if len(sweep) > 1 else "ctx"
+    commit_contexts(api, torch, cfg, model, kv, ws, full_ctx, B, dev)
     torch.cuda.synchronize()
-    len0 = kv.len.clone()
+    len0 = torch.from_numpy(np.asarray(ctx, np.int32)).to(dev)
+    kv.len.copy_(len0)
 
     t0 = torch.from_numpy(synth.tokens(cfg.seed, "t0", b, cfg.V)).to(dev)
-    draft = torch.empty((b, cfg.B - 1), dtype=torch.int32, device=dev)
+    draft = torch.empty((b, B - 1), dtype=torch.int32, device=dev)
     api.dflash_draft_block(model, kv, t0, draft, ws)
     torch.cuda.synchronize()
-    nacc = synth.accept_lengths(cfg.seed, "acc", b, cfg.B - 1, cfg.accept_mean)
+    nacc = synth.accept_lengths(cfg.seed, "acc", b, B - 1, cfg.accept_mean)
     lg_host = synth.verify_logits(cfg.seed, "verify", draft.cpu().numpy(), cfg.R, cfg.V, nacc)
     logits = torch.from_numpy(lg_host).to(dev)
-    blk_host = np.stack([synth.target_hidden(cfg.seed, f"blk{j}", cfg.B, cfg.k * cfg.H) for j in range(b)])
+    blk_host = np.stack([synth.target_hidden(cfg.seed, f"blk{j}", B, cfg.k * cfg.H) for j in range(b)])
     blk = torch.from_numpy(blk_host).to(dev)
     n_out = torch.empty(b, dtype=torch.int32, device=dev)
     corr = torch.empty(b, dtype=torch.int32, device=dev)
@@ -262,211 +332,202 @@ def run_ours(args, rank, world, local_rank):
         api.dflash_commit_draft_block(model, kv, blk, n_out, t0, draft, ws)
         api.dflash_verify_accept(logits, draft, n_out, corr, emitted, nxt, vws)
 
-    def draft_only():
-        api.dflash_draft_block(model, kv, t0, draft, ws)
+    results = {}
+    for mode, mname in ((api.LAUNCH_EARLY, "early"), (api.LAUNCH_STREAM_ORDER, "stream_order")):
+        with api.launch_mode(mode):
+            g_step = capture(torch, step)
+            if mode == api.LAUNCH_EARLY:
+                with ClockSampler(local_rank) as clk:
+                    total_ms, _ = timed_graph(torch, g_step, K, Wm, world, dev)
+                clocks = clk.summary()
+            else:
+                total_ms, _ = timed_graph(torch, g_step, K, Wm, world, dev)
+            res = {"step_total_ms": total_ms, "draft_us": {}}
+            for label, lens in sweep:
+                cl = torch.tensor(lens, dtype=torch.int32, device=dev)
 
-    s = torch.cuda.Stream(device=dev)
-    s.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(s):
-        for _ in range(3):
-            step_folded()
-            step()
-    torch.cuda.current_stream().wait_stream(s)
-    torch.cuda.synchronize()
-    assert api.dflash_get_status() == 0, "device status flagged during warm-up"
+                def draft_only():
+                    kv.len.copy_(cl)
+                    api.dflash_draft_block(model, kv, t0, draft, ws)
 
-    def capture(fn, reps=1):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for _ in range(reps):
-                fn()
-        return g
-
-    g_step = capture(step)
-    g_folded = capture(step_folded)
-    g_draft = capture(draft_only)
-    g_fused = None
-    if cfg.M <= 32:
-        try:
-            api.dflash_draft_block_fused(model, kv, t0, draft, ws)
-            torch.cuda.synchronize()
-            g_fused = capture(lambda: api.dflash_draft_block_fused(model, kv, t0, draft, ws))
-        except api.DflashError:
-            g_fused = None
-    VREP = 100
-    g_verify = capture(lambda: api.dflash_verify_accept(logits, draft, n_out, corr, emitted, nxt, vws), VREP)
-    # temperature speculative-sampling accept on the same rows (T = 0.8,
-    # uniforms drawn once on the device)
-    u_acc = torch.rand((b, cfg.B - 1), device=dev).clamp_(1e-7, 1 - 1e-7)
-    u_smp = torch.rand((b, cfg.V), device=dev).clamp_(1e-7, 1 - 1e-7)
-    sws = torch.zeros(api.dflash_verify_sample_workspace_size(b, cfg.R, cfg.V), dtype=torch.uint8, device=dev)
-    s_n, s_c = torch.empty_like(n_out), torch.empty_like(corr)
-    g_sample = capture(lambda: api.dflash_verify_accept_sample(logits, draft, 0.8, u_acc, u_smp, s_n, s_c,
-                                                               ws=sws), VREP)
-    M1 = b * (cfg.B - 1)
-    lm_idx = torch.empty(M1, dtype=torch.int32, device=dev)
-    lmws = torch.zeros(4096, dtype=torch.uint8, device=dev)
-    hbuf = torch.zeros((M1, cfg.H), dtype=torch.bfloat16, device=dev)
-    g_lm = capture(lambda: api.dflash_lmhead_argmax(hbuf.view(torch.int16), model.lm_t, lm_idx, ws=lmws))
-
-    def timed(g, K, W_):
-        for _ in range(W_):
-            g.replay()
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-        evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
-        evs[0].record()
-        for i in range(K):
-            g.replay()
-            evs[i + 1].record()
-        torch.cuda.synchronize()
-        per = [evs[i].elapsed_time(evs[i + 1]) for i in range(K)]
-        total = max_over_ranks(evs[0].elapsed_time(evs[K]), world, dev)
-        return total, per
-
-    K, Wm = args.steps, max(3, args.warmup)
-    with ClockSampler(local_rank) as clk:
-        total_ms, per_ms = timed(g_step, K, Wm)
-    clocks = clk.summary()
-    fold_total, _ = timed(g_folded, K, Wm)
-    _, draft_ms = timed(g_draft, K, Wm)
-    fused_ms = timed(g_fused, K, Wm)[1] if g_fused is not None else None
-    _, ver_ms = timed(g_verify, max(3, K // 5), 2)
-    _, smp_ms = timed(g_sample, max(3, K // 5), 2)
-    _, lm_ms = timed(g_lm, K, Wm)
+                _, per = timed_graph(torch, capture(torch, draft_only), K, Wm, world, dev)
+                res["draft_us"][label] = per
+            kv.len.copy_(len0)
+            results[mname] = res
+            del g_step
     assert api.dflash_get_status() == 0, "device status flagged during the timed region"
+    early = results["early"]
+    dms = statistics.median(early["draft_us"][head_label])
 
-    # end to end through the public API with host buffers: H2D of the step's
-    # inputs (last token, target logits, target hidden rows), D2H of results
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    h_t0, h_lg, h_blk = pin(t0.cpu().numpy()), pin(lg_host), pin(blk_host)
-    o_draft = torch.empty_like(draft, device="cpu").pin_memory()
-    o_n = torch.empty_like(n_out, device="cpu").pin_memory()
-    o_em = torch.empty_like(emitted, device="cpu").pin_memory()
-    o_nx = torch.empty_like(nxt, device="cpu").pin_memory()
-    h2d = h_t0.numel() * 4 + h_lg.numel() * 4 + h_blk.numel() * 2
-    d2h = (o_draft.numel() + o_n.numel() + o_em.numel() + o_nx.numel()) * 4
+    with api.launch_mode(api.LAUNCH_EARLY):
+        fold_total, _ = timed_graph(torch, capture(torch, step_folded), K, Wm, world, dev)
+        VREP = 100
+        _, ver_ms = timed_graph(torch, capture(torch, lambda: api.dflash_verify_accept(
+            logits, draft, n_out, corr, emitted, nxt, vws), VREP), max(3, K // 20), 2, world, dev)
+        # temperature speculative-sampling accept on the same rows (T = 0.8,
+        # uniforms drawn once on the device)
+        u_acc = torch.rand((b, B - 1), device=dev).clamp_(1e-7, 1 - 1e-7)
+        u_smp = torch.rand((b, cfg.V), device=dev).clamp_(1e-7, 1 - 1e-7)
+        sws = torch.zeros(api.dflash_verify_sample_workspace_size(b, cfg.R, cfg.V), dtype=torch.uint8, device=dev)
+        s_n, s_c = torch.empty_like(n_out), torch.empty_like(corr)
+        _, smp_ms = timed_graph(torch, capture(torch, lambda: api.dflash_verify_accept_sample(
+            logits, draft, 0.8, u_acc, u_smp, s_n, s_c, ws=sws), VREP), max(3, K // 20), 2, world, dev)
+        # the lm-head alone (same table, bf16 rows)
+        M1 = b * (B - 1)
+        lm_idx = torch.empty(M1, dtype=torch.int32, device=dev)
+        lmws = torch.zeros(4096, dtype=torch.uint8, device=dev)
+        hbuf = torch.zeros((M1, cfg.H), dtype=torch.bfloat16, device=dev)
+        _, lm_ms = timed_graph(torch, capture(torch, lambda: api.dflash_lmhead_argmax(
+            hbuf.view(torch.int16), model.lm_t, lm_idx, ws=lmws)), K, Wm, world, dev)
+        # the projection kernel alone, over the step's 4 L layer matrices in
+        # the step's order (plain fp32 store epilogue, same weight stream)
+        xs = torch.zeros((cfg.M, max(cfg.H, cfg.F, cfg.nq * cfg.d)), dtype=torch.float16, device=dev)
+        ys = torch.empty((cfg.M, max(cfg.nqkv, cfg.H, 2 * cfg.F)), dtype=torch.float32, device=dev)
+        mats = []
+        for l in range(cfg.L):
+            for name in ("qkv", "o", "gu", "down"):
+                mats.append(getattr(model, name)[l])
+        proj_bytes = sum(m.N * m.K + 2 * m.N + 2 * cfg.M * m.K + 4 * cfg.M * m.N for m in mats)
 
-    def e2e_step():
-        t0.copy_(h_t0, non_blocking=True)
-        logits.copy_(h_lg, non_blocking=True)
-        blk.copy_(h_blk, non_blocking=True)
-        g_step.replay()
-        o_draft.copy_(draft, non_blocking=True)
-        o_n.copy_(n_out, non_blocking=True)
-        o_em.copy_(emitted, non_blocking=True)
-        o_nx.copy_(nxt, non_blocking=True)
+        def projections():
+            for m in mats:
+                api.dflash_w8a16_linear(m, xs.view(-1)[:cfg.M * m.K].view(cfg.M, m.K),
+                                        y=ys.view(-1)[:cfg.M * m.N].view(cfg.M, m.N))
 
-    for _ in range(Wm):
-        e2e_step()
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(K):
-        e2e_step()
-    e1.record()
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+        _, proj_ms = timed_graph(torch, capture(torch, projections), K, Wm, world, dev)
+
+        # end to end through the public API with host buffers, every step:
+        # H2D of the step's inputs (last token, target logits, target hidden
+        # rows) from pinned memory, the three C-ABI calls issued eagerly, D2H
+        # of the drafts and accept outputs
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        h_t0, h_lg, h_blk = pin(t0.cpu().numpy()), pin(lg_host), pin(blk_host)
+        o_draft = torch.empty_like(draft, device="cpu").pin_memory()
+        o_n = torch.empty_like(n_out, device="cpu").pin_memory()
+        o_em = torch.empty_like(emitted, device="cpu").pin_memory()
+        o_nx = torch.empty_like(nxt, device="cpu").pin_memory()
+        h2d = h_t0.numel() * 4 + h_lg.numel() * 4 + h_blk.numel() * 2
+        d2h = (o_draft.numel() + o_n.numel() + o_em.numel() + o_nx.numel()) * 4
+
+        def copies_in():
+            t0.copy_(h_t0, non_blocking=True)
+            logits.copy_(h_lg, non_blocking=True)
+            blk.copy_(h_blk, non_blocking=True)
+
+        def copies_out():
+            o_draft.copy_(draft, non_blocking=True)
+            o_n.copy_(n_out, non_blocking=True)
+            o_em.copy_(emitted, non_blocking=True)
+            o_nx.copy_(nxt, non_blocking=True)
+
+        def e2e_eager():
+            copies_in()
+            step()
+            copies_out()
+
+        g_step = capture(torch, step)
+
+        def e2e_graph():
+            copies_in()
+            g_step.replay()
+            copies_out()
+
+        def timed_host(fn):
+            for _ in range(Wm):
+                fn()
+            torch.cuda.synchronize()
+            if world > 1:
+                torch.distributed.barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(K):
+                fn()
+            e1.record()
+            torch.cuda.synchronize()
+            return max_over_ranks(e0.elapsed_time(e1), world, dev)
+
+        e2e_ms = timed_host(e2e_eager)
+        e2e_graph_ms = timed_host(e2e_graph)
+        assert api.dflash_get_status() == 0, "device status flagged during the API timing"
+        del g_step
 
     # the same draft step with int4 projections (W4A16, group scales in the
     # packed tiles); the cache and inputs are the ones above
-    W4 = synth.drafter_weights(cfg, bits=4)
-    m4 = api.DeviceDrafter(cfg, W4, dev, bits=4)
-    del W4
-    draft4 = torch.empty_like(draft)
-    api.dflash_draft_block(m4, kv, t0, draft4, ws)
-    torch.cuda.synchronize()
-    g_draft4 = capture(lambda: api.dflash_draft_block(m4, kv, t0, draft4, ws))
-    _, draft4_ms = timed(g_draft4, K, Wm)
-    assert api.dflash_get_status() == 0, "device status flagged during the int4 draft timing"
-    del g_draft4, m4
+    w4 = None
+    if not args.no_w4:
+        W4 = synth.drafter_weights(cfg, bits=4)
+        m4 = api.DeviceDrafter(cfg, W4, dev, bits=4)
+        del W4
+        draft4 = torch.empty_like(draft)
+        with api.launch_mode(api.LAUNCH_EARLY):
+            _, d4 = timed_graph(torch, capture(torch, lambda: api.dflash_draft_block(m4, kv, t0, draft4, ws)),
+                                K, Wm, world, dev)
+        assert api.dflash_get_status() == 0, "device status flagged during the int4 draft timing"
+        b4 = cfg.step_bytes_w4(list(ctx))
+        w4 = {"median_us": med_us(d4), "bytes": b4, "frac_of_measured": b4 / (statistics.median(d4) * 1e-3) / 1e9 / hbm}
+        del m4
 
-    # draft || verify overlap: two groups (sequence sets) of this workload on
-    # two streams, each step = draft, the int4 QMM stand-in for the target's
-    # verify forward, verify-accept, commit; serial vs side by side
-    overlap = None
-    if b == 1 and not args.no_overlap:
-        from block_diffusion_speculative_draft_gb300 import workload as WL
-        standin = WL.TargetStandIn(api, torch, cfg, dev)
-        groups = []
-        for i in range(2):
-            hids = [synth.target_hidden(cfg.seed, f"ovl-g{i}-ctx{j}", int(ctx[j]), cfg.k * cfg.H)
-                    for j in range(b)]
-            groups.append(WL.Group(api, torch, cfg, model, dev, ctx, hids,
-                                   synth.tokens(cfg.seed, f"ovl-g{i}-t0", b, cfg.V), f"ovl-g{i}-"))
-        side = [torch.cuda.Stream(device=dev)]
-        WL.run_serial(api, torch, cfg, model, standin, groups, reset=True)
-        WL.run_overlapped(api, torch, cfg, model, standin, groups, side, reset=True, stagger=True)
-        torch.cuda.synchronize()
-        g_ser = capture(lambda: WL.run_serial(api, torch, cfg, model, standin, groups, reset=True))
-        g_free = capture(lambda: WL.run_overlapped(api, torch, cfg, model, standin, groups, side, reset=True))
-        g_stag = capture(lambda: WL.run_overlapped(api, torch, cfg, model, standin, groups, side, reset=True,
-                                                   stagger=True))
-        g_qmm = capture(lambda: api.dflash_w8a16_linear(standin.desc, groups[0].blk.view(-1, cfg.k * cfg.H),
-                                                        ws=standin.ws, y=groups[0].logits.view(-1, cfg.V)))
-        ser_ms, _ = timed(g_ser, K, Wm)
-        free_ms, _ = timed(g_free, K, Wm)
-        stag_ms, _ = timed(g_stag, K, Wm)
-        _, qmm_ms = timed(g_qmm, K, Wm)
-        assert api.dflash_get_status() == 0, "device status flagged during the overlap timing"
-        nb = 2 * b
-        best = min(free_ms, stag_ms)
-        overlap = {
-            "workload": f"2 groups x {cfg.name}; target stand-in: int4 QMM [{cfg.V}][{cfg.k * cfg.H}] "
-                        f"({standin.bytes() / 1e6:.0f} MB) from the block's target hidden rows to its logits",
-            "serial_ms_per_step": ser_ms / K, "free_ms_per_step": free_ms / K, "staggered_ms_per_step": stag_ms / K,
-            "blocks_per_s_serial": whole_job_rate(world, nb, K, ser_ms),
-            "blocks_per_s_free": whole_job_rate(world, nb, K, free_ms),
-            "blocks_per_s_staggered": whole_job_rate(world, nb, K, stag_ms),
-            "standin_qmm_us": statistics.median(qmm_ms) * 1e3,
-            "draft_time_hidden_frac": (ser_ms - best) / K / (nb * statistics.median(draft_ms)),
-        }
-        del g_ser, g_free, g_stag, g_qmm, groups, standin
+    overlap = None if args.no_overlap else overlap_measurement(torch, api, args, world, dev, K, Wm)
 
-    hbm, peak_kind = peaks()
-    ms_step = total_ms / K
-    value = whole_job_rate(world, b, K, total_ms)
-    dms = statistics.median(draft_ms)
+    ms_step = early["step_total_ms"] / K
+    value = whole_job_rate(world, b, K, early["step_total_ms"])
     step_bytes = cfg.step_bytes(list(ctx))
     lm_bytes = cfg.V * cfg.H * 2 + M1 * cfg.H * 2 + M1 * 4
-    lm_avg_ms = statistics.mean(lm_ms)
-    lm_gbs = lm_bytes / (lm_avg_ms * 1e-3) / 1e9
-    tr = NCU_TRAFFIC.get("lmhead_kernel")
-    traffic = tr["bytes"] if tr and tr["src"] == src_hash("k_lmhead.cu") and tr["workload"] == cfg.name else None
+    lm_gbs = lm_bytes / (statistics.mean(lm_ms) * 1e-3) / 1e9
+    proj_avg_ms = statistics.mean(proj_ms) / len(mats)
+    proj_gbs = proj_bytes / (statistics.mean(proj_ms) * 1e-3) / 1e9
+    tr = NCU_TRAFFIC.get("w8_gemm_kernel")
+    traffic = tr["bytes"] if tr and tr["src"] == src_hash("k_gemm_w8.cu") and tr["workload"] == cfg.name else None
+    trl = NCU_TRAFFIC.get("lmhead_kernel")
+    traffic_lm = trl["bytes"] if trl and trl["src"] == src_hash("k_lmhead.cu") and trl["workload"] == cfg.name \
+        else None
+    sweep_out = {}
+    for label, lens in sweep:
+        cb = cfg.step_bytes(lens)
+        sweep_out[label] = {}
+        for mname, res in results.items():
+            dm = statistics.median(res["draft_us"][label])
+            sweep_out[label][mname] = {
+                "median_us": dm * 1e3, "p10_us": float(np.percentile(res["draft_us"][label], 10)) * 1e3,
+                "p90_us": float(np.percentile(res["draft_us"][label], 90)) * 1e3, "bytes": cb,
+                "frac_of_measured": cb / (dm * 1e-3) / 1e9 / hbm, "frac_of_8TBps": cb / (dm * 1e-3) / 1e9 / 8000.0}
     out = {
         "metric": METRIC, "value": value, "unit": "blocks/s", "n_gpus": world, "steps": K, "warmup": Wm,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8xf16->f32 (W8A16), bf16 lm-head, fp16 KV", "data": "synthetic",
-        "config": {"workload": cfg.name, "b": b, "B": cfg.B, "ctx": [int(c) for c in ctx], "L": cfg.L,
-                   "H": cfg.H, "V": cfg.V, "l2": "inputs larger than L2: weights+lm-head "
-                   f"{step_bytes / 1e9:.2f} GB streamed per step", "parallelism": f"replicas x{world}"},
-        "step": "draft + verify-accept + commit of the accepted rows (separate calls)",
-        "step_commit_folded": {"blocks_per_s": whole_job_rate(world, b, K, fold_total),
-                               "ms_per_step": fold_total / K,
+        "config": config_dict(cfg, ctx, world),
+        "launch_mode": "early (programmatic dependent launch; one stream on a dedicated GPU)",
+        "step": "draft + verify-accept + commit of the accepted rows (separate calls, one CUDA graph)",
+        "step_stream_order": {"ms_per_step": results["stream_order"]["step_total_ms"] / K,
+                              "blocks_per_s": whole_job_rate(world, b, K, results["stream_order"]["step_total_ms"])},
+        "step_commit_folded": {"blocks_per_s": whole_job_rate(world, b, K, fold_total), "ms_per_step": fold_total / K,
                                "gpu_launches_per_step": launches_per_step(cfg, folded=True)},
-        "draft_step_us": {"median": dms * 1e3, "p10": float(np.percentile(draft_ms, 10)) * 1e3,
-                          "p90": float(np.percentile(draft_ms, 90)) * 1e3},
+        "draft_step_us": {"median": dms * 1e3, "p10": float(np.percentile(early["draft_us"][head_label], 10)) * 1e3,
+                          "p90": float(np.percentile(early["draft_us"][head_label], 90)) * 1e3},
+        "draft_step_ctx_sweep": sweep_out,
         "draft_step_weight_GBps": step_bytes / (dms * 1e-3) / 1e9,
-        "draft_step_w4a16": {"median_us": statistics.median(draft4_ms) * 1e3,
-                             "bytes": cfg.step_bytes_w4(list(ctx)),
-                             "frac_of_measured": cfg.step_bytes_w4(list(ctx))
-                             / (statistics.median(draft4_ms) * 1e-3) / 1e9 / hbm},
-        "draft_verify_overlap": overlap,
-        "draft_step_fused_kernel_us": None if fused_ms is None else statistics.median(fused_ms) * 1e3,
         "step_roofline": {"bytes": step_bytes, "frac_of_measured": step_bytes / (dms * 1e-3) / 1e9 / hbm,
                           "frac_of_8TBps": step_bytes / (dms * 1e-3) / 1e9 / 8000.0},
+        "draft_step_w4a16": w4,
+        "draft_verify_overlap": overlap,
         "verify_accept_blocks_per_s": b / (statistics.median(ver_ms) / VREP / 1e3),
         "verify_sample_blocks_per_s": b / (statistics.median(smp_ms) / VREP / 1e3),
-        "roofline": {"kernel": "lmhead_kernel (bf16 GEMV + fused argmax)", "bound": "hbm", "achieved": lm_gbs,
-                     "peak": hbm, "unit": "GB/s", "frac": lm_gbs / hbm, "traffic": traffic,
-                     "peak_kind": peak_kind, "algorithmic_bytes_per_launch": lm_bytes},
+        "roofline": {"kernel": f"w8_gemm_kernel: the {len(mats)} layer projections of one draft step, launched "
+                               "back to back alone", "bound": "hbm", "achieved": proj_gbs, "peak": hbm,
+                     "unit": "GB/s", "frac": proj_gbs / hbm, "traffic": traffic, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": proj_bytes / len(mats), "avg_launch_us": proj_avg_ms * 1e3},
+        "roofline_lmhead": {"kernel": "lmhead_kernel (bf16 GEMV + fused argmax), alone", "bound": "hbm",
+                            "achieved": lm_gbs, "peak": hbm, "unit": "GB/s", "frac": lm_gbs / hbm,
+                            "traffic": traffic_lm, "algorithmic_bytes_per_launch": lm_bytes,
+                            "avg_launch_us": statistics.mean(lm_ms) * 1e3},
         "clocks": clocks,
         "gpu_launches": K * launches_per_step(cfg),
         "e2e": {"value": whole_job_rate(world, b, K, e2e_ms), "unit": "blocks/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "path": "pinned host buffers in, dflash_draft_block + dflash_verify_accept + dflash_kv_commit "
+                        "called every step, results back to pinned host buffers"},
+        "e2e_graph": {"value": whole_job_rate(world, b, K, e2e_graph_ms), "unit": "blocks/s",
+                      "path": "the same copies around a replay of the captured step"},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         C = int(ctx[0])
@@ -483,16 +544,66 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(out), flush=True)
 
 
+def overlap_measurement(torch, api, args, world, dev, K, Wm):
+    """Draft || verify overlap on two streams (mirror-sd README, "How It
+    Works"): two groups of the Qwen3-4B-shaped workload, each step = draft,
+    the int4 QMM stand-in for the target's verify forward, verify-accept,
+    commit; serial vs side by side.  Several streams run at once, so the
+    library runs in stream-order mode."""
+    from block_diffusion_speculative_draft_gb300 import workload as WL
+    cfg = configs.QWEN3_4B
+    b = cfg.b
+    model = api.DeviceDrafter(cfg, synth.drafter_weights(cfg), dev)
+    ctx = WL.contexts(cfg)
+    standin = WL.TargetStandIn(api, torch, cfg, dev)
+    groups = []
+    for i in range(2):
+        hids = [synth.target_hidden(cfg.seed, f"ovl-g{i}-ctx{j}", int(ctx[j]), cfg.k * cfg.H) for j in range(b)]
+        groups.append(WL.Group(api, torch, cfg, model, dev, ctx, hids,
+                               synth.tokens(cfg.seed, f"ovl-g{i}-t0", b, cfg.V), f"ovl-g{i}-"))
+    side = [torch.cuda.Stream(device=dev)]
+    with api.launch_mode(api.LAUNCH_STREAM_ORDER):
+        g_ser = capture(torch, lambda: WL.run_serial(api, torch, cfg, model, standin, groups, reset=True))
+        g_free = capture(torch, lambda: WL.run_overlapped(api, torch, cfg, model, standin, groups, side, reset=True))
+        g_stag = capture(torch, lambda: WL.run_overlapped(api, torch, cfg, model, standin, groups, side,
+                                                          reset=True, stagger=True))
+        g_qmm = capture(torch, lambda: api.dflash_w8a16_linear(standin.desc, groups[0].blk.view(-1, cfg.k * cfg.H),
+                                                                ws=groups[0].tws, y=groups[0].logits.view(-1, cfg.V)))
+        g_draft = capture(torch, lambda: api.dflash_draft_block(model, groups[0].kv, groups[0].t0, groups[0].draft,
+                                                                groups[0].ws))
+        ser_ms, _ = timed_graph(torch, g_ser, K, Wm, world, dev)
+        free_ms, _ = timed_graph(torch, g_free, K, Wm, world, dev)
+        stag_ms, _ = timed_graph(torch, g_stag, K, Wm, world, dev)
+        _, qmm_ms = timed_graph(torch, g_qmm, K, Wm, world, dev)
+        _, dr_ms = timed_graph(torch, g_draft, K, Wm, world, dev)
+    assert api.dflash_get_status() == 0, "device status flagged during the overlap timing"
+    nb = 2 * b
+    best = min(free_ms, stag_ms)
+    return {
+        "workload": f"2 groups x {cfg.name}; target stand-in: int4 QMM [{cfg.V}][{cfg.k * cfg.H}] "
+                    f"({standin.bytes() / 1e6:.0f} MB) from the block's target hidden rows to its logits",
+        "launch_mode": "stream order (several streams at once)",
+        "serial_ms_per_step": ser_ms / K, "free_ms_per_step": free_ms / K, "staggered_ms_per_step": stag_ms / K,
+        "blocks_per_s_serial": whole_job_rate(world, nb, K, ser_ms),
+        "blocks_per_s_free": whole_job_rate(world, nb, K, free_ms),
+        "blocks_per_s_staggered": whole_job_rate(world, nb, K, stag_ms),
+        "standin_qmm_us": med_us(qmm_ms), "draft_us": med_us(dr_ms),
+        "draft_time_hidden_frac": (ser_ms - best) / K / (nb * statistics.median(dr_ms)),
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-overlap", action="store_true", help="skip the two-stream draft || verify measurement")
+    ap.add_argument("--no-w4", action="store_true", help="skip the int4 (W4A16) draft timing")
     ap.add_argument("--config", default=None, choices=sorted(configs.BY_NAME),
-                    help="another workload of the parity suite (default: the Qwen3-4B-shaped one)")
+                    help="another workload of the parity suite (default: the 27B-class drafter at 4096 "
+                         "context rows)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

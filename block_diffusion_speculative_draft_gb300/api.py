@@ -26,11 +26,13 @@ DEV_KV_CAPACITY, DEV_BAD_TOKEN, DEV_BAD_LENGTH, DEV_WAIT_TIMEOUT = 0x1, 0x2, 0x4
 EXPORTS = [
     "dflash_version", "dflash_status_string", "dflash_workspace_size", "dflash_pack_w8a16",
     "dflash_w4a16_packed_bytes", "dflash_pack_w4a16",
-    "dflash_w8a16_linear_workspace_size", "dflash_w8a16_linear", "dflash_draft_block", "dflash_draft_block_fused",
+    "dflash_w8a16_linear_workspace_size", "dflash_w8a16_linear", "dflash_draft_block",
     "dflash_lmhead_workspace_size", "dflash_lmhead_argmax", "dflash_verify_workspace_size",
     "dflash_verify_accept", "dflash_verify_accept_noalloc", "dflash_verify_sample_workspace_size",
-    "dflash_verify_accept_sample", "dflash_kv_commit", "dflash_commit_draft_block", "dflash_get_status",
+    "dflash_verify_accept_sample", "dflash_kv_commit", "dflash_commit_draft_block", "dflash_set_launch_mode",
+    "dflash_get_launch_mode", "dflash_get_status",
 ]
+LAUNCH_STREAM_ORDER, LAUNCH_EARLY = 0, 1
 
 
 class DflashError(RuntimeError):
@@ -88,7 +90,6 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dflash_w8a16_linear_workspace_size": ([I64, I64, I64, PSZ], I32),
         "dflash_w8a16_linear": ([ctypes.POINTER(W8), P, I64, P, P, SZ, P], I32),
         "dflash_draft_block": ([ctypes.POINTER(Weights), ctypes.POINTER(KV), P, P, P, P, P, SZ, P], I32),
-        "dflash_draft_block_fused": ([ctypes.POINTER(Weights), ctypes.POINTER(KV), P, P, P, P, P, SZ, P], I32),
         "dflash_lmhead_workspace_size": ([I64, PSZ], I32),
         "dflash_lmhead_argmax": ([P, P, I64, I64, I64, P, P, P, P, SZ, P], I32),
         "dflash_verify_workspace_size": ([I32, I32, I64, PSZ], I32),
@@ -100,6 +101,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "dflash_kv_commit": ([ctypes.POINTER(Weights), ctypes.POINTER(KV), P, I32, P, P, SZ, P], I32),
         "dflash_commit_draft_block": ([ctypes.POINTER(Weights), ctypes.POINTER(KV), P, I32, P, P, P, P, P, P, SZ, P],
                                       I32),
+        "dflash_set_launch_mode": ([I32], I32),
+        "dflash_get_launch_mode": ([], I32),
         "dflash_get_status": ([ctypes.POINTER(ctypes.c_int32), I32], I32),
     }
     if set(sig) != set(EXPORTS):  # every export is called with declared argument types
@@ -192,16 +195,25 @@ def w8_desc(q, s, N: int, K: int, layout: int = LAYOUT_PLAIN, bits: int = 8) -> 
     return W8(q.data_ptr(), s.data_ptr() if s is not None else None, N, K, layout, bits)
 
 
+def dflash_w8a16_linear_workspace_size(M: int, N: int, K: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check("dflash_w8a16_linear_workspace_size",
+           load_library().dflash_w8a16_linear_workspace_size(M, N, K, ctypes.byref(n)))
+    return n.value
+
+
 def dflash_w8a16_linear(desc: W8, x, ws=None, stream=None, y=None):
-    """y[M][N] fp32 = W8(desc) applied to fp16 x[M][K] (y may be given)."""
+    """y[M][N] fp32 = W8(desc) applied to fp16 x[M][K] (y may be given).  ws:
+    a zero-filled uint8 workspace of dflash_w8a16_linear_workspace_size bytes
+    (allocated here when not given)."""
     torch = _torch()
     lib = load_library()
     M = x.shape[0]
-    n = ctypes.c_size_t(0)
-    _check("dflash_w8a16_linear_workspace_size",
-           lib.dflash_w8a16_linear_workspace_size(M, desc.N, desc.K, ctypes.byref(n)))
-    if ws is None or ws.numel() < n.value:
-        ws = torch.zeros(max(n.value, 256), dtype=torch.uint8, device=x.device)
+    need = dflash_w8a16_linear_workspace_size(M, desc.N, desc.K)
+    if ws is None:
+        ws = torch.zeros(max(need, 256), dtype=torch.uint8, device=x.device)
+    elif ws.numel() < need:
+        raise ValueError(f"dflash_w8a16_linear: workspace of {ws.numel()} bytes, {need} needed")
     if y is None:
         y = torch.empty((M, desc.N), dtype=torch.float32, device=x.device)
     elif y.numel() < M * desc.N or not y.is_contiguous() or y.dtype != torch.float32:
@@ -288,14 +300,6 @@ def dflash_draft_block(model: "DeviceDrafter", kv: "KVCache", last_tok, draft_ou
         _ptr(logits), ws.data_ptr(), ws.numel(), _stream(stream)))
 
 
-def dflash_draft_block_fused(model: "DeviceDrafter", kv: "KVCache", last_tok, draft_out, ws, hidden=None,
-                             logits=None, stream=None):
-    """The draft step as one persistent cooperative kernel (b * B <= 32)."""
-    _check("dflash_draft_block_fused", load_library().dflash_draft_block_fused(
-        ctypes.byref(model.c), ctypes.byref(kv.c), last_tok.data_ptr(), draft_out.data_ptr(), _ptr(hidden),
-        _ptr(logits), ws.data_ptr(), ws.numel(), _stream(stream)))
-
-
 def dflash_kv_commit(model: "DeviceDrafter", kv: "KVCache", hid, n, ws, stream=None):
     """hid fp16 [b][rows_per_seq][k*H]; n int32 [b] (device)."""
     rps = hid.shape[1]
@@ -312,6 +316,31 @@ def dflash_commit_draft_block(model: "DeviceDrafter", kv: "KVCache", hid, n, las
     _check("dflash_commit_draft_block", load_library().dflash_commit_draft_block(
         ctypes.byref(model.c), ctypes.byref(kv.c), hid.data_ptr(), rps, n.data_ptr(), last_tok.data_ptr(),
         draft_out.data_ptr(), _ptr(hidden), _ptr(logits), ws.data_ptr(), ws.numel(), _stream(stream)))
+
+
+def dflash_set_launch_mode(mode: int):
+    """LAUNCH_STREAM_ORDER (default) or LAUNCH_EARLY (dedicated GPU, one
+    stream only; see include/dflash.h)."""
+    _check("dflash_set_launch_mode", load_library().dflash_set_launch_mode(mode))
+
+
+def dflash_get_launch_mode() -> int:
+    return load_library().dflash_get_launch_mode()
+
+
+class launch_mode:
+    """Context manager: the given launch mode inside, the previous one after."""
+
+    def __init__(self, mode: int):
+        self.mode = mode
+
+    def __enter__(self):
+        self.prev = dflash_get_launch_mode()
+        dflash_set_launch_mode(self.mode)
+        return self
+
+    def __exit__(self, *exc):
+        dflash_set_launch_mode(self.prev)
 
 
 def dflash_get_status(clear: bool = True) -> int:

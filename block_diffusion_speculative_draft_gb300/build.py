@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdflash.so")
-SOURCES = ["dflash_abi.cu", "k_gemm_w8.cu", "k_lmhead.cu", "k_attn.cu", "k_small.cu", "k_step.cu", "k_sample.cu"]
+SOURCES = ["dflash_abi.cu", "k_gemm_w8.cu", "k_lmhead.cu", "k_attn.cu", "k_small.cu", "k_sample.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-DNDEBUG"]

@@ -26,21 +26,6 @@ int* status_ptr() {
   return ptrs[dev];
 }
 
-struct DevInfo {
-  int sms = 0, smem_optin = 0, smem_sm = 0;
-};
-DevInfo dev_info() {
-  static DevInfo cache[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DevInfo();
-  if (!cache[dev].sms) {
-    cudaDeviceGetAttribute(&cache[dev].sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaDeviceGetAttribute(&cache[dev].smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    cudaDeviceGetAttribute(&cache[dev].smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
-  }
-  return cache[dev];
-}
-
 inline size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -79,43 +64,11 @@ struct WS {
   __nv_bfloat16* h;
   float* ss;  // per-row, per-128-column sums of squares of x (deferred RMSNorm)
   void* lm;
-  // fused-step kernel
-  int* stick;
-  unsigned long long* skeys;
-  unsigned* sbar;
-  float* spart;
-  size_t spart_bytes;
-  float* sattn_o;
-  float* sattn_lse;
   size_t total;
 };
 
-constexpr int kStepMaxSplits = 8;
 // bytes of the lm-head table prefetched into L2 during the layers' attention
 constexpr size_t kLmPrefetchBytes = (size_t)96 << 20;
-
-int step_rows_pad(const dflash_config& c) {
-  const int rows = c.B * (c.nq / c.nkv);
-  return (rows + 63) / 64 * 64;
-}
-
-int step_ntiles_max(const dflash_config& c) {
-  int n = (c.nq + 2 * c.nkv) * c.d;
-  n = n > c.H ? n : c.H;
-  n = n > 2 * c.F ? n : 2 * c.F;
-  return n / 128;
-}
-
-int step_nslots_for(const dflash_config& c, int G) {
-  const int nqkv = (c.nq + 2 * c.nkv) * c.d;
-  int s = step_nslots(nqkv / 128, c.H / 128, G);
-  int t = step_nslots(c.H / 128, c.nq * c.d / 128, G);
-  s = s > t ? s : t;
-  t = step_nslots(2 * c.F / 128, c.H / 128, G);
-  s = s > t ? s : t;
-  t = step_nslots(c.H / 128, c.F / 128, G);
-  return s > t ? s : t;
-}
 
 // Carves the workspace; the lm-head's argmax keys and ticket come first so a
 // single zero-fill of the whole buffer initialises them.
@@ -129,10 +82,6 @@ WS carve(const dflash_config& c, int b, int rps, uint8_t* base) {
     return p;
   };
   w.lm = take(lmhead_ws_bytes(b * (c.B - 1)));
-  const bool step = M <= 32;
-  w.stick = (int*)take(step ? 2 * (size_t)step_ntiles_max(c) * sizeof(int) : 0);
-  w.skeys = (unsigned long long*)take(step ? 32 * sizeof(unsigned long long) : 0);
-  w.sbar = (unsigned*)take(step ? 2 * sizeof(unsigned) : 0);
   w.x = (float*)take((size_t)M * c.H * 4);
   w.u = (__half*)take((size_t)(M + Mc) * c.H * 2);  // block rows, then commit rows
   w.q = (__half*)take((size_t)M * c.nq * c.d * 2);
@@ -142,21 +91,17 @@ WS carve(const dflash_config& c, int b, int rps, uint8_t* base) {
   w.g = (__half*)take((size_t)M * c.F * 2);
   w.h = (__nv_bfloat16*)take((size_t)b * (c.B - 1) * c.H * 2);
   w.ss = (float*)take((size_t)(M + Mc) * (c.H / 128) * 4);
-  w.spart_bytes = step ? (size_t)step_ntiles_max(c) * step_nslots_for(c, 2 * kNumSMs) * 32 * 128 * sizeof(float) : 0;
-  w.spart = (float*)take(w.spart_bytes);
-  const size_t na = step ? (size_t)b * c.nkv * kStepMaxSplits * step_rows_pad(c) : 0;
-  w.sattn_o = (float*)take(na * c.d * sizeof(float));
-  w.sattn_lse = (float*)take(na * sizeof(float));
   w.total = off;
   return w;
 }
 
 int map_err(cudaError_t e) { return e == cudaSuccess ? DFLASH_OK : DFLASH_ECUDA; }
 
-// Every launch, the first of a call included, allows programmatic dependent
-// launch: each kernel reads nothing but constant weights before its
-// griddepcontrol.wait, so it may start while the stream's previous kernel
-// (of this call or of an earlier one) is still finishing.
+// Every launch, the first of a call included, requests programmatic dependent
+// launch, which the library's launch mode grants or not: each kernel reads
+// nothing but constant weights (and, for attention, the context it is given)
+// before its griddepcontrol.wait, so it may start while the stream's
+// previous kernel (of this call or of an earlier one) is still finishing.
 
 W8Args base_args(const dflash_w8& w, int M, int epi) {
   W8Args a;
@@ -308,7 +253,7 @@ static int check_kv(const dflash_kv* kv) {
 // against the grown context, exactly as a commit followed by a draft.
 static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, const int32_t* last_tok,
                                 int32_t* draft_out, float* hidden_out, float* logits_out, void* ws, size_t ws_bytes,
-                                void* stream, bool fused, const uint16_t* hid = nullptr, int rps = 0,
+                                void* stream, const uint16_t* hid = nullptr, int rps = 0,
                                 const int32_t* ncommit = nullptr) {
   if (int r = check_weights(w)) return r;
   if (int r = check_kv(kv)) return r;
@@ -317,12 +262,10 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
   const dflash_config& c = w->cfg;
   const int b = kv->b;
   if ((int64_t)b * c.B > 4096) return DFLASH_EUNSUPPORTED;
-  if (fused && w->fc.bits == 4) return DFLASH_EUNSUPPORTED;  // the single-kernel step is int8 only
   const bool commit = hid != nullptr;
   if (commit) {
     if (!ncommit || !aligned16(hid)) return DFLASH_EINVAL;
     if (rps < 1 || rps > 256 || (int64_t)b * rps > 4096) return DFLASH_EINVAL;
-    if (fused) return DFLASH_EUNSUPPORTED;
   }
   const int rps_ws = commit ? rps : c.B;
   WS need = carve(c, b, rps_ws, nullptr);
@@ -335,104 +278,6 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
   const int qd = c.nq * c.d, kd = c.nkv * c.d;
   const size_t layer_kv = (size_t)b * c.nkv * kv->cap * c.d;
   cudaError_t e;
-  if (fused) {
-    if (M > step_max_mch() || c.L > 8) return DFLASH_EUNSUPPORTED;
-    // the whole step as one persistent kernel when it fits
-    const DevInfo di = dev_info();
-    const int mt = M <= 16 ? 2 : 4;
-    const size_t xb = step_x_bytes(mt, c.d, c.H);
-    // two CTAs per SM: ring depth from half the SM's shared memory
-    int ring = 0, G = 0;
-    if (di.smem_sm > 0) {
-      const size_t per_cta = (size_t)di.smem_sm / 2 - 1024;
-      const size_t fixed = step_smem_bytes(mt, 0, xb);
-      ring = fixed < per_cta ? (int)((per_cta - fixed) / (step_stage_bytes(mt) + 16)) : 0;
-      ring = ring > 4 ? 4 : ring;
-      if (ring >= 2) {
-        const int occ = step_occupancy(mt, step_smem_bytes(mt, ring, xb));
-        G = occ >= 1 ? di.sms * (occ > 2 ? 2 : occ) : 0;
-      }
-    }
-    const size_t ring_bytes = (size_t)ring * step_stage_bytes(mt);
-    const int akt = ring_bytes >= step_attn_bytes(c.d, 64) ? 64 : 32;
-    const int nslots = G > 0 ? step_nslots_for(c, G) : 0;
-    const size_t need_part = (size_t)step_ntiles_max(c) * nslots * 32 * 128 * sizeof(float);
-    if (ring_bytes < step_attn_bytes(c.d, akt)) ring = 0;
-    if (ring >= 2 && G > 0 && need_part <= s.spart_bytes) {
-      StepArgs a;
-      memset(&a, 0, sizeof(a));
-      a.L = c.L;
-      a.H = c.H;
-      a.nq = c.nq;
-      a.nkv = c.nkv;
-      a.d = c.d;
-      a.F = c.F;
-      a.V = c.V;
-      a.B = c.B;
-      a.b = b;
-      a.M = M;
-      a.mask_id = c.mask_id;
-      a.cap = kv->cap;
-      const int nrc = step_rows_pad(c) / 64;
-      int nsa = (G + 2 * b * c.nkv * nrc - 1) / (2 * b * c.nkv * nrc);
-      const int maxk = (kv->cap + c.B + 127) / 128;
-      nsa = nsa > maxk ? maxk : nsa;
-      nsa = nsa > kStepMaxSplits ? kStepMaxSplits : nsa;
-      a.nsa = nsa < 1 ? 1 : nsa;
-      a.ring_stages = ring;
-      a.nslots = nslots;
-      a.xbytes = (int)xb;
-      a.attn_kt = akt;
-      a.ntmax = step_ntiles_max(c);
-      a.eps = c.eps;
-      split_inv_freq(a.inv_hi, a.inv_lo, c.rope_theta, c.d);
-      auto sw = [](const dflash_w8& x) {
-        StepW8 r;
-        r.q = static_cast<const uint8_t*>(x.q);
-        r.s = reinterpret_cast<const __half*>(x.s);
-        r.N = (int)x.N;
-        r.K = (int)x.K;
-        r.layout = x.layout;
-        return r;
-      };
-      for (int l = 0; l < c.L; ++l) {
-        a.qkv[l] = sw(w->qkv[l]);
-        a.o[l] = sw(w->o[l]);
-        a.gu[l] = sw(w->gu[l]);
-        a.down[l] = sw(w->down[l]);
-      }
-      a.gamma_in = w->gamma_in;
-      a.gamma_post = w->gamma_post;
-      a.gamma_q = w->gamma_q;
-      a.gamma_k = w->gamma_k;
-      a.gamma_final = w->gamma_final;
-      a.embed = reinterpret_cast<const __nv_bfloat16*>(w->embed);
-      a.kc = reinterpret_cast<const __half*>(kv->k);
-      a.vc = reinterpret_cast<const __half*>(kv->v);
-      a.len = kv->len;
-      a.last_tok = last_tok;
-      a.draft_out = draft_out;
-      a.hidden_out = hidden_out;
-      a.logits_out = logits_out;
-      a.x = s.x;
-      a.u = s.u;
-      a.q = s.q;
-      a.kb = s.kb;
-      a.vb = s.vb;
-      a.ao = s.ao;
-      a.g = s.g;
-      a.h = s.h;
-      a.part = s.spart;
-      a.tickets = s.stick;
-      a.attn_o = s.sattn_o;
-      a.attn_lse = s.sattn_lse;
-      a.keys = s.skeys;
-      a.bar = s.sbar;
-      a.status = status;
-      return map_err(draft_step(a, reinterpret_cast<const __nv_bfloat16*>(w->lm_head), st, G));
-    }
-    return DFLASH_EUNSUPPORTED;
-  }
   // L2 prefetch of the lm-head: a whole number of rows of each first-round
   // tile, about kLmPrefetchBytes in total
   const bool debug_out = hidden_out || logits_out;
@@ -569,20 +414,14 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
 
 int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* kv, const int32_t* last_tok, int32_t* draft_out,
                            float* hidden_out, float* logits_out, void* ws, size_t ws_bytes, void* stream) {
-  return draft_block_impl(w, kv, last_tok, draft_out, hidden_out, logits_out, ws, ws_bytes, stream, false);
-}
-
-int32_t dflash_draft_block_fused(const dflash_weights* w, const dflash_kv* kv, const int32_t* last_tok,
-                                 int32_t* draft_out, float* hidden_out, float* logits_out, void* ws, size_t ws_bytes,
-                                 void* stream) {
-  return draft_block_impl(w, kv, last_tok, draft_out, hidden_out, logits_out, ws, ws_bytes, stream, true);
+  return draft_block_impl(w, kv, last_tok, draft_out, hidden_out, logits_out, ws, ws_bytes, stream);
 }
 
 int32_t dflash_commit_draft_block(const dflash_weights* w, const dflash_kv* kv, const uint16_t* hid,
                                   int32_t rows_per_seq, const int32_t* n, const int32_t* last_tok, int32_t* draft_out,
                                   float* hidden_out, float* logits_out, void* ws, size_t ws_bytes, void* stream) {
   if (!hid) return DFLASH_EINVAL;
-  return draft_block_impl(w, kv, last_tok, draft_out, hidden_out, logits_out, ws, ws_bytes, stream, false, hid,
+  return draft_block_impl(w, kv, last_tok, draft_out, hidden_out, logits_out, ws, ws_bytes, stream, hid,
                           rows_per_seq, n);
 }
 
@@ -717,6 +556,14 @@ int32_t dflash_kv_commit(const dflash_weights* w, const dflash_kv* kv, const uin
   }
   return map_err(commit_len_update(kv->len, n, b, rows_per_seq, kv->cap, st, true, status));
 }
+
+int32_t dflash_set_launch_mode(int32_t mode) {
+  if (mode != DFLASH_LAUNCH_STREAM_ORDER && mode != DFLASH_LAUNCH_EARLY) return DFLASH_EINVAL;
+  set_launch_mode(mode);
+  return DFLASH_OK;
+}
+
+int32_t dflash_get_launch_mode(void) { return get_launch_mode(); }
 
 int32_t dflash_get_status(int32_t* host_status, int32_t clear) {
   if (!host_status) return DFLASH_EINVAL;

@@ -422,7 +422,7 @@ cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
   // no more splits than keep about two CTAs per SM busy when the batch and
   // the kv heads already fill the GPU (a grid of several waves costs more than
   // longer splits)
-  const int fill = (2 * kNumSMs + a.b * a.nkv - 1) / (a.b * a.nkv);
+  const int fill = (2 * num_sms() + a.b * a.nkv - 1) / (a.b * a.nkv);
   if (ns > fill) ns = fill;
   if (ns > kMaxSplits) ns = kMaxSplits;
   if (ns < 1) ns = 1;

@@ -706,7 +706,7 @@ __global__ void pack4_q_kernel(const void* w, int64_t N, int64_t K, int layout, 
 int w8_pick_splits(int units, int KT) {
   // enough CTAs for two per SM, at most one cluster of 8 splits, and at
   // least two 128-column k-tiles per split
-  int target = 2 * kNumSMs;  // one wave at two CTAs per SM
+  int target = 2 * num_sms();  // one wave at two CTAs per SM
   int s = target / units;
   int smax = KT >= 4 ? KT / 2 : 1;
   if (s > smax) s = smax;

@@ -214,7 +214,7 @@ size_t lmhead_ws_bytes(int64_t M) { return 128 * sizeof(unsigned long long) + 25
 int lmhead_first_tiles(int M, int V) {
   const int chunks = (M + (M <= 16 ? 16 : 32) - 1) / (M <= 16 ? 16 : 32);
   const int ntiles = (V + 127) / 128;
-  int per_chunk = (2 * kNumSMs) / chunks;
+  int per_chunk = (2 * num_sms()) / chunks;
   if (per_chunk < 1) per_chunk = 1;
   return ntiles < per_chunk ? ntiles : per_chunk;  // one CTA per tile of the first round
 }

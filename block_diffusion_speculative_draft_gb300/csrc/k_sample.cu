@@ -170,13 +170,13 @@ __global__ void __launch_bounds__(kThr) sample_pick_kernel(const SampleArgs a) {
 }  // namespace
 
 int sample_parts(int b, int R, int64_t V) {
-  int P = (4 * kNumSMs + b * R - 1) / (b * R);
+  int P = (4 * num_sms() + b * R - 1) / (b * R);
   const int64_t pmax = (V + 2047) / 2048;
   if (P > pmax) P = (int)pmax;
   return P < 1 ? 1 : P;
 }
 int sample_parts2(int b, int64_t V) {
-  int P = (2 * kNumSMs + b - 1) / b;
+  int P = (2 * num_sms() + b - 1) / b;
   const int64_t pmax = (V + 1023) / 1024;
   if (P > pmax) P = (int)pmax;
   return P < 1 ? 1 : P;

@@ -2,6 +2,7 @@
 // RMSNorm, RMSNorm, final norm, commit-length update and the greedy
 // verify-accept; plus the launch and tensor-map helpers shared by all
 // kernels.
+#include <atomic>
 #include <mutex>
 
 #include "kernels.h"
@@ -10,6 +11,25 @@
 namespace dfl {
 
 // ------------------------------------------------------------- helpers ----
+// Launch mode (dflash_set_launch_mode): 0 = stream order, 1 = early launch.
+static std::atomic<int> g_launch_mode{0};
+
+bool launch_early() { return g_launch_mode.load(std::memory_order_relaxed) == 1; }
+void set_launch_mode(int mode) { g_launch_mode.store(mode, std::memory_order_relaxed); }
+int get_launch_mode() { return g_launch_mode.load(std::memory_order_relaxed); }
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
 cudaError_t launch_k(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, void** args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -20,7 +40,7 @@ cudaError_t launch_k(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStr
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = pdl && launch_early() ? 1 : 0;
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
@@ -33,7 +53,7 @@ cudaError_t launch_kc(const void* fn, dim3 grid, dim3 block, size_t smem, cudaSt
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   int n = 0;
-  if (pdl) {
+  if (pdl && launch_early()) {
     attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[n].val.programmaticStreamSerializationAllowed = 1;
     ++n;
@@ -343,7 +363,7 @@ __global__ void __launch_bounds__(256) verify_kernel(const VerifyArgs a) {
 
 int verify_parts(int b, int R, int64_t V) {
   int rows = b * R;
-  int P = (4 * kNumSMs + rows - 1) / rows;
+  int P = (4 * num_sms() + rows - 1) / rows;
   int64_t pmax = (V + 2047) / 2048;
   if (P > pmax) P = (int)pmax;
   if (P < 1) P = 1;

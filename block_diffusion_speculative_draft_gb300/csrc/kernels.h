@@ -9,10 +9,18 @@
 
 namespace dfl {
 
-constexpr int kTile = 128;
-constexpr int kLayersPerLaunch = 8;  // layers batched into one commit GEMM         // packed W8 tile edge (rows x k-columns)
-constexpr int kTileBytes = 16384;  // one packed int8 tile
-constexpr int kNumSMs = 152;
+constexpr int kTile = 128;            // packed weight tile edge (rows x k-columns)
+constexpr int kLayersPerLaunch = 8;   // layers batched into one commit GEMM launch
+constexpr int kTileBytes = 16384;     // one packed int8 tile
+
+// Streaming multiprocessors of the current device (queried once per device).
+int num_sms();
+
+// Whether launches may start early as programmatic dependents of the
+// previous kernel in their stream (the library's launch mode).
+bool launch_early();
+void set_launch_mode(int mode);
+int get_launch_mode();
 
 enum Epi : int {
   EPI_STORE_F32 = 0,  // out[m][n] = y
@@ -92,8 +100,10 @@ struct W8Args {
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);
 
-// Launch helpers: PDL attribute on when `pdl`; launch_kc also groups blocks
-// into thread-block clusters of shape `cluster` (no cluster when 1x1x1).
+// Launch helpers: the programmatic-dependent-launch attribute is set when
+// `pdl` is requested and the library's launch mode allows early launches
+// (launch_early()); launch_kc also groups blocks into thread-block clusters
+// of shape `cluster` (no cluster when 1x1x1).
 cudaError_t launch_k(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, void** args);
 cudaError_t launch_kc(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl, dim3 cluster,
                       void** args);
@@ -191,66 +201,6 @@ cudaError_t verify_sample(const float* logits, const int* draft, int b, int R, i
 size_t verify_ws_bytes(int b, int R, int64_t V);
 cudaError_t verify_accept(const float* logits, const int* draft, int b, int R, int D, int64_t V, int* n_out,
                           int* corr_out, int* emitted, int* next_tok, void* ws, cudaStream_t st, bool pdl);
-
-// --- whole draft step as one persistent cooperative kernel (k_step.cu) ---
-struct StepW8 {
-  const uint8_t* q;
-  const __half* s;
-  int N, K, layout;
-};
-struct StepArgs {
-  int L, H, nq, nkv, d, F, V, B, b, M, mask_id, cap;
-  int nsa;          // attention key splits
-  int ring_stages;  // weight ring depth
-  int nslots;       // partial slots per row tile
-  int xbytes;       // epilogue / reduction region bytes
-  int attn_kt;      // attention key tile (64 or 32)
-  int ntmax;        // row tiles of the widest projection (counter stride)
-  float eps;
-  float inv_hi[64];  // RoPE frequencies as float pairs (see W8Args)
-  float inv_lo[64];
-  StepW8 qkv[8], o[8], gu[8], down[8];
-  const float* gamma_in;
-  const float* gamma_post;
-  const float* gamma_q;
-  const float* gamma_k;
-  const float* gamma_final;
-  const __nv_bfloat16* embed;
-  const __half* kc;
-  const __half* vc;
-  const int* len;
-  const int* last_tok;
-  int* draft_out;
-  float* hidden_out;
-  float* logits_out;
-  float* x;
-  __half* u;
-  __half* q;
-  __half* kb;
-  __half* vb;
-  __half* ao;
-  __half* g;
-  __nv_bfloat16* h;
-  float* part;
-  int* tickets;
-  float* attn_o;
-  float* attn_lse;
-  unsigned long long* keys;
-  unsigned* bar;
-  int* status;
-};
-struct StepMaps {
-  CUtensorMap lm, u, ao, g, h;  // lm-head weights; activation buffers
-};
-int step_max_mch();
-size_t step_stage_bytes(int mt);
-size_t step_smem_bytes(int mt, int ring_stages, size_t xbytes);
-size_t step_x_bytes(int mt, int d, int H);
-int step_nslots(int ntiles, int KT, int G);
-size_t step_attn_bytes(int d, int kt);
-int step_threads();
-int step_occupancy(int mt, size_t smem);
-cudaError_t draft_step(const StepArgs& a, const __nv_bfloat16* lm_head, cudaStream_t st, int G);
 
 // Allocation-free variant of verify_accept: scratch lives in a fixed device
 // array of kNoAllocScratchBytes inside the library (k_small.cu).

@@ -82,7 +82,6 @@ class TargetStandIn:
             del w
         torch.cuda.synchronize()
         self.desc = api.w8_desc(self.q, None, V, K, 0, bits=4)
-        self.ws = torch.zeros(256, dtype=torch.uint8, device=dev)
 
     def bytes(self) -> int:
         V, K = self.cfg.V, self.cfg.k * self.cfg.H
@@ -111,6 +110,9 @@ class Group:
         self.emitted = torch.empty((b, cfg.R), dtype=torch.int32, device=dev)
         self.nxt = torch.empty(b, dtype=torch.int32, device=dev)
         self.vws = torch.zeros(api.dflash_verify_workspace_size(b, cfg.R, V), dtype=torch.uint8, device=dev)
+        # the target stand-in's workspace (each group runs on its own stream)
+        need = api.dflash_w8a16_linear_workspace_size(b * B, V, cfg.k * cfg.H)
+        self.tws = torch.zeros(max(need, 256), dtype=torch.uint8, device=dev)
 
 
 def group_step(api, cfg, model, standin, g, stream=None, reset: bool = False):
@@ -120,7 +122,7 @@ def group_step(api, cfg, model, standin, g, stream=None, reset: bool = False):
     if reset:
         g.kv.len.copy_(g.len0)
     api.dflash_draft_block(model, g.kv, g.t0, g.draft, g.ws, stream=stream)
-    api.dflash_w8a16_linear(standin.desc, g.blk.view(-1, cfg.k * cfg.H), ws=standin.ws, stream=stream,
+    api.dflash_w8a16_linear(standin.desc, g.blk.view(-1, cfg.k * cfg.H), ws=g.tws, stream=stream,
                             y=g.logits.view(-1, cfg.V))
     api.dflash_verify_accept(g.logits, g.draft, g.n, g.corr, g.emitted, g.nxt, g.vws, stream=stream)
     api.dflash_kv_commit(model, g.kv, g.blk, g.n, g.ws, stream=stream)
@@ -152,7 +154,7 @@ def run_overlapped(api, torch, cfg, model, standin, groups, side, reset: bool = 
             api.dflash_draft_block(model, g.kv, g.t0, g.draft, g.ws, stream=s)
             prev_draft = torch.cuda.Event()
             prev_draft.record(s)
-            api.dflash_w8a16_linear(standin.desc, g.blk.view(-1, cfg.k * cfg.H), ws=standin.ws, stream=s,
+            api.dflash_w8a16_linear(standin.desc, g.blk.view(-1, cfg.k * cfg.H), ws=g.tws, stream=s,
                                     y=g.logits.view(-1, cfg.V))
             api.dflash_verify_accept(g.logits, g.draft, g.n, g.corr, g.emitted, g.nxt, g.vws, stream=s)
             api.dflash_kv_commit(model, g.kv, g.blk, g.n, g.ws, stream=s)

@@ -156,10 +156,11 @@ DFLASH_API const char* dflash_version(void);
 /* Human-readable name of a dflash_status (static storage). */
 DFLASH_API const char* dflash_status_string(int32_t status);
 
-/* Workspace bytes for dflash_draft_block and dflash_kv_commit with b
- * sequences and up to rows_per_seq hidden rows per commit call (use B for the
- * decode loop).  One workspace serves both calls.  Returns DFLASH_EINVAL /
- * DFLASH_EUNSUPPORTED for a bad config. */
+/* Workspace bytes for dflash_draft_block, dflash_kv_commit and
+ * dflash_commit_draft_block with b sequences and up to rows_per_seq hidden
+ * rows per commit call (use B for the decode loop).  One workspace serves all
+ * three calls.  Returns DFLASH_EINVAL / DFLASH_EUNSUPPORTED for a bad
+ * config. */
 DFLASH_API int32_t dflash_workspace_size(const dflash_config* cfg, int32_t b,
                               int32_t rows_per_seq, size_t* bytes);
 
@@ -196,7 +197,8 @@ DFLASH_API int32_t dflash_pack_w4a16(const void* w, int32_t w_dtype, int64_t N, 
                           int32_t layout, void* q_out, uint16_t* s_out,
                           void* stream);
 
-/* Workspace bytes for dflash_w8a16_linear. */
+/* Workspace bytes for dflash_w8a16_linear (0: split-K partial sums are
+ * reduced on chip, so the call needs no scratch; ws may be NULL). */
 DFLASH_API int32_t dflash_w8a16_linear_workspace_size(int64_t M, int64_t N, int64_t K,
                                            size_t* bytes);
 
@@ -231,21 +233,6 @@ DFLASH_API int32_t dflash_draft_block(const dflash_weights* w, const dflash_kv* 
                            const int32_t* last_tok, int32_t* draft_out,
                            float* hidden_out, float* logits_out, void* ws,
                            size_t ws_bytes, void* stream);
-
-/* The same draft step as dflash_draft_block, computed by ONE persistent
- * cooperative kernel (all phases of the step inside one launch, two CTAs per
- * SM, weights streamed through a shared-memory ring across phase boundaries,
- * grid barriers between dependent phases).  Same arguments, results within
- * the same tolerances.  Requires b * B <= 32 and L <= 8; otherwise, or when
- * the device cannot hold two such CTAs per SM, returns DFLASH_EUNSUPPORTED.
- * Uses the same workspace as dflash_draft_block. */
-DFLASH_API int32_t dflash_draft_block_fused(const dflash_weights* w,
-                                           const dflash_kv* kv,
-                                           const int32_t* last_tok,
-                                           int32_t* draft_out,
-                                           float* hidden_out,
-                                           float* logits_out, void* ws,
-                                           size_t ws_bytes, void* stream);
 
 /* Workspace bytes for dflash_lmhead_argmax with M rows. */
 DFLASH_API int32_t dflash_lmhead_workspace_size(int64_t M, size_t* bytes);
@@ -291,8 +278,9 @@ DFLASH_API int32_t dflash_verify_accept(const float* logits, const int32_t* draf
  * exits.  Shapes whose scratch would exceed that (more than 1024 sequences,
  * or b*R*slices keys beyond the array) return DFLASH_EWORKSPACE.  The first
  * call on a device resolves the array's device address (cudaGetSymbolAddress
- * with that device current); make that first call before any stream
- * capture.  Each call clears the per-sequence counters it needs with
+ * with that device current) and keeps it for the life of the process; make
+ * that first call before any stream capture, and do not call it again on a
+ * device after cudaDeviceReset there (the kept address would be stale).  Each call clears the per-sequence counters it needs with
  * cudaMemsetAsync on the stream.  All calls share the one array, which keeps
  * the last call's contents, so calls that can overlap on the GPU (different
  * streams without ordering) race: serialise them.  No cudaMalloc, cudaFree
@@ -347,7 +335,7 @@ DFLASH_API int32_t dflash_verify_accept_sample(const float* logits, const int32_
  * K/V weights are read once and the separate K/V launch disappears; the
  * block is drafted against the grown context and len[] is advanced at the
  * end.  Arguments and errors are the union of the two calls'; ws is sized by
- * dflash_workspace_size(cfg, b, rows_per_seq).  Multi-kernel path only. */
+ * dflash_workspace_size(cfg, b, rows_per_seq). */
 DFLASH_API int32_t dflash_commit_draft_block(const dflash_weights* w, const dflash_kv* kv,
                                              const uint16_t* hid, int32_t rows_per_seq,
                                              const int32_t* n, const int32_t* last_tok,
@@ -371,6 +359,30 @@ DFLASH_API int32_t dflash_kv_commit(const dflash_weights* w, const dflash_kv* kv
                          const uint16_t* hid, int32_t rows_per_seq,
                          const int32_t* n, void* ws, size_t ws_bytes,
                          void* stream);
+
+/* Launch modes (dflash_set_launch_mode).
+ *  DFLASH_LAUNCH_STREAM_ORDER (the default): every kernel starts after the
+ *    previous work of its stream has finished.  Correct whatever else runs
+ *    on the GPU at the same time.
+ *  DFLASH_LAUNCH_EARLY: every kernel is launched as a programmatic dependent
+ *    of the previous kernel of its stream and lets its own dependents launch
+ *    early, so each kernel's weight copies start while the previous kernel
+ *    finishes (about 10 % shorter draft steps on a dedicated GPU).  Only for
+ *    callers that own the GPU and issue the library's calls from one stream:
+ *    on GB300 (driver 580), early-launched kernels gave wrong results, now
+ *    and then, while other kernels (the library's on another stream, or any
+ *    other work) ran on the same GPU. */
+#define DFLASH_LAUNCH_STREAM_ORDER 0
+#define DFLASH_LAUNCH_EARLY 1
+
+/* Sets the launch mode of every later call in this process (all devices,
+ * all threads).  A CUDA graph keeps the mode its kernels were captured with.
+ * DFLASH_EINVAL for an unknown mode.  No page describes this; it is a
+ * property of this library's kernels. */
+DFLASH_API int32_t dflash_set_launch_mode(int32_t mode);
+
+/* The current launch mode. */
+DFLASH_API int32_t dflash_get_launch_mode(void);
 
 /* Reads (and, when clear != 0, resets) the device status word of the current
  * device into *host_status.  Synchronises the device. */

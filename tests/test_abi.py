@@ -154,7 +154,13 @@ def test_weight_bits_checked_before_launch(lib):
     assert draft(W) == -1
     W, keep = _tiny_weights(api, c, 4, fc_bits=8)
     assert draft(W) == -1                                # mixed widths
-    W, keep = _tiny_weights(api, c, 4)
-    assert draft(W, lib.dflash_draft_block_fused) == -2  # single-kernel step is int8 only
-    W, keep = _tiny_weights(api, c, 8)
-    assert draft(W, lib.dflash_draft_block_fused) == -5
+
+
+def test_launch_mode_switch(lib):
+    from block_diffusion_speculative_draft_gb300 import api
+    assert lib.dflash_get_launch_mode() == api.LAUNCH_STREAM_ORDER  # the default
+    with api.launch_mode(api.LAUNCH_EARLY):
+        assert lib.dflash_get_launch_mode() == api.LAUNCH_EARLY
+    assert lib.dflash_get_launch_mode() == api.LAUNCH_STREAM_ORDER
+    assert lib.dflash_set_launch_mode(2) == -1 and lib.dflash_set_launch_mode(-1) == -1
+    assert lib.dflash_get_launch_mode() == api.LAUNCH_STREAM_ORDER

@@ -35,14 +35,14 @@ def _setup(cfg, rows_per_seq, extra_cap=64):
     return W, model, ctx, kv, ws, hids
 
 
-def _check_draft(cfg, W, model, kv, ws, hids, ctx, seqs=None, fused=False):
+def _check_draft(cfg, W, model, kv, ws, hids, ctx, seqs=None):
     b = cfg.b
     t0 = synth.tokens(cfg.seed, "t0", b, cfg.V)
     last = torch.from_numpy(t0).to(DEV)
     draft = torch.empty((b, cfg.B - 1), dtype=torch.int32, device=DEV)
     hidden = torch.empty((b, cfg.B - 1, cfg.H), dtype=torch.float32, device=DEV)
     logits = torch.empty((b, cfg.B - 1, cfg.V), dtype=torch.float32, device=DEV)
-    fn = api.dflash_draft_block_fused if fused else api.dflash_draft_block
+    fn = api.dflash_draft_block
     fn(model, kv, last, draft, ws, hidden=hidden, logits=logits)
     # without the optional outputs the final RMSNorm is folded into the last
     # GEMM (argmax only); its drafts must meet the same bar
@@ -87,12 +87,11 @@ def _check_cache(cfg, W, kv, hids, ctx, seqs):
             assert not kc[l, j, :, C:, :].any()  # nothing past the committed rows
 
 
-@pytest.mark.parametrize("fused", [False, True])
-def test_tiny_commit_and_draft(fused):
+def test_tiny_commit_and_draft():
     cfg = TINY
     W, model, ctx, kv, ws, hids = _setup(cfg, cfg.B)
     _check_cache(cfg, W, kv, hids, ctx, range(cfg.b))
-    _check_draft(cfg, W, model, kv, ws, hids, ctx, fused=fused)
+    _check_draft(cfg, W, model, kv, ws, hids, ctx)
 
 
 def test_tiny_long_context_multi_tile_splits():
@@ -171,12 +170,12 @@ def test_bad_token_flag():
     assert api.dflash_get_status() & api.DEV_BAD_TOKEN
 
 
-@pytest.mark.parametrize("b,lo,hi,fused", [(2, 20, 70, False), (4, 16, 90, False), (2, 20, 70, True)])
-def test_tiny_batched_ragged(b, lo, hi, fused):
+@pytest.mark.parametrize("b,lo,hi", [(2, 20, 70), (4, 16, 90)])
+def test_tiny_batched_ragged(b, lo, hi):
     """Ragged batches: b = 2 (32 block rows) and b = 4 (64 block rows) cover
     both launch shapes of the draft step; every sequence matches the oracle."""
     import dataclasses
     cfg = dataclasses.replace(TINY, b=b, ctx=(), ctx_range=(lo, hi), seed=1100 + b)
     W, model, ctx, kv, ws, hids = _setup(cfg, cfg.B)
     _check_cache(cfg, W, kv, hids, ctx, range(b))
-    _check_draft(cfg, W, model, kv, ws, hids, ctx, fused=fused)
+    _check_draft(cfg, W, model, kv, ws, hids, ctx)

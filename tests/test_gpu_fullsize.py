@@ -1,6 +1,7 @@
 """Whole-step GPU parity at the full workload sizes (Qwen3-4B-shaped,
-Qwen3-8B-shaped, 27B-class, batched 8 x Qwen3-8B-shaped with ragged
-contexts), in the launch configuration bench.py times, through the C ABI.
+Qwen3-8B-shaped, 27B-class at 64 / 2048 / 4096 context rows, batched 8 x
+Qwen3-8B-shaped with ragged contexts), in the launch configuration bench.py
+times (early-launch mode, one stream), through the C ABI.
 
 The oracle recomputes sampled sequences one by one (all of them when b = 1,
 two of eight for the batched workload).  Tolerances as in the tiny tests:
@@ -23,11 +24,18 @@ if gpu_available():
     from block_diffusion_speculative_draft_gb300 import api
     DEV = torch.device("cuda:0")
 
-CASES = [(configs.QWEN3_4B, [0]), (configs.QWEN3_8B, [0]), (configs.DENSE_27B, [0]),
-         (configs.BATCHED_8B, [1, 6])]
+CASES = ([(configs.QWEN3_4B, [0]), (configs.QWEN3_8B, [0])]
+         + [(configs.DENSE_27B.with_ctx((c,)), [0]) for c in configs.DENSE_27B_CTX_SWEEP]
+         + [(configs.BATCHED_8B, [1, 6])])
 
 
-@pytest.mark.parametrize("cfg,seqs", CASES, ids=[c.name for c, _ in CASES])
+@pytest.fixture(autouse=True)
+def _early_launch():
+    with api.launch_mode(api.LAUNCH_EARLY):
+        yield
+
+
+@pytest.mark.parametrize("cfg,seqs", CASES, ids=[f"{c.name}-ctx{c.ctx[0] if c.ctx else 'ragged'}" for c, _ in CASES])
 def test_fullsize_step(cfg, seqs):
     W = synth.drafter_weights(cfg)
     model = api.DeviceDrafter(cfg, W, DEV)
@@ -39,7 +47,7 @@ def test_fullsize_step(cfg, seqs):
     hids = commit_contexts(api, torch, cfg, model, kv, ws, ctx, rps, DEV)
     t0 = synth.tokens(cfg.seed, "t0", b, cfg.V)
     last = torch.from_numpy(t0).to(DEV)
-    paths = [api.dflash_draft_block] + ([api.dflash_draft_block_fused] if cfg.M <= 32 else [])
+    paths = [api.dflash_draft_block]
     outs = []
     for fn in paths:
         draft = torch.empty((b, cfg.B - 1), dtype=torch.int32, device=DEV)

@@ -5,10 +5,13 @@ Overlap must not change a single result: from identical states, running the
 groups side by side (free, or staggered so each draft runs beside the
 previous group's verify forward), eagerly or replayed from a CUDA graph,
 gives bit-identical drafts, accept outputs, logits, lengths and committed
-cache rows to running them one after another.  The stand-in's logits match
-the oracle's int4 linear within 1e-3 of max-abs (all rows for the tiny
-workload, sampled row ranges at full size), and the accept outputs equal
-the oracle's greedy rule on those logits.
+cache rows to running them one after another.  Every mode runs several
+times (a race shows up only in some runs), and every mode's committed K/V
+rows are also checked against the oracle's context path, so a mismatch
+says which mode is wrong.  The stand-in's logits match the oracle's int4
+linear within 1e-3 of max-abs (all rows for the tiny workload, sampled row
+ranges at full size), and the accept outputs equal the oracle's greedy rule
+on those logits.
 """
 import numpy as np
 import pytest
@@ -50,35 +53,75 @@ def _snapshot(cfg, gs):
 
 
 def _same(a, b):
-    for ga, gb in zip(a, b):
+    for gi, (ga, gb) in enumerate(zip(a, b)):
         for k in ("draft", "logits", "n", "corr", "emitted", "nxt", "len"):
-            assert np.array_equal(ga[k], gb[k]), k
+            assert np.array_equal(ga[k], gb[k]), (gi, k)
         for (ka, va), (kb, vb) in zip(ga["rows"], gb["rows"]):
-            assert np.array_equal(ka.view(np.uint16), kb.view(np.uint16))
-            assert np.array_equal(va.view(np.uint16), vb.view(np.uint16))
+            assert np.array_equal(ka.view(np.uint16), kb.view(np.uint16)), (gi, "K rows")
+            assert np.array_equal(va.view(np.uint16), vb.view(np.uint16)), (gi, "V rows")
 
 
-def _run_all_ways(cfg, model, standin, gs):
+REPS = 4  # runs of every mode
+
+
+def _oracle_rows(cfg, W, gs, snap):
+    """The oracle's K/V [L][rows][nkv][d] of each group's and sequence's
+    committed rows (the accept lengths of `snap`) at their positions."""
+    D = O.Drafter(cfg, W)
+    out = []
+    for g, sg in zip(gs, snap):
+        l0 = g.len0.cpu().numpy()
+        per = []
+        for j in range(cfg.b):
+            keep = O.commit_rows(int(sg["n"][j]), cfg.B)
+            c = O.context_rows(D, g.blk_host[j][:keep])
+            kv = [O.context_kv_layer(D, l, c, int(l0[j]) + np.arange(keep)) for l in range(cfg.L)]
+            per.append((int(l0[j]), keep, np.stack([k for k, _ in kv]), np.stack([v for _, v in kv])))
+        out.append(per)
+    D.drop()
+    return out
+
+
+def _committed_err(snap, expect):
+    """Max relative error of the committed rows [len0, len) of every group
+    and sequence against the oracle's."""
+    errs = []
+    for sg, per in zip(snap, expect):
+        for j, (l0, keep, k, v) in enumerate(per):
+            assert int(sg["len"][j]) == l0 + keep
+            gk, gv = sg["rows"][j]
+            errs.append(rel_err(gk[:, :, l0:, :].transpose(0, 2, 1, 3), k))
+            errs.append(rel_err(gv[:, :, l0:, :].transpose(0, 2, 1, 3), v))
+    return max(errs)
+
+
+def _run_all_ways(cfg, W, model, standin, gs):
     side = [torch.cuda.Stream(device=DEV) for _ in gs[1:]]
-    results = []
     WL.run_serial(api, torch, cfg, model, standin, gs, reset=True)
     torch.cuda.synchronize()
-    results.append(_snapshot(cfg, gs))
-    for stagger in (False, True):
-        WL.run_overlapped(api, torch, cfg, model, standin, gs, side, reset=True, stagger=stagger)
-        torch.cuda.synchronize()
-        results.append(_snapshot(cfg, gs))
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        WL.run_overlapped(api, torch, cfg, model, standin, gs, side, reset=True, stagger=True)
-    for _ in range(2):
-        g.replay()
-    torch.cuda.synchronize()
-    results.append(_snapshot(cfg, gs))
+    ref = _snapshot(cfg, gs)
+    expect = _oracle_rows(cfg, W, gs, ref)
+    assert _committed_err(ref, expect) <= 1e-2
+    modes = {
+        "serial": lambda: WL.run_serial(api, torch, cfg, model, standin, gs, reset=True),
+        "free": lambda: WL.run_overlapped(api, torch, cfg, model, standin, gs, side, reset=True),
+        "staggered": lambda: WL.run_overlapped(api, torch, cfg, model, standin, gs, side, reset=True,
+                                               stagger=True),
+    }
+    for name in list(modes):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            modes[name]()
+        modes["graph " + name] = g.replay
+    for name, fn in modes.items():
+        for r in range(REPS):
+            fn()
+            torch.cuda.synchronize()
+            snap = _snapshot(cfg, gs)
+            assert _committed_err(snap, expect) <= 1e-2, (name, r)
+            _same(ref, snap)
     assert api.dflash_get_status() == 0
-    for r in results[1:]:
-        _same(results[0], r)
-    return results[0]
+    return ref
 
 
 def _check_standin_and_accept(cfg, gs, snap, row_ranges):
@@ -99,10 +142,11 @@ def _check_standin_and_accept(cfg, gs, snap, row_ranges):
 
 def test_overlap_tiny():
     cfg = TINY
-    model = api.DeviceDrafter(cfg, synth.drafter_weights(cfg), DEV)
+    W = synth.drafter_weights(cfg)
+    model = api.DeviceDrafter(cfg, W, DEV)
     standin = WL.TargetStandIn(api, torch, cfg, DEV)
     gs = _groups(cfg, model, 3)
-    snap = _run_all_ways(cfg, model, standin, gs)
+    snap = _run_all_ways(cfg, W, model, standin, gs)
     _check_standin_and_accept(cfg, gs, snap, [(0, 0, cfg.V)])
     for g, s in zip(gs, snap):
         assert np.array_equal(s["len"], g.len0.cpu().numpy() + s["n"] + 1)
@@ -110,9 +154,10 @@ def test_overlap_tiny():
 
 def test_overlap_qwen3_4b_shape():
     cfg = QWEN3_4B
-    model = api.DeviceDrafter(cfg, synth.drafter_weights(cfg), DEV)
+    W = synth.drafter_weights(cfg)
+    model = api.DeviceDrafter(cfg, W, DEV)
     standin = WL.TargetStandIn(api, torch, cfg, DEV)
     gs = _groups(cfg, model, 2)
-    snap = _run_all_ways(cfg, model, standin, gs)
+    snap = _run_all_ways(cfg, W, model, standin, gs)
     last = len(WL.standin_chunks(cfg)) - 1
     _check_standin_and_accept(cfg, gs, snap, [(0, 0, 256), (7, 4000, 4256), (last, 4224, 4480)])

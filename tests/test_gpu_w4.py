@@ -82,15 +82,6 @@ def test_w4_tiny_commit_and_draft(cfg):
     _check_draft(cfg, W, model, kv, ws, hids, ctx)
 
 
-def test_w4_fused_single_kernel_is_unsupported():
-    W, model, ctx, kv, ws, hids = _w4_model(TINY, 16)
-    draft = torch.empty((TINY.b, TINY.B - 1), dtype=torch.int32, device=DEV)
-    last = torch.zeros(TINY.b, dtype=torch.int32, device=DEV)
-    with pytest.raises(api.DflashError) as e:
-        api.dflash_draft_block_fused(model, kv, last, draft, ws)
-    assert e.value.code == -2  # DFLASH_EUNSUPPORTED
-
-
 def test_w4_qwen3_4b_shape():
     cfg = QWEN3_4B
     W, model, ctx, kv, ws, hids = _w4_model(cfg, cfg.B, extra_cap=cfg.B)
