@@ -1,37 +1,46 @@
 // k_gemm_w8.cu — skinny W8A16 GEMM  Y[M x N] = s[N] . (X[M x K] Q[N x K]^T)
-// with fused epilogues, and the packer that produces its weight layout.
+// with fused epilogues, and the packers that produce its weight layouts.
 //
 // Method: int8 projection weights with one fp16 scale per output channel,
 // dequantised as q * s (mirror-sd README, "The Story", Phase 3; "How It Works":
-// int8 constants dequantised affinely).  At M = 16..32 activation rows the
-// contraction streams every weight byte once and does 2M flops per byte, far
-// below GB300's ridge, so the kernel is built to keep HBM busy:
-//  * swap-AB: weights are the 16-row MMA operand, activations the 8-column
-//    one, so the thin M side never pads a 128-row tile;
+// int8 constants dequantised affinely).  At M = 16..128 activation rows the
+// contraction streams every weight byte once and does 2M flops per byte, so
+// it has to run at HBM speed.  Two kernels read the same packed int8 tiles:
+//  * up to 32 rows, a warp-level MMA kernel (m16n8k16) — these launches are
+//    short and latency-bound, and two CTAs per SM in split-K clusters keep
+//    them short;
+//  * above 32 rows, a fifth-generation tensor-core kernel (tcgen05) with the
+//    accumulator in tensor memory — at 64 to 128 rows the contraction (128 to
+//    256 flop per weight byte) outruns what the warp-level MMA sustains.
+// Shared structure:
+//  * swap-AB: the 128-row weight tile is the MMA's M operand, the activation
+//    rows of a chunk its N operand;
 //  * a producer warp streams 16 KB packed weight tiles with 1-D bulk copies
-//    (the packer lays each tile out in MMA-fragment order, so a copy needs no
-//    tensor map and every consumer lane reads 16 contiguous bytes), and the
-//    matching 128-column activation slice with a 2-D TMA load (128-byte
-//    swizzle, rows past M zero-filled), into a 4-stage mbarrier ring (3
-//    stages for 64-row chunks, which keeps two CTAs per SM);
-//  * activation rows are taken 16, 32 or 64 at a time per CTA (one chunk
-//    per grid z index); larger M runs several chunks of the same tiles;
-//  * consumer warps turn biased int8 into fp16 exactly in registers and issue
-//    m16n8k16 MMAs with fp32 accumulation; the scale is applied after the
-//    K reduction;
+//    and the matching 128-column activation slice with a 2-D TMA load
+//    (128-byte swizzle, rows past M zero-filled) into an mbarrier ring;
+//  * biased int8 weights become fp16 exactly in registers (magic-number
+//    conversion); the scale is applied after the K reduction;
 //  * split-K over the CTAs of a thread-block cluster: each split keeps its
 //    fp32 partial tile in shared memory, and after a cluster barrier every
 //    CTA sums one slice of activation rows over all splits through
 //    distributed shared memory, in split order (deterministic), then runs the
 //    epilogue for that slice; no partial ever touches global memory;
-//  * programmatic dependent launch: the weight copies of the first stages are
-//    issued before griddepcontrol.wait, overlapping the previous kernel's tail.
-// The same kernel runs int4 weights (W4A16; a 4-bit drafter is the default of
-// mlx-dspark v0.0.3, release notes "Notes"): symmetric codes in [-7, 7] with
-// one fp16 scale per row and 128-column group, packed as 8448-byte tiles
-// (fragment-ordered nibbles + the tile's group scales).  A k-tile is one
-// group, so each stage's partial sums are scaled per row as they join the
-// accumulators, and the ring is deeper to keep as many bytes in flight.
+//  * programmatic dependent launch (when the library's launch mode allows
+//    it): the weight copies of the first stages are issued before
+//    griddepcontrol.wait, overlapping the previous kernel's tail.
+// The tensor-memory kernel: four converter warps turn each int8 weight row
+// into fp16 pairs (one row per thread) and store them to tensor memory
+// (tcgen05.st), double-buffered; one MMA warp issues tcgen05.mma kind::f16
+// with A from tensor memory and the activations (K-major, 128-byte swizzle)
+// through a shared-memory descriptor; tcgen05.commit releases ring stages
+// and A buffers when their MMAs have run; the accumulator is read back with
+// tcgen05.ld and the tensor memory freed before the reduction.
+// int4 weights (W4A16; a 4-bit drafter is the default of mlx-dspark v0.0.3,
+// release notes "Notes") run on the warp-level kernel: symmetric codes in
+// [-7, 7] with one fp16 scale per row and 128-column group, packed as
+// 8448-byte tiles (fragment-ordered nibbles + the tile's group scales).  A
+// k-tile is one group, so each stage's partial sums are scaled per row as
+// they join the accumulators.
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -43,6 +52,9 @@ namespace dfl {
 
 namespace {
 
+constexpr int kTStride = 132;  // epilogue tile row stride (floats)
+
+// ------------------------------------------- warp-level MMA kernel ----
 constexpr int kConsumerWarps = 4;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 
@@ -50,7 +62,7 @@ constexpr int kThreads = (kConsumerWarps + 1) * 32;
 // fp16 scales of the tile's 128-column group
 constexpr int kTile4Bytes = (int)kW4TileBytes;
 
-template <int MT, int BITS = 8>
+template <int MT, int BITS>
 struct Geo {
   static constexpr int MCH = MT * 8;          // activation rows per chunk
   // ring stages: int8 3 / 4 (3 keeps two 64-row CTAs per SM); int4 tiles are
@@ -59,11 +71,10 @@ struct Geo {
   static constexpr int NST = BITS == 8 ? (MT >= 8 ? 3 : 4) : (MT >= 8 ? 4 : (MT >= 4 ? 6 : 8));
   static constexpr int ABYTES = 2 * MCH * 128;  // two [MCH][64] fp16 halves
   static constexpr int WBYTES = BITS == 8 ? kTileBytes : kTile4Bytes;  // weight bytes per stage
-  static constexpr int WSLOT = (WBYTES + 1023) / 1024 * 1024;          // activations 1 KB aligned
+  static constexpr int WSLOT = (WBYTES + 1023) / 1024 * 1024;  // activations 1 KB aligned
   static constexpr int STAGE = WSLOT + ABYTES;
   static constexpr int TX = WBYTES + ABYTES;  // bytes a stage's copies deliver
-  static constexpr int TSTRIDE = 132;  // epilogue tile row stride (floats)
-  static constexpr int TBYTES = (MCH * TSTRIDE * 4 + 1023) / 1024 * 1024;
+  static constexpr int TBYTES = (MCH * kTStride * 4 + 1023) / 1024 * 1024;
   static_assert(2 * TBYTES <= NST * STAGE, "epilogue tiles must fit in the ring");
   // side data after the barriers: row scales, gamma, next gamma, per-row
   // positions, per-row norm factors
@@ -87,11 +98,11 @@ __device__ __forceinline__ int logical_row(int prow, int layout, int N) {
 // the per-head gamma and pos[t] the position of row t (-1: not written), all
 // staged in shared memory before the main loop so that no global load sits on
 // the epilogue's critical path except the residual read, issued in batches.
-template <int MT>
+template <int MCH>
 __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float* gam, const int* pos,
                          const float* gn, const float* rr, __half* kout, __half* vout, int nt, int z, int tlo,
                          int thi, int warp, int lane) {
-  using G = Geo<MT>;
+  constexpr int TS = kTStride;
   const int tid = threadIdx.x;
   const int nthr = blockDim.x;
   const int ntok = thi - tlo;
@@ -99,7 +110,7 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
   if (a.ss_in) {  // deferred RMSNorm of the input rows: one factor per row
     for (int i = tid; i < ntok * kTile; i += nthr) {
       const int tok = tlo + (i >> 7);
-      T[tok * G::TSTRIDE + (i & 127)] *= rr[tok];
+      T[tok * TS + (i & 127)] *= rr[tok];
     }
     __syncthreads();
   }
@@ -113,7 +124,7 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
         xo[u] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (it < items && a.epi == EPI_RESID_F32) {
           const int tok = tlo + it / (kTile / 4), r = 4 * (it % (kTile / 4));
-          const int m = z * G::MCH + tok;
+          const int m = z * MCH + tok;
           if (m < a.M) {
             const int n = logical_row(prow0 + r, a.layout, a.N);
             xo[u] = *reinterpret_cast<const float4*>(a.out_f32 + (size_t)m * a.ldo + (n - a.row0));
@@ -129,10 +140,10 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
         int m = a.M;
         if (it < items) {
           const int tok = tlo + it / (kTile / 4), r = 4 * (it % (kTile / 4));
-          m = z * G::MCH + tok;
+          m = z * MCH + tok;
           if (m < a.M) {
             const int n = logical_row(prow0 + r, a.layout, a.N);
-            const float* t = T + tok * G::TSTRIDE + r;
+            const float* t = T + tok * TS + r;
             float4 v = make_float4(t[0] * sc[r] + xo[u].x, t[1] * sc[r + 1] + xo[u].y,
                                    t[2] * sc[r + 2] + xo[u].z, t[3] * sc[r + 3] + xo[u].w);
             if (a.out_f32) *reinterpret_cast<float4*>(a.out_f32 + (size_t)m * a.ldo + (n - a.row0)) = v;
@@ -173,9 +184,9 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
     const int items = ntok * 16;  // groups of 4 output columns
     for (int it = tid; it < items; it += nthr) {
       const int tok = tlo + it / 16, r = 4 * (it % 16);
-      const int m = z * G::MCH + tok;
+      const int m = z * MCH + tok;
       if (m >= a.M) continue;
-      const float* t = T + tok * G::TSTRIDE;
+      const float* t = T + tok * TS;
       float g[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -194,8 +205,9 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
   // per-head epilogues: one warp per activation row, lane holds rows lane+32i
   const int qd = a.nq * a.d, kd = a.nkv * a.d;
   const int kind = prow0 < qd ? 0 : (prow0 < qd + kd ? 1 : 2);  // q, k, v
-  for (int tok = tlo + warp; tok < thi; tok += kConsumerWarps + 1) {
-    const int m = z * G::MCH + tok;
+  const int nwarps = blockDim.x >> 5;
+  for (int tok = tlo + warp; tok < thi; tok += nwarps) {
+    const int m = z * MCH + tok;
     const int p = pos[tok];
     if (m >= a.M || p < 0) continue;
     const bool crow = a.epi == EPI_QKV && a.c_nacc && m >= a.mc0;  // folded commit row
@@ -205,7 +217,7 @@ __device__ void epilogue(const W8Args& a, float* T, const float* sc, const float
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       int r = lane + 32 * i;
-      v[i] = T[tok * G::TSTRIDE + r] * sc[r];
+      v[i] = T[tok * TS + r] * sc[r];
     }
     if (kind != 2) {
       if (a.d == 128) {
@@ -284,9 +296,59 @@ __device__ __forceinline__ void biased_u4x8_to_half2x4(uint32_t w, uint32_t (&r)
   r[3] = *reinterpret_cast<uint32_t*>(&d);
 }
 
+
+// Split-K reduction across the thread-block cluster and the epilogue, shared
+// by the int8 (tensor-memory) and int4 kernels.  On entry every CTA of the
+// cluster has its own fp32 partial tile P[tok][kTStride] at the start of its
+// (idle) stage ring; TBYTES is that tile's size rounded to 1 KB.
+template <int MCH, int TBYTES>
+__device__ __forceinline__ void split_reduce_epilogue(const W8Args& a, uint8_t* smem, const float* s_sc,
+                                                      const float* s_gam, const int* s_pos, const float* s_gn,
+                                                      const float* s_rr, __half* kout, __half* vout, int nt, int z,
+                                                      int sp, int warp, int lane) {
+  float* P = reinterpret_cast<float*>(smem);
+  float* T = reinterpret_cast<float*>(smem + TBYTES);
+  if (a.splits == 1) {
+    __syncthreads();
+    epilogue<MCH>(a, P, s_sc, s_gam, s_pos, s_gn, s_rr, kout, vout, nt, z, 0, MCH, warp, lane);
+    // the next kernel reads these outputs with TMA (async proxy)
+    fence_proxy_async_global();
+    return;
+  }
+  // ---- split-K reduction across the cluster through distributed smem ----
+  cluster_sync();
+  const int S = a.splits;
+  const int tlo = (sp * MCH) / S, thi = ((sp + 1) * MCH) / S;
+  const int items = (thi - tlo) * (kTile / 4);  // float4 items of this slice
+  const uint32_t pbase = smem_u32(P);
+  for (int it = threadIdx.x; it < items; it += blockDim.x) {
+    const int tok = tlo + it / (kTile / 4), c4 = it % (kTile / 4);
+    const uint32_t off = pbase + (uint32_t)(tok * kTStride + 4 * c4) * 4u;
+    float4 v[8];
+    float4 accv = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < S; s0 += 8) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (s0 + q < S) v[q] = ld_dsmem_f4(dsmem_addr(off, (uint32_t)(s0 + q)));
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (s0 + q < S) {
+          accv.x += v[q].x;
+          accv.y += v[q].y;
+          accv.z += v[q].z;
+          accv.w += v[q].w;
+        }
+    }
+    *reinterpret_cast<float4*>(T + tok * kTStride + 4 * c4) = accv;
+  }
+  cluster_sync();  // every peer has finished reading this CTA's partial
+  epilogue<MCH>(a, T, s_sc, s_gam, s_pos, s_gn, s_rr, kout, vout, nt, z, tlo, thi, warp, lane);
+  fence_proxy_async_global();  // the next kernel reads these outputs with TMA
+}
+
 template <int MT, int BITS>
-__global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_constant__ CUtensorMap xmap,
-                                                               const W8Args a) {
+__global__ void __launch_bounds__(kThreads, 1) wmma_gemm_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                 const W8Args a) {
   using G = Geo<MT, BITS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -375,6 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
       const int r = threadIdx.x;  // 0..127
       const int prow = a.row0 + nt * kTile + r;
       // int4 weights carry their group scales in the tile (applied per stage)
+      // int4 tiles carry their group scales, applied per stage
       s_sc[r] = BITS == 8 ? __half2float(wsc[logical_row(prow, a.layout, a.N)]) : 1.f;
       if (a.epi == EPI_QKV || a.epi == EPI_KVCOMMIT) {
         const int qd = a.nq * a.d;
@@ -437,15 +500,24 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
       if (!mbar_wait(&full[slot], (i / G::NST) & 1, a.status)) break;
       const uint32_t abase = smem_u32(smem + slot * G::STAGE + G::WSLOT);
       if constexpr (BITS == 8) {
-        const uint8_t* wl = smem + slot * G::STAGE + (warp * 8 * 32 + lane) * 16;
+        // the int8 tile is [row 128][128 bytes], 16-byte chunks swizzled by
+        // row, each chunk holding lane t's fragment bytes (columns 2t, 2t+1,
+        // 2t+8, 2t+9 of the 16-column group) at bytes 4t..4t+3.  Read as
+        // 8x8 matrices of 16-bit pairs, ldmatrix hands lane (g, t) exactly
+        // word t of row g's chunk: one ldmatrix.x4 per k-step loads the
+        // words of rows g, g+8, g+16, g+24 of this warp's 32 rows
+        // (conflict-free: the row swizzle spreads the 8 rows of a matrix).
+        const uint32_t wst = smem_u32(smem + slot * G::STAGE);
+        const int wr = warp * 32 + lane;  // row this lane addresses (wr % 8 == lane % 8)
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          uint4 wq = *reinterpret_cast<const uint4*>(wl + ks * 32 * 16);
           uint32_t af[2][4];
-          biased_u8x4_to_half2x2(wq.x, af[0][0], af[0][1]);
-          biased_u8x4_to_half2x2(wq.y, af[0][2], af[0][3]);
-          biased_u8x4_to_half2x2(wq.z, af[1][0], af[1][1]);
-          biased_u8x4_to_half2x2(wq.w, af[1][2], af[1][3]);
+          uint32_t w00, w01, w10, w11;
+          ldsm_x4(wst + wr * 128 + ((ks ^ (lane & 7)) << 4), w00, w01, w10, w11);
+          biased_u8x4_to_half2x2(w00, af[0][0], af[0][2]);
+          biased_u8x4_to_half2x2(w01, af[0][1], af[0][3]);
+          biased_u8x4_to_half2x2(w10, af[1][0], af[1][2]);
+          biased_u8x4_to_half2x2(w11, af[1][1], af[1][3]);
           const uint32_t hbase = abase + (ks >> 2) * (G::MCH * 128);
           const int ch = ((ks & 3) << 1) + ch_hi;
 #pragma unroll
@@ -508,10 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
   }
   __syncthreads();  // all stages consumed: the ring can be reused as scratch
 
-  // own partial tile P[tok][TSTRIDE] at the ring's start; the reduced slice
+  // own partial tile P[tok][kTStride] at the ring's start; the reduced slice
   // goes to a second buffer so peers can keep reading P meanwhile
   float* P = reinterpret_cast<float*>(smem);
-  float* T = reinterpret_cast<float*>(smem + G::TBYTES);
   const int g = lane >> 2, t = lane & 3;
   if (warp < kConsumerWarps) {
 #pragma unroll
@@ -522,45 +593,332 @@ __global__ void __launch_bounds__(kThreads, 1) w8_gemm_kernel(const __grid_const
         for (int e = 0; e < 4; ++e) {
           int r = warp * 32 + mg * 16 + g + ((e >> 1) << 3);
           int tok = j * 8 + 2 * t + (e & 1);
-          P[tok * G::TSTRIDE + r] = acc[mg][j][e];
+          P[tok * kTStride + r] = acc[mg][j][e];
         }
   }
-  if (a.splits == 1) {
-    __syncthreads();
-    epilogue<MT>(a, P, s_sc, s_gam, s_pos, s_gn, s_rr, kout, vout, nt, z, 0, G::MCH, warp, lane);
-    // the next kernel reads these outputs with TMA (async proxy)
-    fence_proxy_async_global();
-    return;
+  split_reduce_epilogue<G::MCH, G::TBYTES>(a, smem, s_sc, s_gam, s_pos, s_gn, s_rr, kout, vout, nt, z, sp, warp,
+                                           lane);
+}
+
+// ---------------------------------------------------- int8, tcgen05 ----
+constexpr int kTcThreads = 6 * 32;  // 4 converter warps, 1 producer, 1 MMA warp
+constexpr int kTcProducer = 4;
+constexpr int kTcMma = 5;
+constexpr uint32_t kTmemCols = 256;  // accumulator [0, 128), A buffers [128, 192), [192, 256)
+constexpr uint32_t kTmemA = 128;
+
+template <int MT>
+struct TcGeo {
+  static constexpr int MCH = MT * 8;  // activation rows per chunk = MMA N
+  static_assert(MCH % 16 == 0 && MCH <= 128, "MMA N: a multiple of 16 up to 128");
+  static constexpr int NST = MT == 8 ? 3 : 4;  // ring stages
+  static constexpr int ABYTES = 2 * MCH * 128;  // two [MCH][64] fp16 halves
+  static constexpr int WBYTES = kTileBytes;      // int8 tile
+  static constexpr int STAGE = WBYTES + ABYTES;  // both 1 KB multiples
+  static constexpr int TX = WBYTES + ABYTES;
+  static constexpr int TBYTES = (MCH * kTStride * 4 + 1023) / 1024 * 1024;
+  static_assert(2 * TBYTES <= NST * STAGE, "epilogue tiles must fit in the ring");
+  static constexpr int NBAR = 2 * NST + 5;  // full, empty, afull[2], afree[2], dfull
+  static constexpr int SIDE = 128 * 4 + 128 * 4 + 128 * 4 + MCH * 4 + MCH * 4;
+  static constexpr size_t SMEM = 1024 + NST * (size_t)STAGE + NBAR * 8 + 16 + SIDE;
+  // two CTAs per SM up to 64 rows (tensor memory: 2 x 256 of 512 columns)
+  static_assert(MT == 16 || SMEM <= 112 * 1024, "two CTAs per SM");
+  static_assert(SMEM <= 227 * 1024, "one CTA per SM");
+};
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Named barrier over the converter warps and the MMA warp (160 threads).
+__device__ __forceinline__ void tc_bar() { asm volatile("bar.sync 1, 160;" ::: "memory"); }
+
+// 32 consecutive tensor-memory columns of this warp's 32 lanes (thread t:
+// lane base + t) from / to registers.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]),
+      "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]),
+      "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+// Instruction descriptor of tcgen05.mma kind::f16: fp32 accumulator, fp16 A
+// and B, both K-major, M = 128, N = n (PTX ISA, tcgen05 instruction
+// descriptor: D format bits 4-5, A / B formats bits 7-9 / 10-12, majors bits
+// 15 / 16, N >> 3 bits 17-22, M >> 4 bits 24-28).
+__host__ __device__ constexpr uint32_t tc_idesc_f16(int n) {
+  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+// Shared-memory matrix descriptor of a K-major operand in the 128-byte
+// swizzled layout (8 rows x 128 bytes per swizzle atom, atoms 1024 bytes
+// apart): start address >> 4 in bits 0-13, leading offset (unused here) 1,
+// stride offset 1024 >> 4 in bits 32-45, descriptor version 1 in bits 46-47,
+// swizzle mode 2 (128 B) in bits 61-63.
+__device__ __forceinline__ uint64_t tc_sdesc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+         ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                              uint32_t accumulate) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.u32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrives on `bar` once every tcgen05 operation this thread issued before it
+// has completed.
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
+template <int MT>
+__global__ void __launch_bounds__(kTcThreads, 1) w8_gemm_kernel(const __grid_constant__ CUtensorMap xmap,
+                                                                 const W8Args a) {
+  using G = TcGeo<MT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::NST * G::STAGE);
+  uint64_t* empty = full + G::NST;  // 4 converter warps + 1 MMA commit
+  uint64_t* afull = empty + G::NST;  // [2]: A buffer stored (4 converter warps)
+  uint64_t* afree = afull + 2;       // [2]: A buffer's MMAs done (commit)
+  uint64_t* dfull = afree + 2;       // accumulator complete (commit)
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(dfull + 1);
+  float* s_sc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s_tmem) + 16);  // [128]
+  float* s_gam = s_sc + 128;                                                          // [128]
+  float* s_gn = s_gam + 128;                                                          // [128]
+  int* s_pos = reinterpret_cast<int*>(s_gn + 128);                                    // [MCH]
+  float* s_rr = reinterpret_cast<float*>(s_pos + G::MCH);                             // [MCH]
+
+  const int sp = blockIdx.y, z = blockIdx.z;
+  int nt = blockIdx.x;
+  const uint8_t* wq = a.q;
+  const __half* wsc = a.s;
+  __half* kout = a.kout;
+  __half* vout = a.vout;
+  const float* gk = a.gk;
+  if (a.nl > 0) {
+    const int li = nt / a.ntl;
+    nt -= li * a.ntl;
+    wq = a.lq[li];
+    wsc = a.ls[li];
+    kout = a.lk[li];
+    vout = a.lv[li];
+    gk = a.lgk[li];
   }
-  // ---- split-K reduction across the cluster through distributed smem ----
-  cluster_sync();
-  const int S = a.splits;
-  const int tlo = (sp * G::MCH) / S, thi = ((sp + 1) * G::MCH) / S;
-  const int items = (thi - tlo) * (kTile / 4);  // float4 items of this slice
-  const uint32_t pbase = smem_u32(P);
-  for (int it = threadIdx.x; it < items; it += blockDim.x) {
-    const int tok = tlo + it / (kTile / 4), c4 = it % (kTile / 4);
-    const uint32_t off = pbase + (uint32_t)(tok * G::TSTRIDE + 4 * c4) * 4u;
-    float4 v[8];
-    float4 accv = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s0 = 0; s0 < S; s0 += 8) {
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (s0 + q < S) v[q] = ld_dsmem_f4(dsmem_addr(off, (uint32_t)(s0 + q)));
-#pragma unroll
-      for (int q = 0; q < 8; ++q)
-        if (s0 + q < S) {
-          accv.x += v[q].x;
-          accv.y += v[q].y;
-          accv.z += v[q].z;
-          accv.w += v[q].w;
-        }
+  const int KT = a.K / kTile;
+  const int kt0 = (int)(((long long)sp * KT) / a.splits);
+  const int kt1 = (int)(((long long)(sp + 1) * KT) / a.splits);
+  const int nk = kt1 - kt0;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < G::NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 5);
     }
-    *reinterpret_cast<float4*>(T + tok * G::TSTRIDE + 4 * c4) = accv;
+    for (int j = 0; j < 2; ++j) {
+      mbar_init(&afull[j], 4);
+      mbar_init(&afree[j], 1);
+    }
+    mbar_init(dfull, 1);
+    fence_mbar_init();
   }
-  cluster_sync();  // every peer has finished reading this CTA's partial
-  epilogue<MT>(a, T, s_sc, s_gam, s_pos, s_gn, s_rr, kout, vout, nt, z, tlo, thi, warp, lane);
-  fence_proxy_async_global();  // the next kernel reads these outputs with TMA
+  __syncthreads();
+
+  if (warp == kTcProducer) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&xmap);
+      const uint8_t* wsrc = wq + ((size_t)((a.row0 >> 7) + nt) * KT + kt0) * G::WBYTES;
+      const uint64_t pol = policy_evict_first();
+      const int pre = nk < G::NST ? nk : G::NST;
+      for (int i = 0; i < pre; ++i) {
+        mbar_arrive_expect_tx(&full[i], G::TX);
+        bulk_g2s_hint(smem + i * G::STAGE, wsrc + (size_t)i * G::WBYTES, G::WBYTES, &full[i], pol);
+      }
+      pdl_wait();
+      // the activations were written by the previous kernel with generic
+      // stores; order this thread's tensor (async-proxy) reads after them
+      fence_proxy_async_global();
+      for (int i = 0; i < pre; ++i) {
+        uint8_t* sa = smem + i * G::STAGE + G::WBYTES;
+        tma_load_2d(sa, &xmap, (kt0 + i) * kTile, z * G::MCH, &full[i]);
+        tma_load_2d(sa + G::MCH * 128, &xmap, (kt0 + i) * kTile + 64, z * G::MCH, &full[i]);
+      }
+      for (int i = pre; i < nk; ++i) {
+        const int slot = i % G::NST;
+        if (!mbar_wait(&empty[slot], ((i / G::NST) - 1) & 1, a.status)) break;
+        mbar_arrive_expect_tx(&full[slot], G::TX);
+        uint8_t* st = smem + slot * G::STAGE;
+        bulk_g2s_hint(st, wsrc + (size_t)i * G::WBYTES, G::WBYTES, &full[slot], pol);
+        tma_load_2d(st + G::WBYTES, &xmap, (kt0 + i) * kTile, z * G::MCH, &full[slot]);
+        tma_load_2d(st + G::WBYTES + G::MCH * 128, &xmap, (kt0 + i) * kTile + 64, z * G::MCH, &full[slot]);
+      }
+    }
+    pdl_trigger();
+  } else {
+    // ------------- converter warps 0..3 and the MMA warp -------------
+    if (warp < 4) {  // weights-side data first (independent of the preceding kernel)
+      const int r = threadIdx.x;  // 0..127
+      const int prow = a.row0 + nt * kTile + r;
+      s_sc[r] = __half2float(wsc[logical_row(prow, a.layout, a.N)]);
+      if (a.epi == EPI_QKV || a.epi == EPI_KVCOMMIT) {
+        const int qd = a.nq * a.d;
+        const float* gsrc = (a.row0 + nt * kTile) < qd ? a.gq : gk;
+        s_gam[r] = (gsrc && r < a.d) ? gsrc[r] : 1.f;
+      }
+      if (a.xg_out || a.hb_out) s_gn[r] = a.g_next[logical_row(prow, a.layout, a.N) - a.row0];
+    }
+    if (warp == 0) tmem_alloc(s_tmem, kTmemCols);
+    tc_fence_before();
+    tc_bar();
+    tc_fence_after();
+    const uint32_t tmem = *s_tmem;
+    pdl_wait();
+    if (warp < 4) {
+      const int rows = G::MCH < 128 ? G::MCH : 128;
+      if (a.ss_in && threadIdx.x < rows) {
+        // deferred RMSNorm factor of each activation row (fixed summation order)
+        const int m = z * G::MCH + threadIdx.x;
+        float rf = 0.f;
+        if (m < a.M) {
+          float sum = 0.f;
+          const float* row = a.ss_in + (size_t)m * a.nss_in;
+          if ((a.nss_in & 3) == 0 && a.nss_in <= 64) {
+            float4 v[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              if (4 * q < a.nss_in) v[q] = reinterpret_cast<const float4*>(row)[q];
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              if (4 * q < a.nss_in) sum += ((v[q].x + v[q].y) + (v[q].z + v[q].w));
+          } else {
+            for (int i = 0; i < a.nss_in; ++i) sum += row[i];
+          }
+          rf = rsqrtf(sum / a.K + a.eps);
+        }
+        s_rr[threadIdx.x] = rf;
+      }
+      if ((a.epi == EPI_QKV || a.epi == EPI_KVCOMMIT) && threadIdx.x < rows) {
+        // position of each activation row of this chunk, -1 when not written
+        const int t = threadIdx.x, m = z * G::MCH + t;
+        int p = -1;
+        if (m < a.M) {
+          if (a.epi == EPI_KVCOMMIT) {
+            const int seq = m / a.rows_per_seq, slot = m - seq * a.rows_per_seq;
+            const int L0 = a.len[seq];
+            p = slot < commit_count(L0, a.nacc[seq], a.rows_per_seq, a.cap) ? L0 + slot : -1;
+          } else if (a.c_nacc && m >= a.mc0) {  // a context row of the folded commit
+            const int mc = m - a.mc0, seq = mc / a.c_rps, slot = mc - seq * a.c_rps;
+            const int L0 = a.len[seq];
+            p = slot < commit_count(L0, a.c_nacc[seq], a.c_rps, a.cap) ? L0 + slot : -1;
+          } else {  // a block row: after the context (grown by the folded commit)
+            const int seq = m / a.rows_per_seq, slot = m - seq * a.rows_per_seq;
+            const int L0 = a.len[seq];
+            int base = L0 < 0 ? 0 : L0;
+            if (a.c_nacc) base += commit_count(L0, a.c_nacc[seq], a.c_rps, a.cap);
+            p = base + slot;
+          }
+        }
+        s_pos[t] = p;
+      }
+      // ---- converter: weight row r of each stage -> fp16 pairs in tensor memory
+      const int r = warp * 32 + lane;
+      const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+      for (int i = 0; i < nk; ++i) {
+        const int slot = i % G::NST, ab = i & 1;
+        if (!mbar_wait(&full[slot], (i / G::NST) & 1, a.status)) break;
+        if (i >= 2 && !mbar_wait(&afree[ab], ((i >> 1) - 1) & 1, a.status)) break;
+        const uint8_t* wrow = smem + slot * G::STAGE + r * 128;
+        const uint32_t ta = tmem + lane_base + kTmemA + 64 * ab;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t words[32];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int cc = 4 * h + c;  // logical 16-column group
+            // chunk word t holds columns (2t, 2t+1, 2t+8, 2t+9): fp16 pairs t and t + 4
+            const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((cc ^ (r & 7)) << 4));
+            biased_u8x4_to_half2x2(v.x, words[8 * c + 0], words[8 * c + 4]);
+            biased_u8x4_to_half2x2(v.y, words[8 * c + 1], words[8 * c + 5]);
+            biased_u8x4_to_half2x2(v.z, words[8 * c + 2], words[8 * c + 6]);
+            biased_u8x4_to_half2x2(v.w, words[8 * c + 3], words[8 * c + 7]);
+          }
+          tmem_st32(ta + 32 * h, words);
+        }
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&empty[slot]);
+          mbar_arrive(&afull[ab]);
+        }
+      }
+      pdl_trigger();
+      // ---- accumulator -> P[tok][kTStride] (this thread: weight row r)
+      mbar_wait(dfull, 0, a.status);
+      tc_fence_after();
+      float* P = reinterpret_cast<float*>(smem);
+      const uint32_t td = tmem + lane_base;
+#pragma unroll
+      for (int c0 = 0; c0 < G::MCH; c0 += 16) {
+        uint32_t v[16];
+        tmem_ld16(td + c0, v);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int j = 0; j < 16; ++j) P[(c0 + j) * kTStride + r] = __uint_as_float(v[j]);
+      }
+    } else if (warp == kTcMma && lane == 0) {
+      // ---------------- MMA issuer ----------------
+      constexpr uint32_t idesc = tc_idesc_f16(G::MCH);
+      for (int i = 0; i < nk; ++i) {
+        const int slot = i % G::NST, ab = i & 1;
+        if (!mbar_wait(&afull[ab], (i >> 1) & 1, a.status)) break;
+        if (!mbar_wait(&full[slot], (i / G::NST) & 1, a.status)) break;
+        tc_fence_after();
+        const uint32_t act = smem_u32(smem + slot * G::STAGE + G::WBYTES);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t bdesc = tc_sdesc_sw128(act + (ks >> 2) * (G::MCH * 128) + (ks & 3) * 32);
+          tc_mma_f16_ta(tmem, tmem + kTmemA + 64 * ab + 8 * ks, bdesc, idesc, (i | ks) != 0);
+        }
+        tc_commit(&afree[ab]);
+        tc_commit(&empty[slot]);
+      }
+      tc_commit(dfull);
+    }
+  }
+  // the accumulator has been read (or abandoned after a timeout): free the
+  // tensor memory before the reduction and epilogue
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(*s_tmem, kTmemCols);
+  }
+  split_reduce_epilogue<G::MCH, G::TBYTES>(a, smem, s_sc, s_gam, s_pos, s_gn, s_rr, kout, vout, nt, z, sp, warp,
+                                           lane);
 }
 
 // ------------------------------------------------------------- packing ----
@@ -592,50 +950,44 @@ __global__ void pack_scale_kernel(const void* w, int64_t N, int64_t K, __half* s
   if (lane == 0) s[row] = __float2half_rn(m / 127.0f);
 }
 
-// one thread per 16-byte lane chunk of the packed layout:
-// tile (nt, kt) -> [warp 4][kstep 8][lane 32][frag(2w) 8 B | frag(2w+1) 8 B]
+// int8 tiles: tile (nt, kt) is 16 KB of [packed row 128][128 bytes]; the
+// 16 columns of group g (columns 16 g .. 16 g + 15 of the tile) of row r
+// sit in the 16-byte chunk at r * 128 + (g xor (r mod 8)) * 16, and inside
+// a chunk bytes 4t .. 4t + 3 hold columns 2t, 2t + 1, 2t + 8, 2t + 9 (t < 4),
+// stored as q + 128.  The tensor-memory kernel reads whole chunks (one row
+// per thread), the warp-level kernel one 4-byte fragment word per lane; the
+// row swizzle keeps both conflict-free.  One thread per chunk.
 template <typename T>
 __global__ void pack_q_kernel(const void* w, int64_t N, int64_t K, int layout, const __half* s, uint8_t* q) {
-  int64_t chunk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  int64_t nchunks = N * K / 16;
+  const int64_t chunk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t nchunks = N * K / 16;
   if (chunk >= nchunks) return;
   const int64_t KT = K / kTile;
-  int64_t tile = chunk >> 10;
-  int within = (int)(chunk & 1023);
-  int wq = within >> 8, ks = (within >> 5) & 7, ln = within & 31;
-  int64_t nt = tile / KT, kt = tile - nt * KT;
-  int g = ln >> 2, t = ln & 3;
-  uint32_t out[4];
-#pragma unroll
-  for (int f = 0; f < 2; ++f) {
-    int mg = 2 * wq + f;
-    uint32_t word[2] = {0u, 0u};
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      // byte order of one m16k16 fragment for lane (g, t)
-      int r = g + ((e >> 1) & 1) * 8;
-      int c = 2 * t + (e & 1) + ((e >> 2) & 1) * 8;
-      int64_t prow = nt * kTile + mg * 16 + r;
-      int64_t lrow = prow;
-      if (layout == 1) {
-        int64_t tl = prow >> 7, rr = prow & 127;
-        lrow = rr < 64 ? tl * 64 + rr : (N >> 1) + tl * 64 + (rr - 64);
-      }
-      int64_t col = kt * kTile + ks * 16 + c;
-      float sc = __half2float(s[lrow]);
-      int qv = 0;
-      if (sc != 0.f) {
-        float r_ = rintf(ld_w<T>(w, lrow * K + col) / sc);
-        r_ = fminf(fmaxf(r_, -127.f), 127.f);
-        qv = (int)r_;
-      }
-      uint32_t byte = (uint32_t)((qv + 128) & 0xFF);
-      word[e >> 2] |= byte << (8 * (e & 3));
-    }
-    out[2 * f] = word[0];
-    out[2 * f + 1] = word[1];
+  const int64_t tile = chunk >> 10;  // 1024 chunks of 16 bytes per tile
+  const int within = (int)(chunk & 1023);
+  const int r = within >> 3, cs = within & 7;  // row, stored chunk slot
+  const int c16 = cs ^ (r & 7);                // logical 16-column group of that slot
+  const int64_t nt = tile / KT, kt = tile - nt * KT;
+  const int64_t prow = nt * kTile + r;
+  int64_t lrow = prow;
+  if (layout == 1) {
+    const int64_t tl = prow >> 7, rr = prow & 127;
+    lrow = rr < 64 ? tl * 64 + rr : (N >> 1) + tl * 64 + (rr - 64);
   }
-  reinterpret_cast<uint4*>(q)[chunk] = make_uint4(out[0], out[1], out[2], out[3]);
+  const float sc = __half2float(s[lrow]);
+  uint32_t word[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    int qv = 0;
+    if (sc != 0.f) {
+      const int col = 2 * (e >> 2) + (e & 1) + ((e >> 1) & 1) * 8;  // column of chunk byte e
+      float r_ = rintf(ld_w<T>(w, lrow * K + kt * kTile + c16 * 16 + col) / sc);
+      r_ = fminf(fmaxf(r_, -127.f), 127.f);
+      qv = (int)r_;
+    }
+    word[e >> 2] |= (uint32_t)((qv + 128) & 0xFF) << (8 * (e & 3));  // byte e of the chunk
+  }
+  reinterpret_cast<uint4*>(q)[chunk] = make_uint4(word[0], word[1], word[2], word[3]);
 }
 
 // int4 group scales: s[n][g] = fp16(absmax of row n over columns
@@ -715,13 +1067,21 @@ int w8_pick_splits(int units, int KT) {
   return s;
 }
 
-static int pick_mt(int M) { return M <= 16 ? 2 : (M <= 32 ? 4 : 8); }
+// Activation rows per CTA: up to 32 rows the warp-level kernel (two CTAs per
+// SM in split-K clusters keep these latency-bound launches short); above 32
+// the tensor-memory kernel (64 or 128 rows per CTA: the contraction is then
+// heavy enough for the legacy MMA to limit the streaming rate).  int4 always
+// runs on the warp-level kernel.
+static int pick_mt(int M, bool w4) {
+  if (w4) return M <= 16 ? 2 : (M <= 32 ? 4 : 8);
+  return M <= 16 ? 2 : (M <= 32 ? 4 : (M <= 64 ? 8 : 16));
+}
 
 // How many clusters of (1, s, 1) CTAs can be resident at once: clusters are
 // placed within one GPC, so sizes that do not divide a GPC's CTA slots leave
 // slots unused and a grid that looked like one wave may need two.  Cached per
 // (device, kernel, s).
-static int max_active_clusters(const void* fn, size_t smem, int s) {
+static int max_active_clusters(const void* fn, int threads, size_t smem, int s) {
   int dev = 0;
   cudaGetDevice(&dev);
   const auto key = std::make_tuple(dev, fn, s);
@@ -734,7 +1094,7 @@ static int max_active_clusters(const void* fn, size_t smem, int s) {
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(1, s, 1);
-  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -755,31 +1115,42 @@ static int max_active_clusters(const void* fn, size_t smem, int s) {
 
 cudaError_t w8_gemm(const W8Args& a0, const __half* x, cudaStream_t st, bool pdl) {
   W8Args a = a0;
+  const bool w4 = a.bits == 4;
   // a QKV with a folded commit runs block rows and context rows as separate
   // 16-row chunks (they share the weight tiles through L2)
-  const int mt = a.c_nacc ? 2 : pick_mt(a.M);
+  const int mt = a.c_nacc ? 2 : pick_mt(a.M, w4);
   const int mch = mt * 8;
   const int chunks = (a.M + mch - 1) / mch;
   const int ntiles = a.nrows / kTile * (a.nl > 0 ? a.nl : 1);
-  const bool w4 = a.bits == 4;
-  const void* fn = w4 ? (mt == 2 ? (const void*)w8_gemm_kernel<2, 4>
-                         : mt == 4 ? (const void*)w8_gemm_kernel<4, 4> : (const void*)w8_gemm_kernel<8, 4>)
-                      : (mt == 2 ? (const void*)w8_gemm_kernel<2, 8>
-                         : mt == 4 ? (const void*)w8_gemm_kernel<4, 8> : (const void*)w8_gemm_kernel<8, 8>);
-  const size_t smem = w4 ? (mt == 2 ? Geo<2, 4>::SMEM : mt == 4 ? Geo<4, 4>::SMEM : Geo<8, 4>::SMEM)
-                         : (mt == 2 ? Geo<2>::SMEM : mt == 4 ? Geo<4>::SMEM : Geo<8>::SMEM);
+  const void* fn;
+  size_t smem;
+  int threads;
+  if (w4) {
+    fn = mt == 2 ? (const void*)wmma_gemm_kernel<2, 4>
+                 : mt == 4 ? (const void*)wmma_gemm_kernel<4, 4> : (const void*)wmma_gemm_kernel<8, 4>;
+    smem = mt == 2 ? Geo<2, 4>::SMEM : mt == 4 ? Geo<4, 4>::SMEM : Geo<8, 4>::SMEM;
+    threads = kThreads;
+  } else if (mt <= 4) {
+    fn = mt == 2 ? (const void*)wmma_gemm_kernel<2, 8> : (const void*)wmma_gemm_kernel<4, 8>;
+    smem = mt == 2 ? Geo<2, 8>::SMEM : Geo<4, 8>::SMEM;
+    threads = kThreads;
+  } else {
+    fn = mt == 8 ? (const void*)w8_gemm_kernel<8> : (const void*)w8_gemm_kernel<16>;
+    smem = mt == 8 ? TcGeo<8>::SMEM : TcGeo<16>::SMEM;
+    threads = kTcThreads;
+  }
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const int units = chunks * ntiles;
   a.splits = w8_pick_splits(units, a.K / kTile);
   // keep the whole grid resident in one wave
-  while (a.splits > 1 && units > max_active_clusters(fn, smem, a.splits)) --a.splits;
+  while (a.splits > 1 && units > max_active_clusters(fn, threads, smem, a.splits)) --a.splits;
   CUtensorMap map;
   if (!encode_tmap_2d(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, (uint64_t)a.K, (uint64_t)a.M,
                       (uint64_t)a.K * 2, 64, (uint32_t)mch, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   void* args[] = {&map, &a};
   dim3 grid(ntiles, a.splits, chunks);
-  return launch_kc(fn, grid, dim3(kThreads), smem, st, pdl, dim3(1, a.splits, 1), args);
+  return launch_kc(fn, grid, dim3(threads), smem, st, pdl, dim3(1, a.splits, 1), args);
 }
 
 cudaError_t w8_pack(const void* w, int w_dtype, int64_t N, int64_t K, int layout, uint8_t* q_out, __half* s_out,

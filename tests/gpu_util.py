@@ -12,34 +12,31 @@ def gpu_available() -> bool:
 
 
 def unpack_tiled_q(qbytes: np.ndarray, N: int, K: int, layout: int = 0) -> np.ndarray:
-    """Restates the packed W8 layout of include/dflash.h's packer to recover
-    the logical int8 q[N][K]: 128x128 tiles in (row-tile, k-tile) order, each
-    [warp 4][k16 step 8][lane 32][16 bytes = two 8-byte m16k16 fragments],
-    bytes stored as q + 128."""
+    """Restates the packed int8 layout of include/dflash.h's packer to recover
+    the logical q[N][K]: 128x128 tiles in (row-tile, k-tile) order, each
+    [packed row 128][128 bytes]; the 16 columns of group g of row r sit in the
+    16-byte chunk at r*128 + (g ^ (r % 8))*16, whose bytes 4t..4t+3 hold
+    columns 2t, 2t+1, 2t+8, 2t+9 of the group; bytes are q + 128.  Packed row
+    p of a gate|up matrix is logical row (p // 128)*64 + p % 128 for
+    p % 128 < 64, else N/2 + (p // 128)*64 + p % 128 - 64."""
     KT = K // 128
-    t = qbytes.reshape(N // 128, KT, 4, 8, 32, 2, 8).astype(np.int16) - 128
+    t = qbytes.reshape(N // 128, KT, 128, 8, 16).astype(np.int16) - 128
+    r = np.arange(128)
+    e = np.arange(16)
+    col_of_byte = 2 * (e >> 2) + (e & 1) + ((e >> 1) & 1) * 8
     q = np.empty((N, K), np.int8)
-    lane = np.arange(32)
-    g, tt = lane // 4, lane % 4
-    e = np.arange(8)
-    r_off = ((e >> 1) & 1) * 8
-    c_off = (e & 1) + ((e >> 2) & 1) * 8
-    rows = g[:, None] + r_off[None, :]          # [32][8]
-    cols = 2 * tt[:, None] + c_off[None, :]     # [32][8]
     for nt in range(N // 128):
-        for w in range(4):
-            for f in range(2):
-                mg = 2 * w + f
-                for ks in range(8):
-                    blk = t[nt, :, w, ks, :, f, :]  # [KT][32][8]
-                    pr = nt * 128 + mg * 16 + rows      # packed rows
-                    if layout == 1:
-                        tl, rr = pr >> 7, pr & 127
-                        lr = np.where(rr < 64, tl * 64 + rr, N // 2 + tl * 64 + (rr - 64))
-                    else:
-                        lr = pr
-                    for kt in range(KT):
-                        q[lr, kt * 128 + ks * 16 + cols] = blk[kt]
+        pr = nt * 128 + r
+        if layout == 1:
+            tl, rr = pr >> 7, pr & 127
+            lr = np.where(rr < 64, tl * 64 + rr, N // 2 + tl * 64 + (rr - 64))
+        else:
+            lr = pr
+        for kt in range(KT):
+            for g in range(8):
+                slot = g ^ (r & 7)
+                chunk = t[nt, kt, r, slot, :]  # [128][16] bytes of group g
+                q[lr[:, None], kt * 128 + g * 16 + col_of_byte[None, :]] = chunk
     return q
 
 

@@ -7,7 +7,7 @@ import numpy as np
 from oracle import dflash_oracle as O
 from block_diffusion_speculative_draft_gb300.configs import QWEN3_4B, TINY, ALL
 from block_diffusion_speculative_draft_gb300 import workload as WL
-from tests.gpu_util import unpack_tiled_q4
+from tests.gpu_util import unpack_tiled_q, unpack_tiled_q4
 
 
 def test_step_bytes_by_hand():
@@ -79,3 +79,33 @@ def test_int4_tile_decoder_reads_the_layout():
         q2, s2 = unpack_tiled_q4(_pack4_by_element(q, s, layout), 256, 256, layout)
         assert np.array_equal(q2, q)
         assert np.array_equal(s2.view(np.uint16), s.view(np.uint16))
+
+
+def _pack8_by_element(q, layout):
+    """Byte image of the packed int8 tiles built element by element from the
+    layout rule (tile (nt, kt) at (nt K/128 + kt) 16 KB; within the tile,
+    column c of packed row r, c = 16 g + j, goes to chunk g ^ (r % 8) of the
+    row at byte 4 (j % 8 // 2) + (j % 2) + 2 (j // 8); q + 128)."""
+    N, K = q.shape
+    KT = K // 128
+    buf = np.zeros(N * K, np.uint8)
+    for p in range(N):
+        nt, r = p // 128, p % 128
+        if layout == 1:
+            lr = nt * 64 + r if r < 64 else N // 2 + nt * 64 + (r - 64)
+        else:
+            lr = p
+        for c in range(K):
+            kt, cc = c // 128, c % 128
+            g, j = cc // 16, cc % 16
+            byte = 4 * ((j % 8) // 2) + (j % 2) + 2 * (j // 8)
+            off = (nt * KT + kt) * 16384 + r * 128 + ((g ^ (r % 8)) * 16) + byte
+            buf[off] = (int(q[lr, c]) + 128) & 0xFF
+    return buf
+
+
+def test_int8_tile_decoder_reads_the_layout():
+    rng = np.random.default_rng(4)
+    q = rng.integers(-127, 128, size=(256, 256)).astype(np.int8)
+    for layout in (0, 1):
+        assert np.array_equal(unpack_tiled_q(_pack8_by_element(q, layout), 256, 256, layout), q)
