@@ -296,7 +296,7 @@ def run_ours(args, rank, world, local_rank):
     K, Wm = args.steps, max(3, args.warmup)
     hbm, peak_kind = peaks()
     W = synth.drafter_weights(cfg)
-    model = api.DeviceDrafter(cfg, W, dev)
+    model = api.DeviceDrafter(cfg, synth.FloatWeights(W), dev)
     ctx = contexts(cfg)
     # context sweep: (label, committed length per sequence); the default
     # workload also times the pages' other contexts, any other workload its own
@@ -469,7 +469,7 @@ def run_ours(args, rank, world, local_rank):
     w4 = None
     if not args.no_w4:
         W4 = synth.drafter_weights(cfg, bits=4)
-        m4 = api.DeviceDrafter(cfg, W4, dev, bits=4)
+        m4 = api.DeviceDrafter(cfg, synth.FloatWeights(W4), dev, bits=4)
         del W4
         draft4 = torch.empty_like(draft)
         with api.launch_mode(api.LAUNCH_EARLY):
@@ -563,7 +563,7 @@ def overlap_measurement(torch, api, args, world, dev, K, Wm):
     from block_diffusion_speculative_draft_gb300 import workload as WL
     cfg = configs.QWEN3_4B
     b = cfg.b
-    model = api.DeviceDrafter(cfg, synth.drafter_weights(cfg), dev)
+    model = api.DeviceDrafter(cfg, synth.FloatWeights(synth.drafter_weights(cfg)), dev)
     ctx = WL.contexts(cfg)
     standin = WL.TargetStandIn(api, torch, cfg, dev)
     groups = []

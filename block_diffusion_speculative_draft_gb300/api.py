@@ -359,30 +359,37 @@ class DeviceDrafter:
     """A drafter's tensors resident on the GPU, packed by dflash_pack_w8a16
     (bits 8) or dflash_pack_w4a16 (bits 4).
 
-    `W` is the host dict from synth.drafter_weights (int8 or int4 grids +
-    fp16 scales, fp32 gammas, bf16 tables).  Each matrix is uploaded as its
-    fp32 float weight and packed on the device, one matrix at a time."""
+    `weights` maps names to host arrays: the projection matrices "fc",
+    "qkv{l}", "o{l}", "gu{l}", "down{l}" as float weights [N][K] (anything
+    numpy can turn into fp32; the gate|up matrix holds F gate rows then F up
+    rows), the fp32 RMSNorm gammas "gamma_hid" [H], "gamma_in" / "gamma_post"
+    [L][H], "gamma_q" / "gamma_k" [L][d], "gamma_final" [H], and the bf16 bit
+    patterns (uint16) of "embed" and "lm_head" [V][H].  Matrices are read one
+    at a time, uploaded as fp32 and packed on the device, so a mapping that
+    builds each matrix on access keeps at most one float matrix alive."""
 
-    def __init__(self, cfg, W: Dict[str, object], device="cuda", bits: int = 8):
+    def __init__(self, cfg, weights, device="cuda", bits: int = 8):
         torch = _torch()
         self.cfg = cfg
         self.keep: List[object] = []
         dev = torch.device(device)
-        from . import synth
-
+        if bits not in (4, 8):
+            raise ValueError("bits must be 4 or 8")
         self.bits = bits
+        W = weights
 
         def pack(name, layout=LAYOUT_PLAIN):
-            q, s = W[name]
+            w = torch.from_numpy(np.ascontiguousarray(W[name], dtype=np.float32)).to(dev)
+            if w.dim() != 2:
+                raise ValueError(f"{name}: expected a 2-D float weight")
+            N, K = w.shape
             if bits == 4:
-                w = torch.from_numpy(synth.w4_float(q, s)).to(dev)
                 qd, sd = dflash_pack_w4a16(w, layout)
             else:
-                w = torch.from_numpy(synth.w8_float(q, s)).to(dev)
                 qd, sd = dflash_pack_w8a16(w, layout)
             del w
             self.keep += [qd, sd]
-            return W8(qd.data_ptr(), sd.data_ptr(), q.shape[0], q.shape[1], layout, bits)
+            return W8(qd.data_ptr(), sd.data_ptr(), N, K, layout, bits)
 
         def up(a, dtype=None):
             t = torch.from_numpy(np.ascontiguousarray(a)).to(dev)
@@ -396,8 +403,8 @@ class DeviceDrafter:
         self.gu = (W8 * L)(*[pack(f"gu{l}", LAYOUT_GATEUP) for l in range(L)])
         self.down = (W8 * L)(*[pack(f"down{l}") for l in range(L)])
         torch.cuda.synchronize()
-        self.embed_t = torch.from_numpy(W["embed"].view(np.int16)).to(dev)
-        self.lm_t = torch.from_numpy(W["lm_head"].view(np.int16)).to(dev)
+        self.embed_t = torch.from_numpy(np.ascontiguousarray(W["embed"]).view(np.int16)).to(dev)
+        self.lm_t = torch.from_numpy(np.ascontiguousarray(W["lm_head"]).view(np.int16)).to(dev)
         self.keep += [self.embed_t, self.lm_t]
         self.c = Weights(to_c_config(cfg), self.fc,
                          ctypes.cast(self.qkv, ctypes.POINTER(W8)), ctypes.cast(self.o, ctypes.POINTER(W8)),

@@ -365,43 +365,43 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
 
 }  // namespace
 
-// Whether a cluster of ns splits can be resident (non-portable sizes above 8
-// need the opt-in attribute and enough free SMs in one GPC).
-// The answer is cached per (device, kernel, ns, threads, smem).
-static bool attn_cluster_fits(const void* fn, int ns, int threads, size_t smem) {
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
+// How many clusters of ns splits can be resident at once (0 when a cluster
+// of that size cannot be launched).  Non-portable sizes above 8 need the
+// opt-in attribute and ns free SMs in one GPC; on a 152-SM part a cluster of
+// 16 one-CTA-per-SM splits fits only seven times, not eight.  The answer is
+// cached per (device, kernel, ns, threads, smem).
+static int attn_max_clusters(const void* fn, int ns, int threads, size_t smem) {
   int dev = 0;
   cudaGetDevice(&dev);
   const auto key = std::make_tuple(dev, fn, ns, threads, smem);
   static std::mutex mu;
-  static std::map<std::tuple<int, const void*, int, int, size_t>, bool> cache;
+  static std::map<std::tuple<int, const void*, int, int, size_t>, int> cache;
   {
     std::lock_guard<std::mutex> lk(mu);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
   }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(ns, 1, 1);
-  cfg.blockDim = dim3(threads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = ns;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    n = 0;
+  if (ns <= kPortable || cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ns, 1, 1);
+    cfg.blockDim = dim3(threads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = ns;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess)
+      n = 0;
   }
+  cudaGetLastError();
   std::lock_guard<std::mutex> lk(mu);
-  cache[key] = n > 0;
-  return n > 0;
+  cache[key] = n;
+  return n;
 }
 
 cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
@@ -415,17 +415,6 @@ cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
     return a.d == 128 ? (kh2 ? (const void*)attn_kernel<128, 2> : (const void*)attn_kernel<128, 1>)
                       : (kh2 ? (const void*)attn_kernel<64, 2> : (const void*)attn_kernel<64, 1>);
   };
-  const void* fn = kernel_for(false);
-  // one 64-key tile per split while the longest possible context allows it,
-  // so the (latency-bound) pass is as short as the split count permits
-  int ns = (a.cap + a.B + kKT - 1) / kKT;
-  // no more splits than keep about two CTAs per SM busy when the batch and
-  // the kv heads already fill the GPU (a grid of several waves costs more than
-  // longer splits)
-  const int fill = (2 * num_sms() + a.b * a.nkv - 1) / (a.b * a.nkv);
-  if (ns > fill) ns = fill;
-  if (ns > kMaxSplits) ns = kMaxSplits;
-  if (ns < 1) ns = 1;
   auto smem_for = [&](int n) {
     // Q, double-buffered K/V, per-row lse, then the merge's receive area
     size_t b = 128 + (size_t)rows_pad * a.d * 2 + 4 * kKT * a.d * 2 + rows_pad * 4;
@@ -435,21 +424,37 @@ cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
     }
     return b;
   };
-  size_t smem = smem_for(ns);
-  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (ns > kPortable && !attn_cluster_fits(fn, ns, nthr, smem)) {
-    ns = kPortable;
-    smem = smem_for(ns);
-    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // Split count: the longest possible context (capacity plus the block) is
+  // cut into ns chunks of whole 64-key tiles, one CTA each, the ns CTAs of a
+  // (sequence, kv head) forming one cluster.  Cost model: waves of resident
+  // clusters times tiles per split (the pass is latency-bound, each tile a
+  // serial step), the fewest splits among equal costs; splits that would be
+  // left empty by the tile rounding are not launched.
+  const int total = a.cap + a.B;
+  const int ntiles = (total + kKT - 1) / kKT;
+  const int need = a.b * a.nkv;  // clusters
+  int ns = 1;
+  long best = -1;
+  for (int n = 1; n <= kMaxSplits && n <= ntiles; ++n) {
+    const int per = (ntiles + n - 1) / n;   // tiles per split
+    const int used = (ntiles + per - 1) / per;  // splits that get keys
+    if (used != n) continue;
+    const int fit = attn_max_clusters(kernel_for(false), n, nthr, smem_for(n));
+    if (fit <= 0) continue;
+    const long cost = (long)((need + fit - 1) / fit) * per;
+    if (best < 0 || cost < best) {
+      best = cost;
+      ns = n;
+    }
   }
+  const int tiles = (ntiles + ns - 1) / ns;
+  size_t smem = smem_for(ns);
   // helper warps take the second key half of every tile when a split has
   // several tiles (one tile: the extra merge costs more than it saves)
-  const int tiles = ((a.cap + a.B + ns - 1) / ns + kKT - 1) / kKT;
-  if (nthr >= 2 * nw * 32 && tiles >= 2) {
-    fn = kernel_for(true);
-    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (ns > kPortable) cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-  }
+  const bool kh2 = nthr >= 2 * nw * 32 && tiles >= 2;
+  const void* fn = kernel_for(kh2);
+  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (ns > kPortable) cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   dim3 grid(ns, a.nkv, a.b);
   void* args[] = {&a};
   return launch_kc(fn, grid, dim3(nthr), smem, st, pdl, dim3(ns, 1, 1), args);

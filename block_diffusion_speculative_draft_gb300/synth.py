@@ -200,6 +200,29 @@ def drafter_weights(cfg, with_float: bool = False, bits: int = 8) -> Dict[str, o
     return W
 
 
+class FloatWeights:
+    """A read-only view of drafter_weights' dict in which every projection
+    matrix reads as its float weight (fp32, grid times scale) and every other
+    entry as stored.  Each matrix is built on access, so a consumer that
+    takes them one at a time holds one float matrix at a time."""
+
+    def __init__(self, W: Dict[str, object]):
+        self.W = W
+
+    def __getitem__(self, name: str):
+        v = self.W[name]
+        if isinstance(v, tuple):
+            q, s = v
+            return w4_float(q, s) if s.ndim == 2 else w8_float(q, s)
+        return v
+
+    def __contains__(self, name: str) -> bool:
+        return name in self.W
+
+    def keys(self):
+        return self.W.keys()
+
+
 W8_NAMES = ("qkv", "o", "gu", "down")
 
 

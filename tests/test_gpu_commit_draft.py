@@ -34,7 +34,7 @@ def test_commit_draft_matches_commit_then_draft(cfg):
     b, B = cfg.b, cfg.B
     rps = B
     W = synth.drafter_weights(cfg)
-    model = api.DeviceDrafter(cfg, W, DEV)
+    model = api.DeviceDrafter(cfg, synth.FloatWeights(W), DEV)
     ctx = contexts(cfg)
     cap = int(ctx.max()) + 2 * B
     kvs, wss = [], []

@@ -27,7 +27,7 @@ TOL = 2e-2
 
 def _setup(cfg, rows_per_seq, extra_cap=64):
     W = synth.drafter_weights(cfg)
-    model = api.DeviceDrafter(cfg, W, DEV)
+    model = api.DeviceDrafter(cfg, synth.FloatWeights(W), DEV)
     ctx = contexts(cfg)
     kv = api.KVCache(cfg, cfg.b, int(ctx.max()) + extra_cap, DEV)
     ws = api.workspace(cfg, cfg.b, rows_per_seq, DEV)
@@ -142,7 +142,7 @@ def test_tiny_loop_commit_rollback():
 def test_capacity_overflow_flags_and_skips():
     cfg = TINY.with_ctx((40,))
     W = synth.drafter_weights(cfg)
-    model = api.DeviceDrafter(cfg, W, DEV)
+    model = api.DeviceDrafter(cfg, synth.FloatWeights(W), DEV)
     kv = api.KVCache(cfg, 1, 48, DEV)
     ws = api.workspace(cfg, 1, cfg.B, DEV)
     api.dflash_get_status(clear=True)
@@ -161,7 +161,7 @@ def test_capacity_overflow_flags_and_skips():
 def test_bad_token_flag():
     cfg = TINY
     W = synth.drafter_weights(cfg)
-    model = api.DeviceDrafter(cfg, W, DEV)
+    model = api.DeviceDrafter(cfg, synth.FloatWeights(W), DEV)
     kv = api.KVCache(cfg, 1, 64, DEV)
     ws = api.workspace(cfg, 1, cfg.B, DEV)
     api.dflash_get_status(clear=True)

@@ -38,7 +38,7 @@ def _early_launch():
 @pytest.mark.parametrize("cfg,seqs", CASES, ids=[f"{c.name}-ctx{c.ctx[0] if c.ctx else 'ragged'}" for c, _ in CASES])
 def test_fullsize_step(cfg, seqs):
     W = synth.drafter_weights(cfg)
-    model = api.DeviceDrafter(cfg, W, DEV)
+    model = api.DeviceDrafter(cfg, synth.FloatWeights(W), DEV)
     ctx = contexts(cfg)
     b = cfg.b
     rps = 64 if b > 1 else cfg.B

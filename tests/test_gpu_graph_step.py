@@ -25,7 +25,7 @@ if gpu_available():
 
 def _run(cfg, check_draft_vs_oracle: bool):
     W = synth.drafter_weights(cfg)
-    model = api.DeviceDrafter(cfg, W, DEV)
+    model = api.DeviceDrafter(cfg, synth.FloatWeights(W), DEV)
     ctx = contexts(cfg)
     b, B = cfg.b, cfg.B
     kv = api.KVCache(cfg, b, int(ctx.max()) + 2 * B, DEV)

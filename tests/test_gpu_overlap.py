@@ -143,7 +143,7 @@ def _check_standin_and_accept(cfg, gs, snap, row_ranges):
 def test_overlap_tiny():
     cfg = TINY
     W = synth.drafter_weights(cfg)
-    model = api.DeviceDrafter(cfg, W, DEV)
+    model = api.DeviceDrafter(cfg, synth.FloatWeights(W), DEV)
     standin = WL.TargetStandIn(api, torch, cfg, DEV)
     gs = _groups(cfg, model, 3)
     snap = _run_all_ways(cfg, W, model, standin, gs)
@@ -155,7 +155,7 @@ def test_overlap_tiny():
 def test_overlap_qwen3_4b_shape():
     cfg = QWEN3_4B
     W = synth.drafter_weights(cfg)
-    model = api.DeviceDrafter(cfg, W, DEV)
+    model = api.DeviceDrafter(cfg, synth.FloatWeights(W), DEV)
     standin = WL.TargetStandIn(api, torch, cfg, DEV)
     gs = _groups(cfg, model, 2)
     snap = _run_all_ways(cfg, W, model, standin, gs)

@@ -66,7 +66,7 @@ def test_w4a16_linear(M, N, K, layout):
 
 def _w4_model(cfg, rps, extra_cap=64):
     W = synth.drafter_weights(cfg, bits=4)
-    model = api.DeviceDrafter(cfg, W, DEV, bits=4)
+    model = api.DeviceDrafter(cfg, synth.FloatWeights(W), DEV, bits=4)
     ctx = contexts(cfg)
     kv = api.KVCache(cfg, cfg.b, int(ctx.max()) + extra_cap, DEV)
     ws = api.workspace(cfg, cfg.b, rps, DEV)

@@ -109,3 +109,23 @@ def test_int8_tile_decoder_reads_the_layout():
     q = rng.integers(-127, 128, size=(256, 256)).astype(np.int8)
     for layout in (0, 1):
         assert np.array_equal(unpack_tiled_q(_pack8_by_element(q, layout), 256, 256, layout), q)
+
+
+def test_float_weights_view_reads_grid_times_scale():
+    """The host view handed to DeviceDrafter: matrices read as grid x scale
+    (row scales for int8, 128-column group scales for int4), every other entry
+    as stored."""
+    from block_diffusion_speculative_draft_gb300 import synth
+    W8 = synth.drafter_weights(TINY)
+    F8 = synth.FloatWeights(W8)
+    q, s = W8["o0"]
+    w = F8["o0"]
+    assert w.dtype == np.float32 and w.shape == q.shape
+    r, c = 3, 5
+    assert w[r, c] == np.float32(q[r, c]) * np.float32(s[r])
+    assert F8["gamma_in"] is W8["gamma_in"] and F8["embed"] is W8["embed"]
+    W4 = synth.drafter_weights(TINY, bits=4)
+    q4, s4 = W4["down0"]
+    w4 = synth.FloatWeights(W4)["down0"]
+    assert w4[r, 130] == np.float32(q4[r, 130]) * np.float32(s4[r, 1])
+    assert w4[r, 127] == np.float32(q4[r, 127]) * np.float32(s4[r, 0])
