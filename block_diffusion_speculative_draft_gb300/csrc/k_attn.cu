@@ -8,17 +8,21 @@
 // nq/nkv query heads that share a kv head form one query tile (64 rows for
 // B = 16, group 4), so every K/V byte is read once per kv head.  One compute
 // warp per 16 query rows; as many helper warps again (up to 10 warps in all)
-// share the copies and the split merge, which are latency-bound, and, when a
-// split spans several tiles, compute the second key half of every tile.  Long contexts
-// are split along the keys (flash-decoding; the pages' long-context verify
-// likewise uses a two-pass attention, dflash-mlx summary, "기술적 도전":
-// JIT SDPA 2-pass for N >= 1024): the splits of one (sequence, kv head) form
-// a thread-block cluster; each keeps an online softmax, leaves its normalised
-// partial output and log-sum-exp in shared memory, and after a cluster
-// barrier every CTA merges one slice of query rows over all splits through
-// distributed shared memory, in split order.  Q.K^T and P.V run on m16n8k16
-// tensor-core MMAs with fp32 accumulation; K/V tiles of 64 keys are
-// double-buffered with cp.async into XOR-swizzled shared memory.
+// share the copies and, when a split spans several tiles, compute the second
+// key half of every tile.  Long contexts are split along the keys
+// (flash-decoding; the pages' long-context verify likewise uses a two-pass
+// attention, dflash-mlx summary, "기술적 도전": JIT SDPA 2-pass for
+// N >= 1024), as many splits as keep every (sequence, kv head) cluster
+// resident at once: the splits of one (sequence, kv head) form a thread-block
+// cluster; each keeps an online softmax, stages its normalised partial rows
+// and log-sum-exps grouped by the CTA that merges them, and sends each group
+// with one bulk shared-to-shared::cluster copy; every CTA then merges its
+// slice of query rows over all splits, in split order.  Q.K^T and P.V run on
+// m16n8k16 tensor-core MMAs with fp32 accumulation.  Whole tiles of committed
+// context (64 keys) arrive by tensor-map copies (128-byte swizzle) into a ring
+// of two or three stages, issued ahead by one thread; the tile where the
+// context meets the block (and any rows a folded commit appends) is gathered
+// row by row with cp.async into the same swizzled layout.
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -42,28 +46,43 @@ __device__ __forceinline__ void split_range(int total, int sp, int ns, int& k0, 
   k1 = min(total, k0 + chunk);
 }
 
-template <int D, int KH>
-__global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
-  constexpr int RB = D * 2;  // bytes per row
+__device__ __forceinline__ float ex2(float x) {  // 2^x, hardware approximation; 2^-inf = 0
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Byte offset of 16-byte chunk ch (of D / 8) of row r in a K or V stage:
+// [D / 64 column halves][64 rows][128 bytes], chunk c of a row at c ^ (r % 8)
+// (the layout a 64 x 64 fp16 tensor-map box with 128-byte swizzle writes).
+__device__ __forceinline__ int kv_off(int r, int ch) {
+  return ((ch >> 3) << 13) + (r << 7) + (((ch & 7) ^ (r & 7)) << 4);
+}
+
+template <int D, int KH, int NST>
+__global__ void __launch_bounds__(320, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
+  constexpr int RB = D * 2;             // bytes per row
+  constexpr int KVB = kKT * RB;         // bytes of one K (or V) tile
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int sp = blockIdx.x, g = blockIdx.y, j = blockIdx.z;
   const int ns = gridDim.x;
   const int grp = a.nq / a.nkv;
   const int rows = a.B * grp;
   const int nwc = a.nwc;
   const int rows_pad = nwc * 16;
-  uint8_t* sQ = smem;
-  uint8_t* sK = sQ + rows_pad * RB;        // [2][64][D]
-  uint8_t* sV = sK + 2 * kKT * RB;         // [2][64][D]
-  float* sLse = reinterpret_cast<float*>(sV + 2 * kKT * RB);  // [rows_pad]
+  uint8_t* sK = smem;                   // [NST][KVB], 1024-aligned
+  uint8_t* sV = sK + NST * KVB;         // [NST][KVB]
+  uint8_t* sQ = sV + NST * KVB;         // [rows_pad][RB], chunk ch of row r at ch ^ (r % 8)
+  uint64_t* full = reinterpret_cast<uint64_t*>(sQ + rows_pad * RB);  // [NST], receive barrier at [7]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // The context K/V and its length are inputs of the whole draft pass (no
-  // kernel of the pass writes them), so the first tile's context keys are
-  // fetched before waiting for the kernel that produces q and the block K/V.
-  // (a commit folded into this pass appends rows [Lold, L), written by this
-  // layer's QKV kernel: those are read only after the wait)
+  // kernel of the pass writes them), so context tiles are fetched before
+  // waiting for the kernel that produces q and the block K/V.  (A commit
+  // folded into this pass appends rows [Lold, L), written by this layer's QKV
+  // kernel: those are read only after the wait.)
   int L = a.len[j];
   if (L < 0) L = 0;
   if (L > a.cap) L = a.cap;
@@ -72,38 +91,78 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
   const int total = L + a.B;
   int k0, k1;
   split_range(total, sp, ns, k0, k1);
+  const int ntile = (k1 - k0 + kKT - 1) / kKT;
+  const int row0 = (j * a.nkv + g) * a.cap;  // this head's first cache row in the tensor maps
+  // tile i is a whole tile of committed context (one tensor-map box per 64
+  // columns of K and of V) or is gathered row by row (the rest)
+  auto is_tma = [&](int i) { return k0 + (i + 1) * kKT <= min(k1, Lold); };
 
-  // part 0: context keys t < Lold only; 1: the rest (appended context rows,
-  // block keys, zero fill); 2: all
-  auto load_kv = [&](int buf, int t0, int part) {
+  // split merge (ns > 1): CTA p of the cluster merges query rows
+  // [p rows / ns, (p + 1) rows / ns); every split sends it those rows, counted
+  // in bytes on its receive barrier
+  constexpr int RS = D + 4;  // staged row: D partial outputs, then the log-sum-exp
+  const int maxr = (rows + ns - 1) / ns;
+  const int r0 = (sp * rows) / ns, r1 = ((sp + 1) * rows) / ns;
+  uint64_t* rbar = full + 7;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) mbar_init(&full[i], 1);
+    if (ns > 1) {
+      mbar_init(rbar, 1);
+      mbar_arrive_expect_tx(rbar, (uint32_t)(ns * (r1 - r0) * RS * 4));
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // peers may target this CTA's receive barrier once they have passed the
+  // matching wait (after their main loop)
+  if (ns > 1) cluster_arrive();
+  auto issue_tma = [&](int i, int stg) {  // thread 0 only
+    fence_proxy_async_shared();  // the stage may last have been written by cp.async
+    mbar_arrive_expect_tx(&full[stg], 2 * KVB);
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+      tma_load_2d(sK + stg * KVB + h * 8192, &kmap, h * 64, row0 + k0 + i * kKT, &full[stg]);
+      tma_load_2d(sV + stg * KVB + h * 8192, &vmap, h * 64, row0 + k0 + i * kKT, &full[stg]);
+    }
+  };
+  // gathered tile: part 0 = committed context rows t < Lold only, 1 = the
+  // rest (appended context rows, block keys, zero fill), 2 = all
+  auto load_rows = [&](int stg, int t0, int part) {
     for (int c = threadIdx.x; c < kKT * (D / 8); c += blockDim.x) {
-      int r = c / (D / 8), ch = c % (D / 8);
-      int t = t0 + r;
-      bool ok = t < k1;
-      const bool ctx = ok && t < L;
+      const int r = c / (D / 8), ch = c % (D / 8);
+      const int t = t0 + r;
+      const bool ok = t < k1;
       const bool old_ctx = ok && t < Lold;
       if (part == 0 && !old_ctx) continue;
       if (part == 1 && old_ctx) continue;
       const __half* ks = a.kc;
       const __half* vs = a.vc;
       if (ok) {
-        if (ctx) {
-          size_t off = (((size_t)j * a.nkv + g) * a.cap + t) * D + ch * 8;
+        if (t < L) {
+          const size_t off = ((size_t)row0 + t) * D + ch * 8;
           ks = a.kc + off;
           vs = a.vc + off;
         } else {
-          size_t off = ((size_t)(j * a.B + (t - L)) * a.nkv + g) * D + ch * 8;
+          const size_t off = ((size_t)(j * a.B + (t - L)) * a.nkv + g) * D + ch * 8;
           ks = a.kblk + off;
           vs = a.vblk + off;
         }
       }
-      int so = buf * kKT * RB + r * RB + ((ch ^ (r & 7)) << 4);
+      const int so = stg * KVB + kv_off(r, ch);
       cp_async16(sK + so, ks, ok);
       cp_async16(sV + so, vs, ok);
     }
   };
-  const int ntile = (k1 - k0 + kKT - 1) / kKT;
-  load_kv(0, k0, 0);
+  // prologue: tiles 0 .. NST-2; the context part before the wait
+  constexpr int PRE = NST - 1;
+  if (threadIdx.x == 0) {
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&vmap);
+    for (int i = 0; i < PRE && i < ntile; ++i)
+      if (is_tma(i)) issue_tma(i, i);
+  }
+  for (int i = 0; i < PRE && i < ntile; ++i)
+    if (!is_tma(i)) load_rows(i, k0 + i * kKT, 0);
   if (a.pf_base && threadIdx.x == 0)
     prefetch_l2_job(a.pf_base, a.pf_stride, a.pf_bytes, a.pf_i0, a.pf_i1,
                     blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z), gridDim.x * gridDim.y * gridDim.z);
@@ -120,16 +179,21 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
     }
     cp_async16(sQ + rho * RB + ((ch ^ (rho & 7)) << 4), src, ok);
   }
-  load_kv(0, k0, 1);
-  cp_async_commit();
+  // one cp.async group per prologue tile (group 0 also holds Q and every
+  // context part issued above: waiting for it early is only conservative)
+  for (int i = 0; i < PRE; ++i) {
+    if (i < ntile && !is_tma(i)) load_rows(i, k0 + i * kKT, 1);
+    cp_async_commit();
+  }
 
-  const float sl2 = rsqrtf((float)D) * 1.4426950408889634f;
+  const float sl2 = rsqrtf((float)D) * 1.4426950408889634f;  // 1/sqrt(d) in log2 units
   const int g8 = lane >> 2, t4 = lane & 3;
   float o[D / 8][4];
 #pragma unroll
   for (int i = 0; i < D / 8; ++i)
 #pragma unroll
     for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
+  // running max (raw score units) and sum of the two rows g8, g8 + 8
   float mrow[2] = {-INFINITY, -INFINITY}, lrow[2] = {0.f, 0.f};
   uint32_t qf[D / 16][4];
 
@@ -140,10 +204,27 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
   constexpr int NN = KK / 8;    // n8 score tiles per warp
   const int rb = warp % nwc, half = warp / nwc;
   const bool cw = warp < nwc * KH;
+  uint32_t phase = 0;  // bit s: parity of the next tensor-map fill of stage s
+  int stg = 0;
   for (int it = 0; it < ntile; ++it) {
-    if (it + 1 < ntile) load_kv((it + 1) & 1, k0 + (it + 1) * kKT, 2);
-    cp_async_commit();
-    cp_async_wait<1>();
+    {  // refill: tile it + PRE goes to the stage tile it - 1 used
+      const int nx = it + PRE;
+      const int ns2 = (stg + PRE) % NST;
+      if (nx < ntile) {
+        if (is_tma(nx)) {
+          if (threadIdx.x == 0) issue_tma(nx, ns2);
+        } else {
+          load_rows(ns2, k0 + nx * kKT, 2);
+        }
+      }
+      cp_async_commit();
+    }
+    const bool tma = is_tma(it);
+    if (tma) {
+      mbar_wait(&full[stg], (phase >> stg) & 1u, a.status);
+      phase ^= 1u << stg;
+    }
+    cp_async_wait<PRE>();
     __syncthreads();
     if (cw) {
       if (it == 0) {
@@ -155,10 +236,9 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
           ldsm_x4(qb + row * RB + ((ch ^ (row & 7)) << 4), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
         }
       }
-      const int buf = it & 1;
-      const uint32_t kb = smem_u32(sK + buf * kKT * RB);
-      const uint32_t vb = smem_u32(sV + buf * kKT * RB);
-      // S = Q K^T : 16 rows x KK keys per warp
+      const uint32_t kb = smem_u32(sK + stg * KVB);
+      const uint32_t vb = smem_u32(sV + stg * KVB);
+      // S = Q K^T : 16 rows x KK keys per warp (raw dot products)
       float s[NN][4];
 #pragma unroll
       for (int n = 0; n < NN; ++n)
@@ -168,48 +248,46 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
       for (int ks = 0; ks < D / 16; ++ks) {
 #pragma unroll
         for (int n16 = 0; n16 < NN / 2; ++n16) {
-          int key = half * KK + n16 * 16 + (lane & 7) + ((lane >> 4) << 3);
-          int ch = 2 * ks + ((lane >> 3) & 1);
+          const int key = half * KK + n16 * 16 + (lane & 7) + ((lane >> 4) << 3);
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(kb + key * RB + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+          ldsm_x4(kb + kv_off(key, 2 * ks + ((lane >> 3) & 1)), b0, b1, b2, b3);
           mma_f16(s[2 * n16], qf[ks], b0, b1);
           mma_f16(s[2 * n16 + 1], qf[ks], b2, b3);
         }
       }
-      // scale, mask, online softmax (rows g8 and g8 + 8 of this warp); a half
-      // may see no valid key yet: its max stays -inf and contributes nothing
+      // keys past the split's end only occur in its last tile
       const int kbase = k0 + it * kKT + half * KK;
-      float mx[2] = {-INFINITY, -INFINITY};
+      if (kbase + KK > k1) {
 #pragma unroll
-      for (int n = 0; n < NN; ++n)
+        for (int n = 0; n < NN; ++n)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          int key = kbase + n * 8 + 2 * t4 + (e & 1);
-          float v = key < k1 ? s[n][e] * sl2 : -INFINITY;
-          s[n][e] = v;
-          mx[e >> 1] = fmaxf(mx[e >> 1], v);
-        }
+          for (int e = 0; e < 4; ++e)
+            if (kbase + n * 8 + 2 * t4 + (e & 1) >= k1) s[n][e] = -INFINITY;
+      }
+      // online softmax in log2 units: p = 2^(s sl2 - m sl2); a half may see
+      // no valid key yet: its max stays -inf and contributes nothing
+      float mx[2] = {mrow[0], mrow[1]};
+#pragma unroll
+      for (int n = 0; n < NN; ++n) {
+        mx[0] = fmaxf(mx[0], fmaxf(s[n][0], s[n][1]));
+        mx[1] = fmaxf(mx[1], fmaxf(s[n][2], s[n][3]));
+      }
+      float corr[2], nb[2], rs[2] = {0.f, 0.f};
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
         mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      }
-      float corr[2], mnew[2], rs[2] = {0.f, 0.f};
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        mnew[r] = fmaxf(mrow[r], mx[r]);
-        corr[r] = mnew[r] == -INFINITY ? 1.f : exp2f(mrow[r] - mnew[r]);
-        mrow[r] = mnew[r];
+        corr[r] = mx[r] == -INFINITY ? 1.f : ex2((mrow[r] - mx[r]) * sl2);
+        nb[r] = mx[r] == -INFINITY ? 0.f : -mx[r] * sl2;
+        mrow[r] = mx[r];
       }
       uint32_t pf[NN / 2][4];  // P as the A operand of P.V, k16 steps over KK keys
 #pragma unroll
       for (int n = 0; n < NN; ++n) {
-        const float q0 = mnew[0] == -INFINITY ? 0.f : mnew[0];
-        const float q1 = mnew[1] == -INFINITY ? 0.f : mnew[1];
-        float p0 = exp2f(s[n][0] - q0);
-        float p1 = exp2f(s[n][1] - q0);
-        float p2 = exp2f(s[n][2] - q1);
-        float p3 = exp2f(s[n][3] - q1);
+        const float p0 = ex2(fmaf(s[n][0], sl2, nb[0]));
+        const float p1 = ex2(fmaf(s[n][1], sl2, nb[0]));
+        const float p2 = ex2(fmaf(s[n][2], sl2, nb[1]));
+        const float p3 = ex2(fmaf(s[n][3], sl2, nb[1]));
         rs[0] += p0 + p1;
         rs[1] += p2 + p3;
         __half2 h01 = __floats2half2_rn(p0, p1);
@@ -235,22 +313,23 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
       for (int kk = 0; kk < NN / 2; ++kk) {
 #pragma unroll
         for (int dp = 0; dp < D / 16; ++dp) {
-          int key = half * KK + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-          int ch = 2 * dp + (lane >> 4);
+          const int key = half * KK + kk * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vb + key * RB + ((ch ^ (key & 7)) << 4), b0, b1, b2, b3);
+          ldsm_x4_t(vb + kv_off(key, 2 * dp + (lane >> 4)), b0, b1, b2, b3);
           mma_f16(o[2 * dp], pf[kk], b0, b1);
           mma_f16(o[2 * dp + 1], pf[kk], b2, b3);
         }
       }
     }
     __syncthreads();
+    stg = stg + 1 == NST ? 0 : stg + 1;
   }
+  cp_async_wait<0>();  // empty trailing groups, and zero-fill copies of an empty split
   if (KH == 2) {
     // merge the key halves of each row block: half 1 hands (max, sum, O) over
-    // through shared memory (the K/V buffers are free once the copies land)
+    // through shared memory (the K/V stages are free once the last tile is
+    // consumed: every copy issued has been waited for)
     constexpr int XS = D + 4;  // row stride (floats)
-    cp_async_wait<0>();
     __syncthreads();
     float* xo = reinterpret_cast<float*>(sK);  // [nwc][16][XS]
     float* xm = xo + (size_t)nwc * 16 * XS;    // [nwc][16]
@@ -275,8 +354,8 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
       for (int r = 0; r < 2; ++r) {
         const float m1 = xm[rb * 16 + g8 + 8 * r], l1 = xl[rb * 16 + g8 + 8 * r];
         const float mn = fmaxf(mrow[r], m1);
-        c0[r] = mrow[r] == -INFINITY ? 0.f : exp2f(mrow[r] - mn);
-        c1[r] = m1 == -INFINITY ? 0.f : exp2f(m1 - mn);
+        c0[r] = mrow[r] == -INFINITY ? 0.f : ex2((mrow[r] - mn) * sl2);
+        c1[r] = m1 == -INFINITY ? 0.f : ex2((m1 - mn) * sl2);
         lrow[r] = lrow[r] * c0[r] + l1 * c1[r];
         mrow[r] = mn;
       }
@@ -295,7 +374,7 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     inv[r] = lrow[r] > 0.f ? 1.f / lrow[r] : 0.f;
-    lse[r] = lrow[r] > 0.f ? mrow[r] + log2f(lrow[r]) : -INFINITY;
+    lse[r] = lrow[r] > 0.f ? mrow[r] * sl2 + log2f(lrow[r]) : -INFINITY;
   }
   if (ns == 1) {
     if (warp < nwc)
@@ -309,19 +388,18 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
         int dim = i * 8 + 2 * t4 + (e & 1);
         a.out[((size_t)(j * a.B + tok) * a.nq + g * grp + hh) * D + dim] = __float2half_rn(o[i][e] * inv[e >> 1]);
       }
-    fence_proxy_async_global();  // the o projection reads the output with TMA
     return;
   }
-  // Push this split's normalised partial rows and log-sum-exps into the
-  // shared memory of the CTA that owns them (CTA p merges rows
-  // [p rows / ns, (p + 1) rows / ns)); remote stores do not wait for a reply,
-  // and the owner then merges from its own shared memory.  The receive area
-  // is separate from Q/K/V, so no barrier is needed before the pushes.
-  const int maxr = (rows + ns - 1) / ns;
-  constexpr int RS = D + 4;  // row stride (floats): conflict-free float2 stores
-  float* rO = reinterpret_cast<float*>(sLse + rows_pad);  // [ns][maxr][RS]
-  float* rL = rO + (size_t)ns * maxr * RS;                 // [ns][maxr]
-  const uint32_t rObase = smem_u32(rO), rLbase = smem_u32(rL);
+  // Stage this split's normalised partial rows and log-sum-exps in its own
+  // shared memory grouped by owner, then hand each owner its group with one
+  // bulk shared-to-shared::cluster copy.  The staging area reuses the K/V
+  // stages and Q (no longer read) when it fits there.
+  float* rO = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 64);  // receive [ns][maxr][RS]
+  const size_t need = (size_t)ns * maxr * RS * 4;
+  float* sst = need <= (size_t)2 * NST * KVB + (size_t)rows_pad * RB ? reinterpret_cast<float*>(sK)
+                                                                      : rO + (size_t)ns * maxr * RS;
+  cluster_wait();   // every peer's receive barrier is initialised and armed
+  __syncthreads();  // nothing reads the K/V stages, Q or the key-half scratch any more
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     if (warp >= nwc) break;
@@ -329,24 +407,35 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
     if (rho >= rows) continue;
     const int own = ((rho + 1) * ns - 1) / rows;
     const int lr = rho - (own * rows) / ns;
-    const uint32_t dst = dsmem_addr(rObase + (uint32_t)((sp * maxr + lr) * RS + 2 * t4) * 4u, (uint32_t)own);
+    float* dst = sst + (size_t)(own * maxr + lr) * RS + 2 * t4;
 #pragma unroll
-    for (int i = 0; i < D / 8; ++i) st_dsmem_f2(dst + i * 32u, o[i][2 * h] * inv[h], o[i][2 * h + 1] * inv[h]);
-    if (t4 == 0) st_dsmem_f32(dsmem_addr(rLbase + (uint32_t)(sp * maxr + lr) * 4u, (uint32_t)own), lse[h]);
+    for (int i = 0; i < D / 8; ++i)
+      *reinterpret_cast<float2*>(dst + i * 8) = make_float2(o[i][2 * h] * inv[h], o[i][2 * h + 1] * inv[h]);
+    if (t4 == 0) sst[(size_t)(own * maxr + lr) * RS + D] = lse[h];
   }
-  cp_async_wait<0>();  // an empty split may still have zero-fill copies in flight
-  cluster_sync();      // every push into this CTA is visible
+  fence_proxy_async_shared();  // each writer: the staged rows are visible to the bulk copies
+  __syncthreads();
+  if (warp == 0 && lane < ns) {
+    const int p = lane;
+    const int nr = ((p + 1) * rows) / ns - (p * rows) / ns;
+    if (nr > 0)
+      bulk_s2cluster(dsmem_addr(smem_u32(rO + (size_t)sp * maxr * RS), (uint32_t)p),
+                     smem_u32(sst + (size_t)p * maxr * RS), (uint32_t)(nr * RS * 4),
+                     dsmem_addr(smem_u32(rbar), (uint32_t)p));
+    bulk_commit();
+  }
   // merge the owned rows over the ns splits, in split order
-  const int r0 = (sp * rows) / ns, r1 = ((sp + 1) * rows) / ns;
+  mbar_wait(rbar, 0, a.status);
   for (int it = threadIdx.x; it < (r1 - r0) * (D / 4); it += blockDim.x) {
     const int lr = it / (D / 4), c4 = it % (D / 4);
     float mmax = -INFINITY;
-    for (int s2 = 0; s2 < ns; ++s2) mmax = fmaxf(mmax, rL[s2 * maxr + lr]);
+    for (int s2 = 0; s2 < ns; ++s2) mmax = fmaxf(mmax, rO[(size_t)(s2 * maxr + lr) * RS + D]);
     float den = 0.f;
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int s2 = 0; s2 < ns; ++s2) {
-      const float w = exp2f(rL[s2 * maxr + lr] - mmax);
-      const float4 ov = *reinterpret_cast<const float4*>(rO + (size_t)(s2 * maxr + lr) * RS + 4 * c4);
+      const float* row = rO + (size_t)(s2 * maxr + lr) * RS;
+      const float w = exp2f(row[D] - mmax);
+      const float4 ov = *reinterpret_cast<const float4*>(row + 4 * c4);
       den += w;
       num.x += w * ov.x;
       num.y += w * ov.y;
@@ -360,7 +449,8 @@ __global__ void __launch_bounds__(320, 1) attn_kernel(const AttnArgs a) {
     dst[0] = __floats2half2_rn(num.x * id, num.y * id);
     dst[1] = __floats2half2_rn(num.z * id, num.w * id);
   }
-  fence_proxy_async_global();  // the o projection reads the output with TMA
+  // the staging area must outlive the copies' reads of it
+  if (warp == 0 && lane < ns) bulk_wait_read_all();
 }
 
 }  // namespace
@@ -404,26 +494,54 @@ static int attn_max_clusters(const void* fn, int ns, int threads, size_t smem) {
   return n;
 }
 
+static int max_smem_optin() {
+  static int cached[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (!cached[dev]) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+      cudaGetLastError();
+      v = 48 * 1024;
+    }
+    cached[dev] = v;
+  }
+  return cached[dev];
+}
+
 cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
   AttnArgs a = a0;
+  if (a.d != 64 && a.d != 128) return cudaErrorInvalidValue;
   const int rows = a.B * (a.nq / a.nkv);
   const int nw = (rows + 15) / 16;
   const int rows_pad = nw * 16;
   a.nwc = nw;
   const int nthr = (2 * nw < 10 ? 2 * nw : (nw > 10 ? nw : 10)) * 32;
-  auto kernel_for = [&](bool kh2) {
-    return a.d == 128 ? (kh2 ? (const void*)attn_kernel<128, 2> : (const void*)attn_kernel<128, 1>)
-                      : (kh2 ? (const void*)attn_kernel<64, 2> : (const void*)attn_kernel<64, 1>);
+  auto kernel_for = [&](bool kh2, int nst) {
+    if (a.d == 128)
+      return nst == 3 ? (kh2 ? (const void*)attn_kernel<128, 2, 3> : (const void*)attn_kernel<128, 1, 3>)
+                      : (kh2 ? (const void*)attn_kernel<128, 2, 2> : (const void*)attn_kernel<128, 1, 2>);
+    return nst == 3 ? (kh2 ? (const void*)attn_kernel<64, 2, 3> : (const void*)attn_kernel<64, 1, 3>)
+                    : (kh2 ? (const void*)attn_kernel<64, 2, 2> : (const void*)attn_kernel<64, 1, 2>);
   };
-  auto smem_for = [&](int n) {
-    // Q, double-buffered K/V, per-row lse, then the merge's receive area
-    size_t b = 128 + (size_t)rows_pad * a.d * 2 + 4 * kKT * a.d * 2 + rows_pad * 4;
+  auto smem_for = [&](int n, int nst) {
+    // 1 KB alignment slack, K/V stages, Q, barriers, then the
+    // merge's receive area (and its staging area, unless that fits in the
+    // K/V stages and Q)
+    const size_t alias = (size_t)2 * nst * kKT * a.d * 2 + (size_t)rows_pad * a.d * 2;
+    size_t b = 1024 + alias + 64;
     if (n > 1) {
       const size_t maxr = (rows + n - 1) / n;
-      b += (size_t)n * maxr * (a.d + 4) * 4 + (size_t)n * maxr * 4;
+      const size_t need = (size_t)n * maxr * (a.d + 4) * 4;
+      b += need;                     // receive area
+      if (need > alias) b += need;   // staging area of its own
     }
     return b;
   };
+  // three stages where they fit (two tiles in flight behind the one being
+  // consumed), else two
+  auto stages_for = [&](int n) { return smem_for(n, 3) <= (size_t)max_smem_optin() ? 3 : 2; };
   // Split count: the longest possible context (capacity plus the block) is
   // cut into ns chunks of whole 64-key tiles, one CTA each, the ns CTAs of a
   // (sequence, kv head) forming one cluster.  Cost model: waves of resident
@@ -433,13 +551,14 @@ cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
   const int total = a.cap + a.B;
   const int ntiles = (total + kKT - 1) / kKT;
   const int need = a.b * a.nkv;  // clusters
-  int ns = 1;
+  int ns = 0;
   long best = -1;
   for (int n = 1; n <= kMaxSplits && n <= ntiles; ++n) {
-    const int per = (ntiles + n - 1) / n;   // tiles per split
+    const int per = (ntiles + n - 1) / n;       // tiles per split
     const int used = (ntiles + per - 1) / per;  // splits that get keys
     if (used != n) continue;
-    const int fit = attn_max_clusters(kernel_for(false), n, nthr, smem_for(n));
+    const int nst = stages_for(n);
+    const int fit = attn_max_clusters(kernel_for(false, nst), n, nthr, smem_for(n, nst));
     if (fit <= 0) continue;
     const long cost = (long)((need + fit - 1) / fit) * per;
     if (best < 0 || cost < best) {
@@ -447,16 +566,27 @@ cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
       ns = n;
     }
   }
+  if (ns == 0) return cudaErrorInvalidConfiguration;  // no split count fits in shared memory
+  const int nst = stages_for(ns);
   const int tiles = (ntiles + ns - 1) / ns;
-  size_t smem = smem_for(ns);
+  const size_t smem = smem_for(ns, nst);
   // helper warps take the second key half of every tile when a split has
   // several tiles (one tile: the extra merge costs more than it saves)
   const bool kh2 = nthr >= 2 * nw * 32 && tiles >= 2;
-  const void* fn = kernel_for(kh2);
+  const void* fn = kernel_for(kh2, nst);
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (ns > kPortable) cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  // the layer's K and V caches as [b nkv cap] rows of d fp16, read in 64 x 64
+  // boxes with 128-byte swizzle
+  CUtensorMap km, vm;
+  const uint64_t crow = (uint64_t)a.b * a.nkv * a.cap;
+  if (!encode_tmap_2d(&km, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.kc, a.d, crow, (uint64_t)a.d * 2, 64, kKT,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !encode_tmap_2d(&vm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.vc, a.d, crow, (uint64_t)a.d * 2, 64, kKT,
+                      CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   dim3 grid(ns, a.nkv, a.b);
-  void* args[] = {&a};
+  void* args[] = {&km, &vm, &a};
   return launch_kc(fn, grid, dim3(nthr), smem, st, pdl, dim3(ns, 1, 1), args);
 }
 
