@@ -61,7 +61,8 @@ __device__ __forceinline__ int kv_off(int r, int ch) {
 
 template <int D, int KH, int NST>
 __global__ void __launch_bounds__(320, 1)
-    attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap, const AttnArgs a) {
+    attn_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                const __grid_constant__ CUtensorMap qmap, const AttnArgs a) {
   constexpr int RB = D * 2;             // bytes per row
   constexpr int KVB = kKT * RB;         // bytes of one K (or V) tile
   extern __shared__ uint8_t smem_raw[];
@@ -74,8 +75,9 @@ __global__ void __launch_bounds__(320, 1)
   const int rows_pad = nwc * 16;
   uint8_t* sK = smem;                   // [NST][KVB], 1024-aligned
   uint8_t* sV = sK + NST * KVB;         // [NST][KVB]
-  uint8_t* sQ = sV + NST * KVB;         // [rows_pad][RB], chunk ch of row r at ch ^ (r % 8)
-  uint64_t* full = reinterpret_cast<uint64_t*>(sQ + rows_pad * RB);  // [NST], receive barrier at [7]
+  uint8_t* sQ = sV + NST * KVB;         // [D / 64][rows_pad][128 bytes], swizzled like a K/V stage
+  // tile barriers [0, NST), the Q barrier at [6], the merge's receive barrier at [7]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sQ + rows_pad * RB);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // The context K/V and its length are inputs of the whole draft pass (no
@@ -100,22 +102,13 @@ __global__ void __launch_bounds__(320, 1)
   // split merge (ns > 1): CTA p of the cluster merges query rows
   // [p rows / ns, (p + 1) rows / ns); every split sends it those rows, counted
   // in bytes on its receive barrier
-  constexpr int RS = D + 4;  // staged row: D partial outputs, then the log-sum-exp
+  // staged row: D fp16 partial outputs, the fp32 log-sum-exp, padding (a
+  // row stride of 2 D + 16 bytes keeps the staging stores conflict-free)
+  constexpr int RSH = D + 8;
   const int maxr = (rows + ns - 1) / ns;
   const int r0 = (sp * rows) / ns, r1 = ((sp + 1) * rows) / ns;
+  uint64_t* qbar = full + 6;
   uint64_t* rbar = full + 7;
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < NST; ++i) mbar_init(&full[i], 1);
-    if (ns > 1) {
-      mbar_init(rbar, 1);
-      mbar_arrive_expect_tx(rbar, (uint32_t)(ns * (r1 - r0) * RS * 4));
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-  // peers may target this CTA's receive barrier once they have passed the
-  // matching wait (after their main loop)
-  if (ns > 1) cluster_arrive();
   auto issue_tma = [&](int i, int stg) {  // thread 0 only
     fence_proxy_async_shared();  // the stage may last have been written by cp.async
     mbar_arrive_expect_tx(&full[stg], 2 * KVB);
@@ -156,11 +149,23 @@ __global__ void __launch_bounds__(320, 1)
   // prologue: tiles 0 .. NST-2; the context part before the wait
   constexpr int PRE = NST - 1;
   if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) mbar_init(&full[i], 1);
+    mbar_init(qbar, 1);
+    if (ns > 1) {
+      mbar_init(rbar, 1);
+      mbar_arrive_expect_tx(rbar, (uint32_t)(ns * (r1 - r0) * RSH * 2));
+    }
+    fence_mbar_init();
     prefetch_tmap(&kmap);
     prefetch_tmap(&vmap);
+    prefetch_tmap(&qmap);
     for (int i = 0; i < PRE && i < ntile; ++i)
       if (is_tma(i)) issue_tma(i, i);
   }
+  __syncthreads();  // the barriers are initialised
+  // peers may target this CTA's receive barrier once they have passed the
+  // matching wait (after their main loop)
+  if (ns > 1) cluster_arrive_relaxed();
   for (int i = 0; i < PRE && i < ntile; ++i)
     if (!is_tma(i)) load_rows(i, k0 + i * kKT, 0);
   if (a.pf_base && threadIdx.x == 0)
@@ -168,19 +173,18 @@ __global__ void __launch_bounds__(320, 1)
                     blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z), gridDim.x * gridDim.y * gridDim.z);
   pdl_wait();
 
-  // ---- Q tile: row rho = tok * grp + hh  ->  q[(j B + tok)][g grp + hh][:]
-  for (int c = threadIdx.x; c < rows_pad * (D / 8); c += blockDim.x) {
-    int rho = c / (D / 8), ch = c % (D / 8);
-    bool ok = rho < rows;
-    const __half* src = a.q;
-    if (ok) {
-      int tok = rho / grp, hh = rho - tok * grp;
-      src = a.q + ((size_t)(j * a.B + tok) * a.nq + (g * grp + hh)) * D + ch * 8;
-    }
-    cp_async16(sQ + rho * RB + ((ch ^ (rho & 7)) << 4), src, ok);
+  // ---- Q tile: row rho = tok * grp + hh is q[(j B + tok)][g grp + hh][:],
+  // one tensor-map box (64 columns x grp heads x B tokens) per 64 columns;
+  // rows past `rows` stay unwritten and are never stored
+  if (threadIdx.x == 0) {
+    // q was written by the preceding kernel with generic stores
+    fence_proxy_async_global();
+    mbar_arrive_expect_tx(qbar, (uint32_t)((D / 64) * rows * 128));
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) tma_load_3d(sQ + h * rows_pad * 128, &qmap, h * 64, g * grp, j * a.B, qbar);
   }
-  // one cp.async group per prologue tile (group 0 also holds Q and every
-  // context part issued above: waiting for it early is only conservative)
+  // one cp.async group per prologue tile (group 0 also holds every context
+  // part issued above: waiting for it early is only conservative)
   for (int i = 0; i < PRE; ++i) {
     if (i < ntile && !is_tma(i)) load_rows(i, k0 + i * kKT, 1);
     cp_async_commit();
@@ -228,12 +232,14 @@ __global__ void __launch_bounds__(320, 1)
     __syncthreads();
     if (cw) {
       if (it == 0) {
+        mbar_wait(qbar, 0, a.status);
         const uint32_t qb = smem_u32(sQ);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          int row = rb * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-          int ch = 2 * ks + (lane >> 4);
-          ldsm_x4(qb + row * RB + ((ch ^ (row & 7)) << 4), qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3]);
+          const int row = rb * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          const int ch = 2 * ks + (lane >> 4);
+          ldsm_x4(qb + (ch >> 3) * rows_pad * 128 + row * 128 + (((ch & 7) ^ (row & 7)) << 4), qf[ks][0], qf[ks][1],
+                  qf[ks][2], qf[ks][3]);
         }
       }
       const uint32_t kb = smem_u32(sK + stg * KVB);
@@ -325,6 +331,7 @@ __global__ void __launch_bounds__(320, 1)
     stg = stg + 1 == NST ? 0 : stg + 1;
   }
   cp_async_wait<0>();  // empty trailing groups, and zero-fill copies of an empty split
+  if (threadIdx.x == 0) mbar_wait(qbar, 0, a.status);  // Q landed even where no tile was computed
   if (KH == 2) {
     // merge the key halves of each row block: half 1 hands (max, sum, O) over
     // through shared memory (the K/V stages are free once the last tile is
@@ -394,10 +401,10 @@ __global__ void __launch_bounds__(320, 1)
   // shared memory grouped by owner, then hand each owner its group with one
   // bulk shared-to-shared::cluster copy.  The staging area reuses the K/V
   // stages and Q (no longer read) when it fits there.
-  float* rO = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 64);  // receive [ns][maxr][RS]
-  const size_t need = (size_t)ns * maxr * RS * 4;
-  float* sst = need <= (size_t)2 * NST * KVB + (size_t)rows_pad * RB ? reinterpret_cast<float*>(sK)
-                                                                      : rO + (size_t)ns * maxr * RS;
+  __half* rO = reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(full) + 64);  // receive [ns][maxr][RSH]
+  const size_t need = (size_t)ns * maxr * RSH * 2;
+  __half* sst = need <= (size_t)2 * NST * KVB + (size_t)rows_pad * RB ? reinterpret_cast<__half*>(sK)
+                                                                      : rO + (size_t)ns * maxr * RSH;
   cluster_wait();   // every peer's receive barrier is initialised and armed
   __syncthreads();  // nothing reads the K/V stages, Q or the key-half scratch any more
 #pragma unroll
@@ -407,11 +414,12 @@ __global__ void __launch_bounds__(320, 1)
     if (rho >= rows) continue;
     const int own = ((rho + 1) * ns - 1) / rows;
     const int lr = rho - (own * rows) / ns;
-    float* dst = sst + (size_t)(own * maxr + lr) * RS + 2 * t4;
+    __half* row = sst + (size_t)(own * maxr + lr) * RSH;
 #pragma unroll
     for (int i = 0; i < D / 8; ++i)
-      *reinterpret_cast<float2*>(dst + i * 8) = make_float2(o[i][2 * h] * inv[h], o[i][2 * h + 1] * inv[h]);
-    if (t4 == 0) sst[(size_t)(own * maxr + lr) * RS + D] = lse[h];
+      *reinterpret_cast<__half2*>(row + i * 8 + 2 * t4) =
+          __floats2half2_rn(o[i][2 * h] * inv[h], o[i][2 * h + 1] * inv[h]);
+    if (t4 == 0) *reinterpret_cast<float*>(row + D) = lse[h];
   }
   fence_proxy_async_shared();  // each writer: the staged rows are visible to the bulk copies
   __syncthreads();
@@ -419,29 +427,43 @@ __global__ void __launch_bounds__(320, 1)
     const int p = lane;
     const int nr = ((p + 1) * rows) / ns - (p * rows) / ns;
     if (nr > 0)
-      bulk_s2cluster(dsmem_addr(smem_u32(rO + (size_t)sp * maxr * RS), (uint32_t)p),
-                     smem_u32(sst + (size_t)p * maxr * RS), (uint32_t)(nr * RS * 4),
+      bulk_s2cluster(dsmem_addr(smem_u32(rO + (size_t)sp * maxr * RSH), (uint32_t)p),
+                     smem_u32(sst + (size_t)p * maxr * RSH), (uint32_t)(nr * RSH * 2),
                      dsmem_addr(smem_u32(rbar), (uint32_t)p));
     bulk_commit();
   }
-  // merge the owned rows over the ns splits, in split order
+  // merge the owned rows over the ns splits, in split order; every load of
+  // an item is issued before its arithmetic
   mbar_wait(rbar, 0, a.status);
   for (int it = threadIdx.x; it < (r1 - r0) * (D / 4); it += blockDim.x) {
     const int lr = it / (D / 4), c4 = it % (D / 4);
+    float lv[kMaxSplits];
+    uint2 pv[kMaxSplits];
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxSplits; ++s2)
+      if (s2 < ns) {
+        const __half* row = rO + (size_t)(s2 * maxr + lr) * RSH;
+        lv[s2] = *reinterpret_cast<const float*>(row + D);
+        pv[s2] = *reinterpret_cast<const uint2*>(row + 4 * c4);
+      }
     float mmax = -INFINITY;
-    for (int s2 = 0; s2 < ns; ++s2) mmax = fmaxf(mmax, rO[(size_t)(s2 * maxr + lr) * RS + D]);
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxSplits; ++s2)
+      if (s2 < ns) mmax = fmaxf(mmax, lv[s2]);
     float den = 0.f;
     float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s2 = 0; s2 < ns; ++s2) {
-      const float* row = rO + (size_t)(s2 * maxr + lr) * RS;
-      const float w = exp2f(row[D] - mmax);
-      const float4 ov = *reinterpret_cast<const float4*>(row + 4 * c4);
-      den += w;
-      num.x += w * ov.x;
-      num.y += w * ov.y;
-      num.z += w * ov.z;
-      num.w += w * ov.w;
-    }
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxSplits; ++s2)
+      if (s2 < ns) {
+        const float w = ex2(lv[s2] - mmax);
+        const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&pv[s2].x));
+        const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&pv[s2].y));
+        den += w;
+        num.x += w * lo.x;
+        num.y += w * lo.y;
+        num.z += w * hi.x;
+        num.w += w * hi.y;
+      }
     const float id = 1.f / den;
     const int rho = r0 + lr;
     int tok = rho / grp, hh = rho - tok * grp;
@@ -533,7 +555,7 @@ cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
     size_t b = 1024 + alias + 64;
     if (n > 1) {
       const size_t maxr = (rows + n - 1) / n;
-      const size_t need = (size_t)n * maxr * (a.d + 4) * 4;
+      const size_t need = (size_t)n * maxr * (a.d + 8) * 2;
       b += need;                     // receive area
       if (need > alias) b += need;   // staging area of its own
     }
@@ -585,8 +607,17 @@ cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
       !encode_tmap_2d(&vm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.vc, a.d, crow, (uint64_t)a.d * 2, 64, kKT,
                       CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
+  // q [b B tokens][nq heads][d]: one box = 64 columns of the grp heads of a kv
+  // head for the B tokens of a sequence (query rows in tok * grp + hh order)
+  CUtensorMap qm;
+  const uint64_t qdims[3] = {(uint64_t)a.d, (uint64_t)a.nq, (uint64_t)a.b * a.B};
+  const uint64_t qstr[2] = {(uint64_t)a.d * 2, (uint64_t)a.nq * a.d * 2};
+  const uint32_t qbox[3] = {64, (uint32_t)(a.nq / a.nkv), (uint32_t)a.B};
+  if (a.B > 256 || a.nq / a.nkv > 256 ||
+      !encode_tmap_3d(&qm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.q, qdims, qstr, qbox, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   dim3 grid(ns, a.nkv, a.b);
-  void* args[] = {&km, &vm, &a};
+  void* args[] = {&km, &vm, &qm, &a};
   return launch_kc(fn, grid, dim3(nthr), smem, st, pdl, dim3(ns, 1, 1), args);
 }
 

@@ -601,11 +601,14 @@ __global__ void __launch_bounds__(kThreads, 1) wmma_gemm_kernel(const __grid_con
 }
 
 // ---------------------------------------------------- int8, tcgen05 ----
-constexpr int kTcThreads = 6 * 32;  // 4 converter warps, 1 producer, 1 MMA warp
-constexpr int kTcProducer = 4;
-constexpr int kTcMma = 5;
-constexpr uint32_t kTmemCols = 256;  // accumulator [0, 128), A buffers [128, 192), [192, 256)
-constexpr uint32_t kTmemA = 128;
+// Eight converter warps in two groups of four (group g converts the k-tiles
+// i with i % 2 == g; warp w reaches tensor-memory lanes 32 (w % 4) ..), then
+// the producer warp and the MMA warp.
+constexpr int kTcConv = 8;
+constexpr int kTcProducer = kTcConv;
+constexpr int kTcMma = kTcConv + 1;
+constexpr int kTcThreads = (kTcConv + 2) * 32;
+constexpr uint32_t kTmemCols = 256;  // per CTA: two CTAs share an SM's 512 columns
 
 template <int MT>
 struct TcGeo {
@@ -618,7 +621,15 @@ struct TcGeo {
   static constexpr int TX = WBYTES + ABYTES;
   static constexpr int TBYTES = (MCH * kTStride * 4 + 1023) / 1024 * 1024;
   static_assert(2 * TBYTES <= NST * STAGE, "epilogue tiles must fit in the ring");
-  static constexpr int NBAR = 2 * NST + 5;  // full, empty, afull[2], afree[2], dfull
+  // tensor memory: accumulator in columns [0, MCH), then NAB A buffers of 64
+  // columns (one k-tile of fp16 pairs) from column TA
+  static constexpr int NAB = MCH <= 64 ? 3 : 2;
+  static constexpr uint32_t TA = MCH <= 64 ? 64 : 128;
+  static_assert(TA + 64 * NAB <= kTmemCols, "tensor-memory columns");
+  static_assert(NST >= NAB, "a ring slot is reused no sooner than an A buffer (converter wait order)");
+  static constexpr int MINB = MT == 16 ? 1 : 2;  // resident CTAs per SM
+  // wfull, xfull, wempty, xempty per stage; afull, afree per A buffer; dfull
+  static constexpr int NBAR = 4 * NST + 2 * NAB + 1;
   static constexpr int SIDE = 128 * 4 + 128 * 4 + 128 * 4 + MCH * 4 + MCH * 4;
   static constexpr size_t SMEM = 1024 + NST * (size_t)STAGE + NBAR * 8 + 16 + SIDE;
   // two CTAs per SM up to 64 rows (tensor memory: 2 x 256 of 512 columns)
@@ -637,8 +648,8 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-// Named barrier over the converter warps and the MMA warp (160 threads).
-__device__ __forceinline__ void tc_bar() { asm volatile("bar.sync 1, 160;" ::: "memory"); }
+// Named barrier over the converter warps and the MMA warp.
+__device__ __forceinline__ void tc_bar() { asm volatile("bar.sync 1, %0;" ::"n"((kTcConv + 1) * 32) : "memory"); }
 
 // 32 consecutive tensor-memory columns of this warp's 32 lanes (thread t:
 // lane base + t) from / to registers.
@@ -693,16 +704,22 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kTcThreads, 1) w8_gemm_kernel(const __grid_constant__ CUtensorMap xmap,
+__global__ void __launch_bounds__(kTcThreads, TcGeo<MT>::MINB) w8_gemm_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                  const W8Args a) {
   using G = TcGeo<MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + G::NST * G::STAGE);
-  uint64_t* empty = full + G::NST;  // 4 converter warps + 1 MMA commit
-  uint64_t* afull = empty + G::NST;  // [2]: A buffer stored (4 converter warps)
-  uint64_t* afree = afull + 2;       // [2]: A buffer's MMAs done (commit)
-  uint64_t* dfull = afree + 2;       // accumulator complete (commit)
+  // A ring stage holds a weight tile and the activation tile it meets; the
+  // two halves are filled and released separately: the weights as soon as
+  // the converter group has read them, the activations when the MMAs that
+  // read them have completed
+  uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + G::NST * G::STAGE);
+  uint64_t* xfull = wfull + G::NST;
+  uint64_t* wempty = xfull + G::NST;   // the converter group's 4 warps
+  uint64_t* xempty = wempty + G::NST;  // 1 MMA commit
+  uint64_t* afull = xempty + G::NST;   // [NAB]: A buffer stored (4 converter warps)
+  uint64_t* afree = afull + G::NAB;    // [NAB]: A buffer's MMAs done (commit)
+  uint64_t* dfull = afree + G::NAB;    // accumulator complete (commit)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(dfull + 1);
   float* s_sc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s_tmem) + 16);  // [128]
   float* s_gam = s_sc + 128;                                                          // [128]
@@ -734,10 +751,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) w8_gemm_kernel(const __grid_con
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < G::NST; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 5);
+      mbar_init(&wfull[i], 1);
+      mbar_init(&xfull[i], 1);
+      mbar_init(&wempty[i], 4);
+      mbar_init(&xempty[i], 1);
     }
-    for (int j = 0; j < 2; ++j) {
+    for (int j = 0; j < G::NAB; ++j) {
       mbar_init(&afull[j], 4);
       mbar_init(&afree[j], 1);
     }
@@ -747,33 +766,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) w8_gemm_kernel(const __grid_con
   __syncthreads();
 
   if (warp == kTcProducer) {
-    // ---------------- producer ----------------
+    // ---------------- producer: lane 0 weights, lane 1 activations ----------------
     if (lane == 0) {
-      prefetch_tmap(&xmap);
       const uint8_t* wsrc = wq + ((size_t)((a.row0 >> 7) + nt) * KT + kt0) * G::WBYTES;
       const uint64_t pol = policy_evict_first();
-      const int pre = nk < G::NST ? nk : G::NST;
-      for (int i = 0; i < pre; ++i) {
-        mbar_arrive_expect_tx(&full[i], G::TX);
-        bulk_g2s_hint(smem + i * G::STAGE, wsrc + (size_t)i * G::WBYTES, G::WBYTES, &full[i], pol);
+      for (int i = 0; i < nk; ++i) {
+        const int slot = i % G::NST;
+        if (i >= G::NST && !mbar_wait(&wempty[slot], ((i / G::NST) - 1) & 1, a.status)) break;
+        mbar_arrive_expect_tx(&wfull[slot], G::WBYTES);
+        bulk_g2s_hint(smem + slot * G::STAGE, wsrc + (size_t)i * G::WBYTES, G::WBYTES, &wfull[slot], pol);
       }
+    } else if (lane == 1) {
+      prefetch_tmap(&xmap);
       pdl_wait();
       // the activations were written by the previous kernel with generic
       // stores; order this thread's tensor (async-proxy) reads after them
       fence_proxy_async_global();
-      for (int i = 0; i < pre; ++i) {
-        uint8_t* sa = smem + i * G::STAGE + G::WBYTES;
-        tma_load_2d(sa, &xmap, (kt0 + i) * kTile, z * G::MCH, &full[i]);
-        tma_load_2d(sa + G::MCH * 128, &xmap, (kt0 + i) * kTile + 64, z * G::MCH, &full[i]);
-      }
-      for (int i = pre; i < nk; ++i) {
+      for (int i = 0; i < nk; ++i) {
         const int slot = i % G::NST;
-        if (!mbar_wait(&empty[slot], ((i / G::NST) - 1) & 1, a.status)) break;
-        mbar_arrive_expect_tx(&full[slot], G::TX);
-        uint8_t* st = smem + slot * G::STAGE;
-        bulk_g2s_hint(st, wsrc + (size_t)i * G::WBYTES, G::WBYTES, &full[slot], pol);
-        tma_load_2d(st + G::WBYTES, &xmap, (kt0 + i) * kTile, z * G::MCH, &full[slot]);
-        tma_load_2d(st + G::WBYTES + G::MCH * 128, &xmap, (kt0 + i) * kTile + 64, z * G::MCH, &full[slot]);
+        if (i >= G::NST && !mbar_wait(&xempty[slot], ((i / G::NST) - 1) & 1, a.status)) break;
+        mbar_arrive_expect_tx(&xfull[slot], G::ABYTES);
+        uint8_t* sa = smem + slot * G::STAGE + G::WBYTES;
+        tma_load_2d(sa, &xmap, (kt0 + i) * kTile, z * G::MCH, &xfull[slot]);
+        tma_load_2d(sa + G::MCH * 128, &xmap, (kt0 + i) * kTile + 64, z * G::MCH, &xfull[slot]);
       }
     }
     pdl_trigger();
@@ -843,68 +858,82 @@ __global__ void __launch_bounds__(kTcThreads, 1) w8_gemm_kernel(const __grid_con
         }
         s_pos[t] = p;
       }
-      // ---- converter: weight row r of each stage -> fp16 pairs in tensor memory
-      const int r = warp * 32 + lane;
-      const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-      for (int i = 0; i < nk; ++i) {
-        const int slot = i % G::NST, ab = i & 1;
-        if (!mbar_wait(&full[slot], (i / G::NST) & 1, a.status)) break;
-        if (i >= 2 && !mbar_wait(&afree[ab], ((i >> 1) - 1) & 1, a.status)) break;
+    }
+    if (warp < kTcConv) {
+      // ---- converter: weight row r of each of this group's k-tiles -> fp16
+      // pairs in tensor memory
+      const int grp = warp >> 2;
+      const int r = (warp & 3) * 32 + lane;
+      const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+      for (int i = grp; i < nk; i += 2) {
+        const int slot = i % G::NST, ab = i % G::NAB;
+        // A buffer first: the MMAs of tile i - NAB (and, in order, of every
+        // earlier tile) being done means the tile that last used this ring
+        // slot (i - NST, NST >= NAB, possibly the other group's) has landed,
+        // so the slot's phase parity below cannot be one phase stale
+        if (i >= G::NAB && !mbar_wait(&afree[ab], ((i / G::NAB) - 1) & 1, a.status)) break;
+        if (!mbar_wait(&wfull[slot], (i / G::NST) & 1, a.status)) break;
         const uint8_t* wrow = smem + slot * G::STAGE + r * 128;
-        const uint32_t ta = tmem + lane_base + kTmemA + 64 * ab;
+        const uint32_t ta = tmem + lane_base + G::TA + 64 * ab;
+        uint4 v[8];  // this thread's 128 weight bytes of the tile
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) v[cc] = *reinterpret_cast<const uint4*>(wrow + ((cc ^ (r & 7)) << 4));
+        // the weight half of the slot can be refilled once every lane has read it
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&wempty[slot]);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t words[32];
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            const int cc = 4 * h + c;  // logical 16-column group
             // chunk word t holds columns (2t, 2t+1, 2t+8, 2t+9): fp16 pairs t and t + 4
-            const uint4 v = *reinterpret_cast<const uint4*>(wrow + ((cc ^ (r & 7)) << 4));
-            biased_u8x4_to_half2x2(v.x, words[8 * c + 0], words[8 * c + 4]);
-            biased_u8x4_to_half2x2(v.y, words[8 * c + 1], words[8 * c + 5]);
-            biased_u8x4_to_half2x2(v.z, words[8 * c + 2], words[8 * c + 6]);
-            biased_u8x4_to_half2x2(v.w, words[8 * c + 3], words[8 * c + 7]);
+            const uint4 u = v[4 * h + c];
+            biased_u8x4_to_half2x2(u.x, words[8 * c + 0], words[8 * c + 4]);
+            biased_u8x4_to_half2x2(u.y, words[8 * c + 1], words[8 * c + 5]);
+            biased_u8x4_to_half2x2(u.z, words[8 * c + 2], words[8 * c + 6]);
+            biased_u8x4_to_half2x2(u.w, words[8 * c + 3], words[8 * c + 7]);
           }
           tmem_st32(ta + 32 * h, words);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&empty[slot]);
-          mbar_arrive(&afull[ab]);
-        }
+        if (lane == 0) mbar_arrive(&afull[ab]);
       }
       pdl_trigger();
-      // ---- accumulator -> P[tok][kTStride] (this thread: weight row r)
+      // ---- accumulator -> P[tok][kTStride] (this thread: weight row r); the
+      // two groups take halves of the columns (one group when MCH = 16)
       mbar_wait(dfull, 0, a.status);
       tc_fence_after();
       float* P = reinterpret_cast<float*>(smem);
       const uint32_t td = tmem + lane_base;
+      constexpr int CW = G::MCH >= 32 ? G::MCH / 2 : G::MCH;
+      if (G::MCH >= 32 || grp == 0) {
 #pragma unroll
-      for (int c0 = 0; c0 < G::MCH; c0 += 16) {
-        uint32_t v[16];
-        tmem_ld16(td + c0, v);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        for (int c0 = grp * CW; c0 < grp * CW + CW; c0 += 16) {
+          uint32_t v[16];
+          tmem_ld16(td + c0, v);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-        for (int j = 0; j < 16; ++j) P[(c0 + j) * kTStride + r] = __uint_as_float(v[j]);
+          for (int j = 0; j < 16; ++j) P[(c0 + j) * kTStride + r] = __uint_as_float(v[j]);
+        }
       }
     } else if (warp == kTcMma && lane == 0) {
       // ---------------- MMA issuer ----------------
       constexpr uint32_t idesc = tc_idesc_f16(G::MCH);
       for (int i = 0; i < nk; ++i) {
-        const int slot = i % G::NST, ab = i & 1;
-        if (!mbar_wait(&afull[ab], (i >> 1) & 1, a.status)) break;
-        if (!mbar_wait(&full[slot], (i / G::NST) & 1, a.status)) break;
+        const int slot = i % G::NST, ab = i % G::NAB;
+        if (!mbar_wait(&afull[ab], (i / G::NAB) & 1, a.status)) break;
+        if (!mbar_wait(&xfull[slot], (i / G::NST) & 1, a.status)) break;
         tc_fence_after();
         const uint32_t act = smem_u32(smem + slot * G::STAGE + G::WBYTES);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint64_t bdesc = tc_sdesc_sw128(act + (ks >> 2) * (G::MCH * 128) + (ks & 3) * 32);
-          tc_mma_f16_ta(tmem, tmem + kTmemA + 64 * ab + 8 * ks, bdesc, idesc, (i | ks) != 0);
+          tc_mma_f16_ta(tmem, tmem + G::TA + 64 * ab + 8 * ks, bdesc, idesc, (i | ks) != 0);
         }
         tc_commit(&afree[ab]);
-        tc_commit(&empty[slot]);
+        tc_commit(&xempty[slot]);
       }
       tc_commit(dfull);
     }

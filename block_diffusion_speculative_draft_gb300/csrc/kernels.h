@@ -99,6 +99,9 @@ struct W8Args {
 // Tensor-map encoder of the CUDA driver API (resolved once through the runtime).
 bool encode_tmap_2d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                     uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz);
+// Same for a 3-D tensor: dims innermost first, strides (bytes) of dims 1 and 2.
+bool encode_tmap_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, const uint64_t dims[3],
+                    const uint64_t strides[2], const uint32_t box[3], CUtensorMapSwizzle swz);
 
 // Launch helpers: the programmatic-dependent-launch attribute is set when
 // `pdl` is requested and the library's launch mode allows early launches
