@@ -601,10 +601,14 @@ __global__ void __launch_bounds__(kThreads, 1) wmma_gemm_kernel(const __grid_con
 }
 
 // ---------------------------------------------------- int8, tcgen05 ----
-// Eight converter warps in two groups of four (group g converts the k-tiles
-// i with i % 2 == g; warp w reaches tensor-memory lanes 32 (w % 4) ..), then
-// the producer warp and the MMA warp.
-constexpr int kTcConv = 8;
+// Converter warps in groups of four (warp w reaches tensor-memory lanes
+// 32 (w % 4) ..; with G groups, group g converts the k-tiles i with
+// i % G == g), then the producer warp and the MMA warp.  One group: six warps
+// a CTA keep two CTAs on an SM within each sub-partition's register file
+// (ten warps do not: three of them on one sub-partition, twice, is too many),
+// and one group converts faster than the single MMA thread consumes.
+constexpr int kTcConv = 4;
+constexpr int kTcGroups = kTcConv / 4;
 constexpr int kTcProducer = kTcConv;
 constexpr int kTcMma = kTcConv + 1;
 constexpr int kTcThreads = (kTcConv + 2) * 32;
@@ -865,7 +869,7 @@ __global__ void __launch_bounds__(kTcThreads, TcGeo<MT>::MINB) w8_gemm_kernel(co
       const int grp = warp >> 2;
       const int r = (warp & 3) * 32 + lane;
       const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-      for (int i = grp; i < nk; i += 2) {
+      for (int i = grp; i < nk; i += kTcGroups) {
         const int slot = i % G::NST, ab = i % G::NAB;
         // A buffer first: the MMAs of tile i - NAB (and, in order, of every
         // earlier tile) being done means the tile that last used this ring
@@ -898,17 +902,23 @@ __global__ void __launch_bounds__(kTcThreads, TcGeo<MT>::MINB) w8_gemm_kernel(co
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&afull[ab]);
+        // the tile's activations must have landed too: waiting here keeps that
+        // wait off the single MMA-issuing thread
+        if (lane == 0) {
+          mbar_wait(&xfull[slot], (i / G::NST) & 1, a.status);
+          mbar_arrive(&afull[ab]);
+        }
       }
       pdl_trigger();
-      // ---- accumulator -> P[tok][kTStride] (this thread: weight row r); the
-      // two groups take halves of the columns (one group when MCH = 16)
+      // ---- accumulator -> P[tok][kTStride] (this thread: weight row r); two
+      // groups take halves of the columns (one group when MCH = 16)
       mbar_wait(dfull, 0, a.status);
       tc_fence_after();
       float* P = reinterpret_cast<float*>(smem);
       const uint32_t td = tmem + lane_base;
-      constexpr int CW = G::MCH >= 32 ? G::MCH / 2 : G::MCH;
-      if (G::MCH >= 32 || grp == 0) {
+      constexpr bool kHalves = kTcGroups == 2 && G::MCH >= 32;
+      constexpr int CW = kHalves ? G::MCH / 2 : G::MCH;
+      if (kHalves || grp == 0) {
 #pragma unroll
         for (int c0 = grp * CW; c0 < grp * CW + CW; c0 += 16) {
           uint32_t v[16];
@@ -923,8 +933,8 @@ __global__ void __launch_bounds__(kTcThreads, TcGeo<MT>::MINB) w8_gemm_kernel(co
       constexpr uint32_t idesc = tc_idesc_f16(G::MCH);
       for (int i = 0; i < nk; ++i) {
         const int slot = i % G::NST, ab = i % G::NAB;
+        // afull: the A buffer is stored and the stage's activations have landed
         if (!mbar_wait(&afull[ab], (i / G::NAB) & 1, a.status)) break;
-        if (!mbar_wait(&xfull[slot], (i / G::NST) & 1, a.status)) break;
         tc_fence_after();
         const uint32_t act = smem_u32(smem + slot * G::STAGE + G::WBYTES);
 #pragma unroll
