@@ -49,8 +49,10 @@ FALLBACK_HBM_GBS = 6800.0
 # the shape, so traffic scales with the algorithmic bytes).  Keyed by a hash
 # of the kernel's source file: reported null once that source has changed.
 NCU_TRAFFIC = {
-    "w8_gemm_kernel": {"ratio": 152.236 / 152.54, "src": "7274955ab357101f",
-                       "capture": "profiles/w8_gemm_kernel_qwen3-4b.md"},
+    # DRAM read + write over algorithmic bytes, four launches of the 32-row
+    # projection kernel on the 27B-class shapes (two fc, two K/V commits)
+    "wmma_gemm_kernel": {"ratio": 377.436 / 374.928, "src": "a4e91caa19d287f3",
+                         "capture": "profiles/wmma_gemm_kernel_27b-class.md"},
     "lmhead_kernel": {"ratio": 781.06 / 777.99, "src": "e87431f2ece8f763",
                       "capture": "profiles/lmhead_kernel_qwen3-4b.md"},
 }
@@ -489,7 +491,7 @@ def run_ours(args, rank, world, local_rank):
     lm_gbs = lm_bytes / (statistics.mean(lm_ms) * 1e-3) / 1e9
     proj_avg_ms = statistics.mean(proj_ms) / len(mats)
     proj_gbs = proj_bytes / (statistics.mean(proj_ms) * 1e-3) / 1e9
-    traffic = traffic_for("w8_gemm_kernel", "k_gemm_w8.cu", proj_bytes / len(mats))
+    traffic = traffic_for("wmma_gemm_kernel", "k_gemm_w8.cu", proj_bytes / len(mats))
     traffic_lm = traffic_for("lmhead_kernel", "k_lmhead.cu", lm_bytes)
     sweep_out = {}
     for label, lens in sweep:
@@ -522,8 +524,8 @@ def run_ours(args, rank, world, local_rank):
         "draft_verify_overlap": overlap,
         "verify_accept_blocks_per_s": b / (statistics.median(ver_ms) / VREP / 1e3),
         "verify_sample_blocks_per_s": b / (statistics.median(smp_ms) / VREP / 1e3),
-        "roofline": {"kernel": f"w8_gemm_kernel: the {len(mats)} layer projections of one draft step, launched "
-                               "back to back alone", "bound": "hbm", "achieved": proj_gbs, "peak": hbm,
+        "roofline": {"kernel": f"wmma_gemm_kernel (W8A16 projection, {cfg.M} rows): the {len(mats)} layer "
+                               "projections of one draft step, launched back to back alone", "bound": "hbm", "achieved": proj_gbs, "peak": hbm,
                      "unit": "GB/s", "frac": proj_gbs / hbm, "traffic": traffic, "peak_kind": peak_kind,
                      "algorithmic_bytes_per_launch": proj_bytes / len(mats), "avg_launch_us": proj_avg_ms * 1e3},
         "roofline_lmhead": {"kernel": "lmhead_kernel (bf16 GEMV + fused argmax), alone", "bound": "hbm",
