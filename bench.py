@@ -51,7 +51,7 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # DRAM read + write over algorithmic bytes, four launches of the 32-row
     # projection kernel on the 27B-class shapes (two fc, two K/V commits)
-    "wmma_gemm_kernel": {"ratio": 377.436 / 374.928, "src": "a4e91caa19d287f3",
+    "wmma_gemm_kernel": {"ratio": 377.436 / 374.928, "src": "7db04118a83def87",
                          "capture": "profiles/wmma_gemm_kernel_27b-class.md"},
     "lmhead_kernel": {"ratio": 781.06 / 777.99, "src": "e87431f2ece8f763",
                       "capture": "profiles/lmhead_kernel_qwen3-4b.md"},

@@ -612,7 +612,11 @@ constexpr int kTcGroups = kTcConv / 4;
 constexpr int kTcProducer = kTcConv;
 constexpr int kTcMma = kTcConv + 1;
 constexpr int kTcThreads = (kTcConv + 2) * 32;
-constexpr uint32_t kTmemCols = 256;  // per CTA: two CTAs share an SM's 512 columns
+// Tensor-memory columns per CTA.  A kernel that allocates tensor memory runs
+// one CTA per SM (the occupancy calculator reports one block per SM for any
+// such kernel, whatever its resources), so this is not shared with a second
+// CTA of the same launch.
+constexpr uint32_t kTmemCols = 256;
 
 template <int MT>
 struct TcGeo {
@@ -631,14 +635,11 @@ struct TcGeo {
   static constexpr uint32_t TA = MCH <= 64 ? 64 : 128;
   static_assert(TA + 64 * NAB <= kTmemCols, "tensor-memory columns");
   static_assert(NST >= NAB, "a ring slot is reused no sooner than an A buffer (converter wait order)");
-  static constexpr int MINB = MT == 16 ? 1 : 2;  // resident CTAs per SM
   // wfull, xfull, wempty, xempty per stage; afull, afree per A buffer; dfull
   static constexpr int NBAR = 4 * NST + 2 * NAB + 1;
   static constexpr int SIDE = 128 * 4 + 128 * 4 + 128 * 4 + MCH * 4 + MCH * 4;
   static constexpr size_t SMEM = 1024 + NST * (size_t)STAGE + NBAR * 8 + 16 + SIDE;
-  // two CTAs per SM up to 64 rows (tensor memory: 2 x 256 of 512 columns)
-  static_assert(MT == 16 || SMEM <= 112 * 1024, "two CTAs per SM");
-  static_assert(SMEM <= 227 * 1024, "one CTA per SM");
+  static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
 };
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -708,7 +709,7 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
 }
 
 template <int MT>
-__global__ void __launch_bounds__(kTcThreads, TcGeo<MT>::MINB) w8_gemm_kernel(const __grid_constant__ CUtensorMap xmap,
+__global__ void __launch_bounds__(kTcThreads, 1) w8_gemm_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                  const W8Args a) {
   using G = TcGeo<MT>;
   extern __shared__ uint8_t smem_raw[];
@@ -1097,7 +1098,9 @@ __global__ void pack4_q_kernel(const void* w, int64_t N, int64_t K, int layout, 
 int w8_pick_splits(int units, int KT) {
   // enough CTAs for two per SM, at most one cluster of 8 splits, and at
   // least two 128-column k-tiles per split
-  int target = 2 * num_sms();  // one wave at two CTAs per SM
+  // one wave at two CTAs per SM (the warp-level kernel; for the tensor-memory
+  // kernel, one CTA per SM, the resident-cluster check that follows lowers it)
+  int target = 2 * num_sms();
   int s = target / units;
   int smax = KT >= 4 ? KT / 2 : 1;
   if (s > smax) s = smax;
