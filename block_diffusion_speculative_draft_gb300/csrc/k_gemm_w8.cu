@@ -612,31 +612,38 @@ constexpr int kTcGroups = kTcConv / 4;
 constexpr int kTcProducer = kTcConv;
 constexpr int kTcMma = kTcConv + 1;
 constexpr int kTcThreads = (kTcConv + 2) * 32;
-// Tensor-memory columns per CTA.  A kernel that allocates tensor memory runs
-// one CTA per SM (the occupancy calculator reports one block per SM for any
-// such kernel, whatever its resources), so this is not shared with a second
-// CTA of the same launch.
-constexpr uint32_t kTmemCols = 256;
+// Projections of at least this many weight bytes run on the tensor-memory
+// kernel from 17 activation rows (measured per shape: it wins for the 27B
+// gate|up, down and fc and the Qwen3-4B gate|up at 32 rows, ties the 27B QKV
+// and loses the smaller ones).
+constexpr int64_t kTcMinWeightBytes = 40ll << 20;
+
+// Tensor memory: 512 columns per SM.  The occupancy calculator reports one
+// block per SM for any kernel that allocates tensor memory, but a 256-column
+// CTA measurably shares its SM with a second one (a 512-column allocation
+// made the 272-CTA gate|up launch run in two waves), so CTAs that fit two to
+// an SM in shared memory take half the columns.
 
 template <int MT>
 struct TcGeo {
   static constexpr int MCH = MT * 8;  // activation rows per chunk = MMA N
   static_assert(MCH % 16 == 0 && MCH <= 128, "MMA N: a multiple of 16 up to 128");
-  static constexpr int NST = MT == 8 ? 3 : 4;  // ring stages
+  static constexpr uint32_t TCOLS = MT == 16 ? 512 : 256;  // tensor-memory columns of a CTA
+  static constexpr int NST = MT == 16 ? 4 : 3;              // ring stages
   static constexpr int ABYTES = 2 * MCH * 128;  // two [MCH][64] fp16 halves
   static constexpr int WBYTES = kTileBytes;      // int8 tile
   static constexpr int STAGE = WBYTES + ABYTES;  // both 1 KB multiples
   static constexpr int TX = WBYTES + ABYTES;
   static constexpr int TBYTES = (MCH * kTStride * 4 + 1023) / 1024 * 1024;
   static_assert(2 * TBYTES <= NST * STAGE, "epilogue tiles must fit in the ring");
-  // tensor memory: accumulator in columns [0, MCH), then NAB A buffers of 64
-  // columns (one k-tile of fp16 pairs) from column TA
-  static constexpr int NAB = MCH <= 64 ? 3 : 2;
+  // tensor memory: accumulator in columns [0, MCH), then one A buffer of 64
+  // columns (one k-tile of fp16 pairs) per ring stage from column TA, so one
+  // MMA completion releases a stage's A buffer and its activations together
+  static constexpr int NAB = NST;
   static constexpr uint32_t TA = MCH <= 64 ? 64 : 128;
-  static_assert(TA + 64 * NAB <= kTmemCols, "tensor-memory columns");
-  static_assert(NST >= NAB, "a ring slot is reused no sooner than an A buffer (converter wait order)");
-  // wfull, xfull, wempty, xempty per stage; afull, afree per A buffer; dfull
-  static constexpr int NBAR = 4 * NST + 2 * NAB + 1;
+  static_assert(TA + 64 * NAB <= TCOLS, "tensor-memory columns");
+  // wfull, xfull, wempty, afull, done per stage; dfull
+  static constexpr int NBAR = 5 * NST + 1;
   static constexpr int SIDE = 128 * 4 + 128 * 4 + 128 * 4 + MCH * 4 + MCH * 4;
   static constexpr size_t SMEM = 1024 + NST * (size_t)STAGE + NBAR * 8 + 16 + SIDE;
   static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
@@ -720,11 +727,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) w8_gemm_kernel(const __grid_con
   // read them have completed
   uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + G::NST * G::STAGE);
   uint64_t* xfull = wfull + G::NST;
-  uint64_t* wempty = xfull + G::NST;   // the converter group's 4 warps
-  uint64_t* xempty = wempty + G::NST;  // 1 MMA commit
-  uint64_t* afull = xempty + G::NST;   // [NAB]: A buffer stored (4 converter warps)
-  uint64_t* afree = afull + G::NAB;    // [NAB]: A buffer's MMAs done (commit)
-  uint64_t* dfull = afree + G::NAB;    // accumulator complete (commit)
+  uint64_t* wempty = xfull + G::NST;  // the converter group's 4 warps
+  uint64_t* afull = wempty + G::NST;  // the stage's A buffer stored and activations landed (4 warps)
+  uint64_t* done = afull + G::NST;    // the stage's MMAs complete (1 commit): A buffer and activations free
+  uint64_t* dfull = done + G::NST;    // accumulator complete (commit)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(dfull + 1);
   float* s_sc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(s_tmem) + 16);  // [128]
   float* s_gam = s_sc + 128;                                                          // [128]
@@ -759,11 +765,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) w8_gemm_kernel(const __grid_con
       mbar_init(&wfull[i], 1);
       mbar_init(&xfull[i], 1);
       mbar_init(&wempty[i], 4);
-      mbar_init(&xempty[i], 1);
-    }
-    for (int j = 0; j < G::NAB; ++j) {
-      mbar_init(&afull[j], 4);
-      mbar_init(&afree[j], 1);
+      mbar_init(&afull[i], 4);
+      mbar_init(&done[i], 1);
     }
     mbar_init(dfull, 1);
     fence_mbar_init();
@@ -789,7 +792,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w8_gemm_kernel(const __grid_con
       fence_proxy_async_global();
       for (int i = 0; i < nk; ++i) {
         const int slot = i % G::NST;
-        if (i >= G::NST && !mbar_wait(&xempty[slot], ((i / G::NST) - 1) & 1, a.status)) break;
+        if (i >= G::NST && !mbar_wait(&done[slot], ((i / G::NST) - 1) & 1, a.status)) break;
         mbar_arrive_expect_tx(&xfull[slot], G::ABYTES);
         uint8_t* sa = smem + slot * G::STAGE + G::WBYTES;
         tma_load_2d(sa, &xmap, (kt0 + i) * kTile, z * G::MCH, &xfull[slot]);
@@ -810,7 +813,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w8_gemm_kernel(const __grid_con
       }
       if (a.xg_out || a.hb_out) s_gn[r] = a.g_next[logical_row(prow, a.layout, a.N) - a.row0];
     }
-    if (warp == 0) tmem_alloc(s_tmem, kTmemCols);
+    if (warp == 0) tmem_alloc(s_tmem, G::TCOLS);
     tc_fence_before();
     tc_bar();
     tc_fence_after();
@@ -871,12 +874,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) w8_gemm_kernel(const __grid_con
       const int r = (warp & 3) * 32 + lane;
       const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
       for (int i = grp; i < nk; i += kTcGroups) {
-        const int slot = i % G::NST, ab = i % G::NAB;
-        // A buffer first: the MMAs of tile i - NAB (and, in order, of every
-        // earlier tile) being done means the tile that last used this ring
-        // slot (i - NST, NST >= NAB, possibly the other group's) has landed,
-        // so the slot's phase parity below cannot be one phase stale
-        if (i >= G::NAB && !mbar_wait(&afree[ab], ((i / G::NAB) - 1) & 1, a.status)) break;
+        const int slot = i % G::NST, ab = slot;
+        // the stage's previous MMAs first: their completion means the tile
+        // that last used this ring slot (i - NST) has landed, so the slot's
+        // phase parity below cannot be one phase stale
+        if (i >= G::NST && !mbar_wait(&done[slot], ((i / G::NST) - 1) & 1, a.status)) break;
         if (!mbar_wait(&wfull[slot], (i / G::NST) & 1, a.status)) break;
         const uint8_t* wrow = smem + slot * G::STAGE + r * 128;
         const uint32_t ta = tmem + lane_base + G::TA + 64 * ab;
@@ -933,9 +935,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) w8_gemm_kernel(const __grid_con
       // ---------------- MMA issuer ----------------
       constexpr uint32_t idesc = tc_idesc_f16(G::MCH);
       for (int i = 0; i < nk; ++i) {
-        const int slot = i % G::NST, ab = i % G::NAB;
+        const int slot = i % G::NST, ab = slot;
         // afull: the A buffer is stored and the stage's activations have landed
-        if (!mbar_wait(&afull[ab], (i / G::NAB) & 1, a.status)) break;
+        if (!mbar_wait(&afull[slot], (i / G::NST) & 1, a.status)) break;
         tc_fence_after();
         const uint32_t act = smem_u32(smem + slot * G::STAGE + G::WBYTES);
 #pragma unroll
@@ -943,8 +945,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w8_gemm_kernel(const __grid_con
           const uint64_t bdesc = tc_sdesc_sw128(act + (ks >> 2) * (G::MCH * 128) + (ks & 3) * 32);
           tc_mma_f16_ta(tmem, tmem + G::TA + 64 * ab + 8 * ks, bdesc, idesc, (i | ks) != 0);
         }
-        tc_commit(&afree[ab]);
-        tc_commit(&xempty[slot]);
+        tc_commit(&done[slot]);
       }
       tc_commit(dfull);
     }
@@ -955,7 +956,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) w8_gemm_kernel(const __grid_con
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(*s_tmem, kTmemCols);
+    tmem_dealloc(*s_tmem, G::TCOLS);
   }
   split_reduce_epilogue<G::MCH, G::TBYTES>(a, smem, s_sc, s_gam, s_pos, s_gn, s_rr, kout, vout, nt, z, sp, warp,
                                            lane);
@@ -1109,11 +1110,7 @@ int w8_pick_splits(int units, int KT) {
   return s;
 }
 
-// Activation rows per CTA: up to 32 rows the warp-level kernel (two CTAs per
-// SM in split-K clusters keep these latency-bound launches short); above 32
-// the tensor-memory kernel (64 or 128 rows per CTA: the contraction is then
-// heavy enough for the legacy MMA to limit the streaming rate).  int4 always
-// runs on the warp-level kernel.
+// Activation rows per CTA (16, 32, 64 or 128, in units of 8).
 static int pick_mt(int M, bool w4) {
   if (w4) return M <= 16 ? 2 : (M <= 32 ? 4 : 8);
   return M <= 16 ? 2 : (M <= 32 ? 4 : (M <= 64 ? 8 : 16));
@@ -1167,25 +1164,35 @@ cudaError_t w8_gemm(const W8Args& a0, const __half* x, cudaStream_t st, bool pdl
   const void* fn;
   size_t smem;
   int threads;
+  int occ = 1;  // resident CTAs per SM beyond the occupancy calculator's count
   if (w4) {
     fn = mt == 2 ? (const void*)wmma_gemm_kernel<2, 4>
                  : mt == 4 ? (const void*)wmma_gemm_kernel<4, 4> : (const void*)wmma_gemm_kernel<8, 4>;
     smem = mt == 2 ? Geo<2, 4>::SMEM : mt == 4 ? Geo<4, 4>::SMEM : Geo<8, 4>::SMEM;
     threads = kThreads;
-  } else if (mt <= 4) {
+  } else if (mt == 2 || (mt == 4 && (int64_t)a.nrows * a.K < kTcMinWeightBytes)) {
+    // up to 16 rows, and up to 32 rows of a small projection: the warp-level
+    // kernel (two CTAs per SM in split-K clusters keep these latency-bound
+    // launches short)
     fn = mt == 2 ? (const void*)wmma_gemm_kernel<2, 8> : (const void*)wmma_gemm_kernel<4, 8>;
     smem = mt == 2 ? Geo<2, 8>::SMEM : Geo<4, 8>::SMEM;
     threads = kThreads;
   } else {
-    fn = mt == 8 ? (const void*)w8_gemm_kernel<8> : (const void*)w8_gemm_kernel<16>;
-    smem = mt == 8 ? TcGeo<8>::SMEM : TcGeo<16>::SMEM;
+    // 32 rows of a large projection and above: the tensor-memory kernel (the
+    // contraction is heavy enough for the legacy MMA to limit the stream)
+    fn = mt == 4 ? (const void*)w8_gemm_kernel<4>
+                 : mt == 8 ? (const void*)w8_gemm_kernel<8> : (const void*)w8_gemm_kernel<16>;
+    smem = mt == 4 ? TcGeo<4>::SMEM : mt == 8 ? TcGeo<8>::SMEM : TcGeo<16>::SMEM;
     threads = kTcThreads;
+    // a 256-column CTA shares its SM with a second one, whatever the
+    // occupancy calculator says (see kTmemCols' note)
+    if (mt <= 8) occ = 2;
   }
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   const int units = chunks * ntiles;
   a.splits = w8_pick_splits(units, a.K / kTile);
   // keep the whole grid resident in one wave
-  while (a.splits > 1 && units > max_active_clusters(fn, threads, smem, a.splits)) --a.splits;
+  while (a.splits > 1 && units > occ * max_active_clusters(fn, threads, smem, a.splits)) --a.splits;
   CUtensorMap map;
   if (!encode_tmap_2d(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, (uint64_t)a.K, (uint64_t)a.M,
                       (uint64_t)a.K * 2, 64, (uint32_t)mch, CU_TENSOR_MAP_SWIZZLE_128B))

@@ -52,7 +52,9 @@ def test_pack_bit_exact(N, K, layout, dtype):
     (17, 384, 640, 0), (128, 512, 1024, 0), (1, 128, 128, 0), (40, 640, 384, 1), (64, 768, 512, 0),
     (100, 640, 2560, 1), (300, 512, 768, 0), (33, 128, 4096, 0),
     # one split over a long K: every ring slot and A buffer cycles several times
-    (64, 19584, 1024, 0), (32, 19584, 1024, 0), (128, 19584, 1024, 1)])
+    (64, 19584, 1024, 0), (32, 19584, 1024, 0), (128, 19584, 1024, 1),
+    # 32 rows of a projection large enough for the tensor-memory kernel
+    (32, 20480, 2560, 0), (31, 20480, 2560, 1)])
 def test_w8a16_linear(M, N, K, layout):
     q, s = synth.w8_grid(5, f"lin{M}{N}{K}", N, K)
     x = synth.target_hidden(5, f"x{M}{K}", M, K)
