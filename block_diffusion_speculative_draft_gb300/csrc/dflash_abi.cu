@@ -281,11 +281,12 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
   // L2 prefetch of the lm-head: a whole number of rows of each first-round
   // tile, about kLmPrefetchBytes in total
   const bool debug_out = hidden_out || logits_out;
-  int lm_first = lmhead_first_tiles(b * (c.B - 1), c.V);
-  if (lm_first > c.V / 128) lm_first = c.V / 128;  // whole tiles only: never past the table
+  const int lm_tile = lmhead_tile_rows(b * (c.B - 1), c.H);
+  int lm_first = lmhead_first_tiles(b * (c.B - 1), c.V, c.H);
+  if (lm_first > c.V / lm_tile) lm_first = c.V / lm_tile;  // whole tiles only: never past the table
   const size_t row_bytes = (size_t)c.H * 2;
-  size_t lm_rows = kLmPrefetchBytes / ((size_t)lm_first * row_bytes);
-  if (lm_rows > 128) lm_rows = 128;
+  size_t lm_rows = lm_first > 0 ? kLmPrefetchBytes / ((size_t)lm_first * row_bytes) : 0;
+  if (lm_rows > (size_t)lm_tile) lm_rows = lm_tile;
   const uint32_t lm_pf_bytes = (uint32_t)(lm_rows * row_bytes);
   const int Mc = commit ? b * rps : 0;
   const int nss = c.H / 128;
@@ -357,7 +358,7 @@ static int32_t draft_block_impl(const dflash_weights* w, const dflash_kv* kv, co
     // tile that starts an lm-head CTA's stream into L2 (a share per layer),
     // so the lm-head reads that part from L2
     at.pf_base = reinterpret_cast<const uint8_t*>(w->lm_head);
-    at.pf_stride = (size_t)128 * c.H * 2;
+    at.pf_stride = (size_t)lm_tile * c.H * 2;
     at.pf_bytes = lm_pf_bytes;
     at.pf_i0 = (int)((long long)lm_first * l / c.L);
     at.pf_i1 = (int)((long long)lm_first * (l + 1) / c.L);

@@ -16,6 +16,7 @@
 // the workspace for the next call.
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tcgen05.cuh"
 
 namespace dfl {
 
@@ -207,11 +208,181 @@ __global__ void __launch_bounds__(kThreads, 1) lmhead_kernel(const __grid_consta
   if (threadIdx.x == 0) *a.ticket = 0;
 }
 
+// ---- tensor-memory path (33 to 128 rows) --------------------------------
+// D[token][vocabulary row] = h . W^T with tcgen05.mma (M = 128 token rows,
+// N = 256 vocabulary rows per tile, K = 16, bf16 operands from 128-byte
+// swizzled shared memory, fp32 accumulator in tensor memory).  Persistent
+// CTAs (one per SM: the kernel holds the SM's 512 tensor-memory columns)
+// walk 256-row vocabulary tiles; a producer warp streams [256 x 64] weight
+// boxes and the matching [128 x 64] box of h into a 4-stage ring, one thread
+// issues the MMAs into two accumulators (tile t into buffer t % 2), and four
+// epilogue warps read a finished accumulator back while the next tile
+// accumulates: thread r owns token row r, so its argmax over the tile's 256
+// logits needs no exchange.  Keys are folded across CTAs as in the
+// warp-level path.
+constexpr int kTcV = 256;                       // vocabulary rows per tile (MMA N)
+constexpr int kTcStages = 4;
+constexpr int kTcWarps = 6;                     // 4 epilogue, producer, MMA
+constexpr int kTcWBytes = kTcV * 128;           // [256 rows][64 bf16]
+constexpr int kTcHBytes = 128 * 128;            // [128 rows][64 bf16]
+constexpr int kTcStage = kTcWBytes + kTcHBytes;  // 48 KB, a 1 KB multiple
+constexpr size_t kTcSmem = 1024 + kTcStages * (size_t)kTcStage + 256;
+
+__global__ void __launch_bounds__(kTcWarps * 32, 1) lmhead_tc_kernel(const __grid_constant__ CUtensorMap wmap,
+                                                                     const __grid_constant__ CUtensorMap hmap,
+                                                                     const LmArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kTcStages * kTcStage);
+  uint64_t* empty = full + kTcStages;  // 1 MMA commit
+  uint64_t* dfull = empty + kTcStages;  // [2] accumulator complete (commit)
+  uint64_t* dfree = dfull + 2;          // [2] accumulator read back (4 epilogue warps)
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(dfree + 2);
+  int* flag = reinterpret_cast<int*>(s_tmem + 1);
+
+  const int ntiles = (a.V + kTcV - 1) / kTcV;
+  const int KS = a.H / 64;
+  const int my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int total = my_tiles * KS;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kTcStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&dfull[b], 1);
+      mbar_init(&dfree[b], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(s_tmem, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  if (warp == 4) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&wmap);
+      prefetch_tmap(&hmap);
+      const uint64_t pol = policy_evict_first();
+      const int pre = total < kTcStages ? total : kTcStages;
+      for (int i = 0; i < pre; ++i) {  // weights need nothing from the preceding kernel
+        const int tile = blockIdx.x + (i / KS) * gridDim.x, ks = i % KS;
+        mbar_arrive_expect_tx(&full[i], kTcStage);
+        tma_load_2d_hint(smem + i * kTcStage, &wmap, ks * 64, tile * kTcV, &full[i], pol);
+      }
+      pdl_wait();
+      fence_proxy_async_global();  // h was written with generic stores: order the tensor reads after them
+      for (int i = 0; i < pre; ++i)
+        tma_load_2d(smem + i * kTcStage + kTcWBytes, &hmap, (i % KS) * 64, 0, &full[i]);
+      for (int i = pre; i < total; ++i) {
+        const int slot = i % kTcStages;
+        const int tile = blockIdx.x + (i / KS) * gridDim.x, ks = i % KS;
+        if (!mbar_wait(&empty[slot], ((i / kTcStages) - 1) & 1, a.status)) break;
+        mbar_arrive_expect_tx(&full[slot], kTcStage);
+        tma_load_2d_hint(smem + slot * kTcStage, &wmap, ks * 64, tile * kTcV, &full[slot], pol);
+        tma_load_2d(smem + slot * kTcStage + kTcWBytes, &hmap, ks * 64, 0, &full[slot]);
+      }
+    }
+    pdl_trigger();
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      constexpr uint32_t idesc = tc_idesc_bf16(128, kTcV);
+      for (int t = 0; t < my_tiles; ++t) {
+        const int db = t & 1;
+        if (t >= 2 && !mbar_wait(&dfree[db], ((t >> 1) - 1) & 1, a.status)) break;
+        tc_fence_after();
+        for (int ks = 0; ks < KS; ++ks) {
+          const int i = t * KS + ks, slot = i % kTcStages;
+          if (!mbar_wait(&full[slot], (i / kTcStages) & 1, a.status)) break;
+          tc_fence_after();
+          const uint32_t wb = smem_u32(smem + slot * kTcStage);
+          const uint32_t hb = wb + kTcWBytes;
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_ss(tmem + db * kTcV, tc_sdesc_sw128(hb + kk * 32), tc_sdesc_sw128(wb + kk * 32), idesc,
+                      (ks | kk) != 0);
+          tc_commit(&empty[slot]);
+        }
+        tc_commit(&dfull[db]);
+      }
+    }
+    pdl_trigger();
+  } else {
+    // ------- epilogue warps 0..3: thread r holds token row r of the accumulator -------
+    pdl_wait();
+    const int r = warp * 32 + lane;
+    const int m = r;
+    unsigned long long best = 0ull;
+    for (int t = 0; t < my_tiles; ++t) {
+      const int db = t & 1;
+      if (!mbar_wait(&dfull[db], (t >> 1) & 1, a.status)) break;
+      tc_fence_after();
+      const int v0 = (blockIdx.x + t * gridDim.x) * kTcV;
+      const uint32_t td = tmem + ((uint32_t)(warp * 32) << 16) + db * kTcV;
+#pragma unroll 1
+      for (int c0 = 0; c0 < kTcV; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32(td + c0, v);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int vv = v0 + c0 + j;
+          const float val = __uint_as_float(v[j]);
+          if (vv < a.V) {
+            best = umax64(best, argmax_key(val, (uint32_t)vv));
+            if (a.logits && m < a.M) a.logits[(size_t)m * a.V + vv] = val;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&dfree[db]);
+    }
+    if (m < a.M && best != 0ull) atomicMax(&a.keys[m], best);
+    pdl_trigger();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int old = atomicAdd(a.ticket, 1);
+    *flag = (old == (int)(gridDim.x * gridDim.y) - 1);
+  }
+  __syncthreads();
+  if (!*flag) return;
+  __threadfence();
+  for (int mm = threadIdx.x; mm < a.M; mm += blockDim.x) {
+    unsigned long long k = atomicExch(&a.keys[mm], 0ull);
+    a.idx[mm] = (int)key_index(k);
+    if (a.maxlogit) a.maxlogit[mm] = key_value(k);
+  }
+  if (threadIdx.x == 0) *a.ticket = 0;
+}
+
 }  // namespace
 
 size_t lmhead_ws_bytes(int64_t M) { return 128 * sizeof(unsigned long long) + 256; }
 
-int lmhead_first_tiles(int M, int V) {
+static bool lmhead_uses_tc(int M, int H) { return M > 32 && M <= 128 && H % 64 == 0; }
+
+int lmhead_tile_rows(int M, int H) { return lmhead_uses_tc(M, H) ? kTcV : 128; }
+
+int lmhead_first_tiles(int M, int V, int H) {
+  if (lmhead_uses_tc(M, H)) {  // one CTA per SM over 256-row tiles
+    const int ntiles = (V + kTcV - 1) / kTcV;
+    return ntiles < num_sms() ? ntiles : num_sms();
+  }
   const int chunks = (M + (M <= 16 ? 16 : 32) - 1) / (M <= 16 ? 16 : 32);
   const int ntiles = (V + 127) / 128;
   int per_chunk = (2 * num_sms()) / chunks;
@@ -241,7 +412,20 @@ cudaError_t lmhead_argmax(const __nv_bfloat16* h, const __nv_bfloat16* w, int M,
   if (!encode_tmap_2d(&hm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, (uint64_t)H, (uint64_t)M, (uint64_t)H * 2, 64,
                       (uint32_t)mch, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  dim3 grid(lmhead_first_tiles(M, V), chunks);
+  if (lmhead_uses_tc(M, H)) {
+    // tensor-memory path: one chunk of up to 128 rows, one CTA per SM
+    CUtensorMap wt, ht;
+    if (!encode_tmap_2d(&wt, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, 64,
+                        kTcV, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tmap_2d(&ht, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h, (uint64_t)H, (uint64_t)M, (uint64_t)H * 2, 64,
+                        128, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
+    dim3 tgrid(lmhead_first_tiles(M, V, H), 1);
+    void* targs[] = {&wt, &ht, &a};
+    cudaFuncSetAttribute((const void*)lmhead_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTcSmem);
+    return launch_k((const void*)lmhead_tc_kernel, tgrid, dim3(kTcWarps * 32), kTcSmem, st, pdl, targs);
+  }
+  dim3 grid(lmhead_first_tiles(M, V, H), chunks);
   void* args[] = {&wm, &hm, &a};
   if (mt == 2) {
     cudaFuncSetAttribute((const void*)lmhead_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,

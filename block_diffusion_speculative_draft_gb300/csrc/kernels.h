@@ -124,9 +124,12 @@ constexpr int64_t kW4TileBytes = 8192 + 256;
 
 // --- lm-head GEMM + argmax (k_lmhead.cu) ---
 size_t lmhead_ws_bytes(int64_t M);
-// Vocabulary tiles (128 rows each) the lm-head kernel reads first: tiles
-// [0, n) start every CTA's stream.
-int lmhead_first_tiles(int M, int V);
+// Vocabulary tiles the lm-head kernel reads first (lmhead_tile_rows rows
+// each): tiles [0, n) start every CTA's stream.
+int lmhead_first_tiles(int M, int V, int H);
+// Vocabulary rows per lm-head tile for M rows (the stride of the tiles that
+// lmhead_first_tiles counts).
+int lmhead_tile_rows(int M, int H);
 cudaError_t lmhead_argmax(const __nv_bfloat16* h, const __nv_bfloat16* w, int M, int V, int H, int* idx_out,
                           float* maxlogit, float* logits, void* ws, cudaStream_t st, bool pdl, int* status);
 
