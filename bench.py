@@ -55,8 +55,11 @@ NCU_TRAFFIC = {
                        "capture": "profiles/w8_gemm_kernel_27b-class.md"},
     "wmma_gemm_kernel": {"ratio": 377.436 / 374.928, "src": "54a33d947721d4ad",
                          "capture": "profiles/wmma_gemm_kernel_27b-class.md"},
-    "lmhead_kernel": {"ratio": 781.06 / 777.99, "src": "e87431f2ece8f763",
+    "lmhead_kernel": {"ratio": 781.06 / 777.99, "src": "01ee840985b7ff35",
                       "capture": "profiles/lmhead_kernel_qwen3-4b.md"},
+    # two launches, 8 x Qwen3-8B-shaped batch (120 rows)
+    "lmhead_tc_kernel": {"ratio": 2497.985 / 2491.286, "src": "01ee840985b7ff35",
+                         "capture": "profiles/lmhead_tc_kernel_b8-qwen3-8b.md"},
 }
 
 
@@ -524,7 +527,9 @@ def run_ours(args, rank, world, local_rank):
     order = sorted(proj, key=lambda k: -statistics.mean(proj[k]["ms"]))
     roofline = proj_roofline(order[0])
     roofline_other = proj_roofline(order[1]) if len(order) > 1 else None
-    traffic_lm = traffic_for("lmhead_kernel", "k_lmhead.cu", lm_bytes)
+    # the library's lm-head runs on tensor memory for 33 to 128 rows
+    lm_kernel = "lmhead_tc_kernel" if 32 < M1 <= 128 and cfg.H % 64 == 0 else "lmhead_kernel"
+    traffic_lm = traffic_for(lm_kernel, "k_lmhead.cu", lm_bytes)
     sweep_out = {}
     for label, lens in sweep:
         cb = cfg.step_bytes(lens)
@@ -558,7 +563,8 @@ def run_ours(args, rank, world, local_rank):
         "verify_sample_blocks_per_s": b / (statistics.median(smp_ms) / VREP / 1e3),
         "roofline": roofline,
         "roofline_projections_other_kernel": roofline_other,
-        "roofline_lmhead": {"kernel": "lmhead_kernel (bf16 GEMV + fused argmax), alone", "bound": "hbm",
+        "roofline_lmhead": {"kernel": (f"{lm_kernel} (bf16 {'tcgen05 GEMM' if lm_kernel == 'lmhead_tc_kernel' else 'GEMV'}"
+                                       f" + fused argmax, {M1} rows), alone"), "bound": "hbm",
                             "achieved": lm_gbs, "peak": hbm, "unit": "GB/s", "frac": lm_gbs / hbm,
                             "traffic": traffic_lm, "algorithmic_bytes_per_launch": lm_bytes,
                             "avg_launch_us": statistics.mean(lm_ms) * 1e3},
