@@ -260,7 +260,11 @@ __global__ void __launch_bounds__(kNormThreads) final_norm_kernel(const float* x
   fence_proxy_async_global();  // the lm-head reads h with TMA
 }
 
-// len[j] += min(n[j] + 1, rows_per_seq) unless that would pass cap
+// len[j] += min(n[j] + 1, rows_per_seq) unless that would pass cap.
+// Deliberately no early trigger (griddepcontrol.launch_dependents): the next
+// draft pass's kernels then start only after this one has completed, which is
+// what lets its attention read len (and the committed context K/V) before its
+// own dependency wait.
 __global__ void commit_len_kernel(int* len, const int* nacc, int b, int rows_per_seq, int cap, int* status) {
   pdl_wait();
   int j = blockIdx.x * blockDim.x + threadIdx.x;
