@@ -51,9 +51,9 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # DRAM read + write over algorithmic bytes of four captured launches of
     # each kernel on the 27B-class step (32 rows)
-    "w8_gemm_kernel": {"ratio": 543.102 / 533.504, "src": "54a33d947721d4ad",
+    "w8_gemm_kernel": {"ratio": 543.048 / 533.504, "src": "c9550cad434bcfaa",
                        "capture": "profiles/w8_gemm_kernel_27b-class.md"},
-    "wmma_gemm_kernel": {"ratio": 377.436 / 374.928, "src": "54a33d947721d4ad",
+    "wmma_gemm_kernel": {"ratio": 377.436 / 374.928, "src": "c9550cad434bcfaa",
                          "capture": "profiles/wmma_gemm_kernel_27b-class.md"},
     "lmhead_kernel": {"ratio": 781.06 / 777.99, "src": "01ee840985b7ff35",
                       "capture": "profiles/lmhead_kernel_qwen3-4b.md"},
