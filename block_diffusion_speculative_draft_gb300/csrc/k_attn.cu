@@ -29,6 +29,7 @@
 
 #include "kernels.h"
 #include "ptx.cuh"
+#include "tcgen05.cuh"
 
 namespace dfl {
 
@@ -38,10 +39,10 @@ constexpr int kMaxSplits = 16;  // one (non-portable) cluster of splits
 constexpr int kPortable = 8;    // largest cluster every sm_90+ part accepts
 constexpr int kKT = 64;         // keys per tile
 
-// keys [k0, k1) of split sp out of ns equal, 64-aligned chunks of `total`
-__device__ __forceinline__ void split_range(int total, int sp, int ns, int& k0, int& k1) {
+// keys [k0, k1) of split sp out of ns equal, kt-aligned chunks of `total`
+__device__ __forceinline__ void split_range(int total, int sp, int ns, int kt, int& k0, int& k1) {
   int chunk = (total + ns - 1) / ns;
-  chunk = (chunk + kKT - 1) / kKT * kKT;
+  chunk = (chunk + kt - 1) / kt * kt;
   k0 = min(total, sp * chunk);
   k1 = min(total, k0 + chunk);
 }
@@ -52,11 +53,112 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x, hardware approximation;
   return y;
 }
 
-// Byte offset of 16-byte chunk ch (of D / 8) of row r in a K or V stage:
-// [D / 64 column halves][64 rows][128 bytes], chunk c of a row at c ^ (r % 8)
-// (the layout a 64 x 64 fp16 tensor-map box with 128-byte swizzle writes).
+// Byte offset of 16-byte chunk ch (of D / 8) of row r in a K or V stage of
+// KT rows: [D / 64 column halves][KT rows][128 bytes], chunk c of a row at
+// c ^ (r % 8) (the layout a 64-column x KT-row fp16 tensor-map box with
+// 128-byte swizzle writes).
+template <int KT = kKT>
 __device__ __forceinline__ int kv_off(int r, int ch) {
-  return ((ch >> 3) << 13) + (r << 7) + (((ch & 7) ^ (r & 7)) << 4);
+  return (ch >> 3) * (KT * 128) + (r << 7) + (((ch & 7) ^ (r & 7)) << 4);
+}
+
+// Gathers keys [t0, t0 + KT) of (sequence j, kv head g) row by row with
+// cp.async (threads tid of nthr) into K/V stage stg, in the swizzled layout of a tensor-map tile:
+// part 0 = committed context rows t < Lold only, 1 = the rest (rows a folded
+// commit appends, the block's keys, zero fill past k1), 2 = all.  Cache row
+// t < L of the head is row row0 + t of kc / vc; block key t - L is row
+// (j B + t - L) of kblk / vblk.
+template <int D, int KT = kKT>
+__device__ __forceinline__ void gather_tile(const AttnArgs& a, uint8_t* sK, uint8_t* sV, int stg, int t0, int part,
+                                            int k1, int Lold, int L, int row0, int j, int g, int tid, int nthr) {
+  constexpr int KVB = KT * D * 2;
+  for (int c = tid; c < KT * (D / 8); c += nthr) {
+    const int r = c / (D / 8), ch = c % (D / 8);
+    const int t = t0 + r;
+    const bool ok = t < k1;
+    const bool old_ctx = ok && t < Lold;
+    if (part == 0 && !old_ctx) continue;
+    if (part == 1 && old_ctx) continue;
+    const __half* ks = a.kc;
+    const __half* vs = a.vc;
+    if (ok) {
+      if (t < L) {
+        const size_t off = ((size_t)row0 + t) * D + ch * 8;
+        ks = a.kc + off;
+        vs = a.vc + off;
+      } else {
+        const size_t off = ((size_t)(j * a.B + (t - L)) * a.nkv + g) * D + ch * 8;
+        ks = a.kblk + off;
+        vs = a.vblk + off;
+      }
+    }
+    const int so = stg * KVB + kv_off<KT>(r, ch);
+    cp_async16(sK + so, ks, ok);
+    cp_async16(sV + so, vs, ok);
+  }
+}
+
+// Split merge, after every split has staged its rows in `sst` grouped by
+// owner ([ns owners][maxr][RSH] fp16: D normalised partial outputs, then the
+// row's fp32 log2-domain log-sum-exp): each owner receives its group from
+// every split with one bulk shared-to-shared::cluster copy into rO
+// ([ns splits][maxr][RSH]), counted on its receive barrier, then merges its
+// query rows [r0, r1) over the splits in split order and writes them out.
+// Every load of an item is issued before its arithmetic.
+template <int D>
+__device__ __forceinline__ void merge_splits(const AttnArgs& a, __half* rO, const __half* sst, uint64_t* rbar,
+                                             int rows, int grp, int ns, int sp, int maxr, int r0, int r1, int j,
+                                             int g) {
+  constexpr int RSH = D + 8;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0 && lane < ns) {
+    const int p = lane;
+    const int nr = ((p + 1) * rows) / ns - (p * rows) / ns;
+    if (nr > 0)
+      bulk_s2cluster(dsmem_addr(smem_u32(rO + (size_t)sp * maxr * RSH), (uint32_t)p),
+                     smem_u32(sst + (size_t)p * maxr * RSH), (uint32_t)(nr * RSH * 2),
+                     dsmem_addr(smem_u32(rbar), (uint32_t)p));
+    bulk_commit();
+  }
+  mbar_wait(rbar, 0, a.status);
+  for (int it = threadIdx.x; it < (r1 - r0) * (D / 4); it += blockDim.x) {
+    const int lr = it / (D / 4), c4 = it % (D / 4);
+    float lv[kMaxSplits];
+    uint2 pv[kMaxSplits];
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxSplits; ++s2)
+      if (s2 < ns) {
+        const __half* row = rO + (size_t)(s2 * maxr + lr) * RSH;
+        lv[s2] = *reinterpret_cast<const float*>(row + D);
+        pv[s2] = *reinterpret_cast<const uint2*>(row + 4 * c4);
+      }
+    float mmax = -INFINITY;
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxSplits; ++s2)
+      if (s2 < ns) mmax = fmaxf(mmax, lv[s2]);
+    float den = 0.f;
+    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxSplits; ++s2)
+      if (s2 < ns) {
+        const float w = ex2(lv[s2] - mmax);
+        const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&pv[s2].x));
+        const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&pv[s2].y));
+        den += w;
+        num.x += w * lo.x;
+        num.y += w * lo.y;
+        num.z += w * hi.x;
+        num.w += w * hi.y;
+      }
+    const float id = 1.f / den;
+    const int rho = r0 + lr;
+    int tok = rho / grp, hh = rho - tok * grp;
+    __half2* dst = reinterpret_cast<__half2*>(a.out + ((size_t)(j * a.B + tok) * a.nq + g * grp + hh) * D + 4 * c4);
+    dst[0] = __floats2half2_rn(num.x * id, num.y * id);
+    dst[1] = __floats2half2_rn(num.z * id, num.w * id);
+  }
+  // the staging area must outlive the copies' reads of it
+  if (warp == 0 && lane < ns) bulk_wait_read_all();
 }
 
 template <int D, int KH, int NST>
@@ -92,7 +194,7 @@ __global__ void __launch_bounds__(320, 1)
   if (a.nacc) L += commit_count(a.len[j], a.nacc[j], a.rps, a.cap);
   const int total = L + a.B;
   int k0, k1;
-  split_range(total, sp, ns, k0, k1);
+  split_range(total, sp, ns, kKT, k0, k1);
   const int ntile = (k1 - k0 + kKT - 1) / kKT;
   const int row0 = (j * a.nkv + g) * a.cap;  // this head's first cache row in the tensor maps
   // tile i is a whole tile of committed context (one tensor-map box per 64
@@ -118,33 +220,8 @@ __global__ void __launch_bounds__(320, 1)
       tma_load_2d(sV + stg * KVB + h * 8192, &vmap, h * 64, row0 + k0 + i * kKT, &full[stg]);
     }
   };
-  // gathered tile: part 0 = committed context rows t < Lold only, 1 = the
-  // rest (appended context rows, block keys, zero fill), 2 = all
   auto load_rows = [&](int stg, int t0, int part) {
-    for (int c = threadIdx.x; c < kKT * (D / 8); c += blockDim.x) {
-      const int r = c / (D / 8), ch = c % (D / 8);
-      const int t = t0 + r;
-      const bool ok = t < k1;
-      const bool old_ctx = ok && t < Lold;
-      if (part == 0 && !old_ctx) continue;
-      if (part == 1 && old_ctx) continue;
-      const __half* ks = a.kc;
-      const __half* vs = a.vc;
-      if (ok) {
-        if (t < L) {
-          const size_t off = ((size_t)row0 + t) * D + ch * 8;
-          ks = a.kc + off;
-          vs = a.vc + off;
-        } else {
-          const size_t off = ((size_t)(j * a.B + (t - L)) * a.nkv + g) * D + ch * 8;
-          ks = a.kblk + off;
-          vs = a.vblk + off;
-        }
-      }
-      const int so = stg * KVB + kv_off(r, ch);
-      cp_async16(sK + so, ks, ok);
-      cp_async16(sV + so, vs, ok);
-    }
+    gather_tile<D>(a, sK, sV, stg, t0, part, k1, Lold, L, row0, j, g, threadIdx.x, blockDim.x);
   };
   // prologue: tiles 0 .. NST-2; the context part before the wait
   constexpr int PRE = NST - 1;
@@ -423,56 +500,389 @@ __global__ void __launch_bounds__(320, 1)
   }
   fence_proxy_async_shared();  // each writer: the staged rows are visible to the bulk copies
   __syncthreads();
-  if (warp == 0 && lane < ns) {
-    const int p = lane;
-    const int nr = ((p + 1) * rows) / ns - (p * rows) / ns;
-    if (nr > 0)
-      bulk_s2cluster(dsmem_addr(smem_u32(rO + (size_t)sp * maxr * RSH), (uint32_t)p),
-                     smem_u32(sst + (size_t)p * maxr * RSH), (uint32_t)(nr * RSH * 2),
-                     dsmem_addr(smem_u32(rbar), (uint32_t)p));
-    bulk_commit();
+  merge_splits<D>(a, rO, sst, rbar, rows, grp, ns, sp, maxr, r0, r1, j, g);
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-memory form: the same grid, splits, gathers and merge; the query
+// tile (rows <= 256, rows past `rows` zero) is the M side of tcgen05.mma, in
+// one or two blocks of 128 rows.  Three roles run their own loops over the
+// split's 64-key tiles, handing off through mbarriers only:
+//  * a producer warp fills a ring of NST K/V stages (tensor-map copies for
+//    whole tiles of committed context; the other tiles gathered row by row
+//    with cp.async by the warp), each stage released by a tcgen05.commit once
+//    the MMAs that read it are done;
+//  * one thread issues S = Q K^T (M 128, N 64, K 16 per instruction; A = Q
+//    from tensor memory, B = K straight from its swizzled tile) and
+//    O += P V (M 128, N d, K 16: A = P from tensor memory, B = V read
+//    MN-major from its tile, 64-dimension halves 8 KB apart, 8-key groups
+//    1 KB apart), committing each block's S to its own mbarrier; the next
+//    tile's S of block 0 is issued right after this tile's P V of block 0,
+//    so with two blocks one block's softmax runs while the other block's
+//    MMAs do;
+//  * a warp per 32 query rows (a thread per row: the row's max and sum need
+//    no shuffles) copies its Q rows to tensor memory, then per tile reads
+//    its scores from tensor memory, runs the online softmax and stores P
+//    back as fp16 pairs over the first half of the row's scores (the next
+//    S of the block is written by an MMA issued after the P V that reads
+//    them, and MMAs from one thread execute in issue order).
+// O stays in tensor memory for the whole split.  A row's reference maximum
+// is raised only when a tile's maximum exceeds it by more than 8 in log2
+// units (the rescale of O is then a read-modify-write of the row); below
+// that the reference stays, every p is at most 2^8, which the fp16 P and the
+// fp32 sums hold as well, and the result is the same softmax normalised by
+// the same sum.
+constexpr int kTcThreads = 320;  // warps 0-7 softmax, 8 tensor memory + MMA issue, 9 producer
+constexpr int kTcMmaWarp = 8;
+constexpr int kTcProdWarp = 9;
+
+template <int D, int NST>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                   const __grid_constant__ CUtensorMap qmap, const AttnArgs a) {
+  constexpr int RB = D * 2;
+  constexpr int KVB = kKT * RB;
+  constexpr int RSH = D + 8;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int sp = blockIdx.x, g = blockIdx.y, j = blockIdx.z;
+  const int ns = gridDim.x;
+  const int grp = a.nq / a.nkv;
+  const int rows = a.B * grp;
+  const int MB = rows > 128 ? 2 : 1;  // 128-row blocks
+  const int rows_pad = MB * 128;
+  uint8_t* sK = smem;            // [NST][KVB], 1024-aligned
+  uint8_t* sV = sK + NST * KVB;  // [NST][KVB]
+  uint8_t* sQ = sV + NST * KVB;  // [D / 64][rows_pad][128 bytes], swizzled like a K/V stage
+  uint64_t* full = reinterpret_cast<uint64_t*>(sQ + rows_pad * RB);  // [NST] a stage has landed
+  uint64_t* empty = full + 3;  // [NST] a stage's MMAs are done
+  uint64_t* sbar = full + 6;   // [2] S of a block is in tensor memory
+  uint64_t* pbar = full + 8;   // [2] P of a block is (one arrival per softmax warp of the block)
+  uint64_t* ofin = full + 10;  // every MMA of the split is done
+  uint64_t* qbar = full + 11;
+  uint64_t* rbar = full + 12;
+  uint64_t* qtm = full + 13;   // Q is in tensor memory (one arrival per softmax warp)
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(full + 14);
+  __half* rO = reinterpret_cast<__half*>(reinterpret_cast<uint8_t*>(full) + 128);  // receive [ns][maxr][RSH]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // softmax warp w < 8 owns query rows 128 (w / 4) + 32 (w % 4) + lane, the
+  // tensor-memory lanes 32 (w % 4) + lane of row block w / 4
+  const bool smx = warp < 8 && (warp >> 2) * 128 + (warp & 3) * 32 < rows;
+  const int nsw0 = rows >= 128 ? 4 : (rows + 31) / 32;
+  const int nsw1 = rows > 128 ? (rows - 128 + 31) / 32 : 0;
+  const uint32_t ncols = MB == 2 ? 512u : 256u;
+  // tensor-memory columns: O of block m at m D, S at MB D + 64 m (P, fp16
+  // pairs, over its first 32), Q (fp16 pairs) at MB D + 64 MB + (D / 2) m
+  const uint32_t cS = MB * D, cQ = MB * D + 64 * MB;
+
+  int L = a.len[j];
+  if (L < 0) L = 0;
+  if (L > a.cap) L = a.cap;
+  const int Lold = L;
+  if (a.nacc) L += commit_count(a.len[j], a.nacc[j], a.rps, a.cap);
+  const int total = L + a.B;
+  int k0, k1;
+  split_range(total, sp, ns, kKT, k0, k1);
+  const int ntile = (k1 - k0 + kKT - 1) / kKT;
+  const int row0 = (j * a.nkv + g) * a.cap;
+  auto is_tma = [&](int i) { return k0 + (i + 1) * kKT <= min(k1, Lold); };
+  const int maxr = (rows + ns - 1) / ns;
+  const int r0 = (sp * rows) / ns, r1 = ((sp + 1) * rows) / ns;
+  const bool prod = warp == kTcProdWarp;
+  auto issue_tma = [&](int i, int stg) {  // producer lane 0
+    fence_proxy_async_shared();
+    mbar_arrive_expect_tx(&full[stg], 2 * KVB);
+#pragma unroll
+    for (int h = 0; h < D / 64; ++h) {
+      tma_load_2d(sK + stg * KVB + h * 8192, &kmap, h * 64, row0 + k0 + i * kKT, &full[stg]);
+      tma_load_2d(sV + stg * KVB + h * 8192, &vmap, h * 64, row0 + k0 + i * kKT, &full[stg]);
+    }
+  };
+  auto gather = [&](int i, int part) {  // producer warp
+    gather_tile<D>(a, sK, sV, i % NST, k0 + i * kKT, part, k1, Lold, L, row0, j, g, lane, 32);
+  };
+  // a gathered stage is complete once the warp's copies have landed and are
+  // visible to the tensor cores
+  auto gathered = [&](int stg) {
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_proxy_async_shared();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&full[stg]);
+  };
+  if (prod && lane == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int m = 0; m < 2; ++m) mbar_init(&sbar[m], 1);
+    mbar_init(&pbar[0], (uint32_t)nsw0);
+    mbar_init(&pbar[1], (uint32_t)(nsw1 > 0 ? nsw1 : 1));
+    mbar_init(ofin, 1);
+    mbar_init(qbar, 1);
+    mbar_init(qtm, (uint32_t)(nsw0 + nsw1));
+    if (ns > 1) {
+      mbar_init(rbar, 1);
+      mbar_arrive_expect_tx(rbar, (uint32_t)(ns * (r1 - r0) * RSH * 2));
+    }
+    fence_mbar_init();
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&vmap);
+    prefetch_tmap(&qmap);
+    // the context K/V and its length are inputs of the whole draft pass, so
+    // whole context tiles are fetched before the dependency wait
+    for (int i = 0; i < NST && i < ntile; ++i)
+      if (is_tma(i)) issue_tma(i, i);
   }
-  // merge the owned rows over the ns splits, in split order; every load of
-  // an item is issued before its arithmetic
-  mbar_wait(rbar, 0, a.status);
-  for (int it = threadIdx.x; it < (r1 - r0) * (D / 4); it += blockDim.x) {
-    const int lr = it / (D / 4), c4 = it % (D / 4);
-    float lv[kMaxSplits];
-    uint2 pv[kMaxSplits];
+  __syncthreads();
+  if (ns > 1) cluster_arrive_relaxed();
+  if (prod)
+    for (int i = 0; i < NST && i < ntile; ++i)
+      if (!is_tma(i)) gather(i, 0);  // committed context rows of a gathered tile
+  if (a.pf_base && threadIdx.x == 0)
+    prefetch_l2_job(a.pf_base, a.pf_stride, a.pf_bytes, a.pf_i0, a.pf_i1,
+                    blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z), gridDim.x * gridDim.y * gridDim.z);
+  pdl_wait();
+  // tensor memory after the dependency wait: the preceding kernel's CTAs on
+  // this SM have finished, so their columns are free
+  if (warp == kTcMmaWarp) tmem_alloc(s_tmem, ncols);
+  if (prod) {
+    if (lane == 0) {
+      fence_proxy_async_global();  // q was written by the preceding kernel with generic stores
+      mbar_arrive_expect_tx(qbar, (uint32_t)((D / 64) * rows * 128));
 #pragma unroll
-    for (int s2 = 0; s2 < kMaxSplits; ++s2)
-      if (s2 < ns) {
-        const __half* row = rO + (size_t)(s2 * maxr + lr) * RSH;
-        lv[s2] = *reinterpret_cast<const float*>(row + D);
-        pv[s2] = *reinterpret_cast<const uint2*>(row + 4 * c4);
+      for (int h = 0; h < D / 64; ++h) tma_load_3d(sQ + h * rows_pad * 128, &qmap, h * 64, g * grp, j * a.B, qbar);
+    }
+    for (int i = 0; i < NST && i < ntile; ++i)
+      if (!is_tma(i)) {
+        gather(i, 1);  // rows the preceding kernels wrote: appended context, the block's keys
+        gathered(i);
       }
-    float mmax = -INFINITY;
-#pragma unroll
-    for (int s2 = 0; s2 < kMaxSplits; ++s2)
-      if (s2 < ns) mmax = fmaxf(mmax, lv[s2]);
-    float den = 0.f;
-    float4 num = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int s2 = 0; s2 < kMaxSplits; ++s2)
-      if (s2 < ns) {
-        const float w = ex2(lv[s2] - mmax);
-        const float2 lo = __half22float2(*reinterpret_cast<const __half2*>(&pv[s2].x));
-        const float2 hi = __half22float2(*reinterpret_cast<const __half2*>(&pv[s2].y));
-        den += w;
-        num.x += w * lo.x;
-        num.y += w * lo.y;
-        num.z += w * hi.x;
-        num.w += w * hi.y;
-      }
-    const float id = 1.f / den;
-    const int rho = r0 + lr;
-    int tok = rho / grp, hh = rho - tok * grp;
-    __half2* dst = reinterpret_cast<__half2*>(a.out + ((size_t)(j * a.B + tok) * a.nq + g * grp + hh) * D + 4 * c4);
-    dst[0] = __floats2half2_rn(num.x * id, num.y * id);
-    dst[1] = __floats2half2_rn(num.z * id, num.w * id);
   }
-  // the staging area must outlive the copies' reads of it
-  if (warp == 0 && lane < ns) bulk_wait_read_all();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const float sl2 = rsqrtf((float)D) * 1.4426950408889634f;  // 1/sqrt(d) in log2 units
+  const int mb = warp >> 2;
+  const int rho = mb * 128 + (warp & 3) * 32 + lane;  // this thread's query row (softmax warps)
+  const uint32_t lanes = (uint32_t)((warp & 3) * 32) << 16;
+  float mref = -INFINITY, lsum = 0.f;  // reference maximum (raw score units) and sum of the row
+  bool dead = false;                   // a wait gave up: the status is raised, the rest only drains
+
+  if (prod) {
+    // ---------------- producer: tiles NST .. ntile-1 ----------------
+    for (int i = NST; i < ntile; ++i) {
+      const int stg = i % NST;
+      if (!dead && !mbar_wait(&empty[stg], ((i / NST) - 1) & 1, a.status)) dead = true;
+      if (is_tma(i)) {
+        if (lane == 0) issue_tma(i, stg);
+      } else {
+        gather(i, 2);
+        gathered(stg);
+      }
+    }
+  } else if (warp == kTcMmaWarp) {
+    // ---------------- MMA issue (one thread) ----------------
+    if (lane == 0 && ntile > 0) {
+      auto qk = [&](int it, int m) {  // S of block m for tile it
+        const uint32_t ksb = smem_u32(sK + (it % NST) * KVB);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          tc_mma_f16_ta(tmem + cS + 64 * m, tmem + cQ + (D / 2) * m + 8 * ks,
+                        tc_sdesc_sw128(ksb + (ks >> 2) * 8192 + (ks & 3) * 32), tc_idesc_f16(kKT), ks != 0);
+        tc_commit(&sbar[m]);
+      };
+      auto pv = [&](int it, int m) {  // O of block m += P V for tile it
+        const uint32_t vsb = smem_u32(sV + (it % NST) * KVB);
+#pragma unroll
+        for (int kk = 0; kk < kKT / 16; ++kk)
+          tc_mma_f16_ta(tmem + D * m, tmem + cS + 64 * m + 8 * kk, tc_sdesc_mn_sw128(vsb + kk * 2048, 8192, 1024),
+                        tc_idesc_f16_bmn(D), (it | kk) != 0);
+      };
+      auto landed = [&](int it) {
+        if (!dead && !mbar_wait(&full[it % NST], (it / NST) & 1, a.status)) dead = true;
+        tc_fence_after();
+      };
+      if (!dead && !mbar_wait(qtm, 0, a.status)) dead = true;
+      tc_fence_after();
+      landed(0);
+      qk(0, 0);
+      if (MB == 2) qk(0, 1);
+      for (int it = 0; it < ntile; ++it) {
+        const bool nxt = it + 1 < ntile;
+        if (!dead && !mbar_wait(&pbar[0], it & 1, a.status)) dead = true;
+        tc_fence_after();
+        pv(it, 0);
+        if (MB == 2) {
+          if (nxt) {
+            landed(it + 1);
+            qk(it + 1, 0);
+          }
+          if (!dead && !mbar_wait(&pbar[1], it & 1, a.status)) dead = true;
+          tc_fence_after();
+          pv(it, 1);
+          tc_commit(&empty[it % NST]);
+          if (nxt) qk(it + 1, 1);
+        } else {
+          tc_commit(&empty[it % NST]);
+          if (nxt) {
+            landed(it + 1);
+            qk(it + 1, 0);
+          }
+        }
+      }
+      tc_commit(ofin);
+    }
+  } else if (smx) {
+    // ---------------- online softmax, a thread per query row ----------------
+    {  // this row of Q (zero past `rows`) to tensor memory as fp16 pairs
+      if (!dead && !mbar_wait(qbar, 0, a.status)) dead = true;
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h) {
+        uint32_t w[32];
+        const uint8_t* qrow = sQ + h * rows_pad * 128 + rho * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          uint4 u = make_uint4(0u, 0u, 0u, 0u);
+          if (rho < rows) u = *reinterpret_cast<const uint4*>(qrow + ((c ^ (rho & 7)) << 4));
+          w[4 * c] = u.x;
+          w[4 * c + 1] = u.y;
+          w[4 * c + 2] = u.z;
+          w[4 * c + 3] = u.w;
+        }
+        tmem_st32(tmem + lanes + cQ + (D / 2) * mb + 32 * h, w);
+      }
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qtm);
+    }
+    for (int it = 0; it < ntile; ++it) {
+      if (!dead && !mbar_wait(&sbar[mb], it & 1, a.status)) dead = true;
+      tc_fence_after();
+      float s[kKT];
+      {
+        uint32_t v[32];
+        tmem_ld32_wait(tmem + lanes + cS + 64 * mb, v);
+#pragma unroll
+        for (int n = 0; n < 32; ++n) s[n] = __uint_as_float(v[n]);
+        tmem_ld32_wait(tmem + lanes + cS + 64 * mb + 32, v);
+#pragma unroll
+        for (int n = 0; n < 32; ++n) s[32 + n] = __uint_as_float(v[n]);
+      }
+      // keys past the split's end only occur in its last tile
+      const int kb = k0 + it * kKT;
+      if (kb + kKT > k1) {
+#pragma unroll
+        for (int n = 0; n < kKT; ++n)
+          if (kb + n >= k1) s[n] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int n = 1; n < kKT; ++n) mx = fmaxf(mx, s[n]);
+      const float mnew = fmaxf(mref, mx);
+      const bool resc = mref != -INFINITY && (mnew - mref) * sl2 > 8.f;
+      const float corr = resc ? ex2((mref - mnew) * sl2) : 1.f;
+      if (mref == -INFINITY || resc) mref = mnew;
+      if (__any_sync(0xffffffffu, resc)) {
+        // O holds the earlier tiles' P V (complete: this tile's S was
+        // committed after it)
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t v[32];
+          tmem_ld32_wait(tmem + lanes + mb * D + c, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * corr);
+          tmem_st32(tmem + lanes + mb * D + c, v);
+        }
+      }
+      lsum *= corr;
+      const float nb = mref == -INFINITY ? 0.f : -mref * sl2;
+      uint32_t pw[32];
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2(fmaf(s[2 * c], sl2, nb));
+        const float p1 = ex2(fmaf(s[2 * c + 1], sl2, nb));
+        rs += p0 + p1;
+        __half2 h = __floats2half2_rn(p0, p1);
+        pw[c] = *reinterpret_cast<uint32_t*>(&h);
+      }
+      lsum += rs;
+      tmem_st32(tmem + lanes + cS + 64 * mb, pw);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pbar[mb]);
+    }
+    // O is final once every MMA of the split is done
+    if (ntile > 0 && !dead && !mbar_wait(ofin, 0, a.status)) dead = true;
+    tc_fence_after();
+  }
+  if (prod) {  // zero-fill copies of an empty split
+    cp_async_commit();
+    cp_async_wait<0>();
+  }
+  if (prod && lane == 0) mbar_wait(qbar, 0, a.status);  // Q landed even where no tile was computed
+  pdl_trigger();
+
+  // normalise this split's rows; log2-domain log-sum-exp (-inf when empty)
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  const float lse = lsum > 0.f ? mref * sl2 + log2f(lsum) : -INFINITY;
+  const int tok = rho / grp, hh = rho - (rho / grp) * grp;
+  __half* sst = nullptr;
+  if (ns > 1) {
+    const size_t need = (size_t)ns * maxr * RSH * 2;
+    sst = need <= (size_t)2 * NST * KVB + (size_t)rows_pad * RB ? reinterpret_cast<__half*>(sK)
+                                                                : rO + (size_t)ns * maxr * RSH;
+    cluster_wait();   // every peer's receive barrier is initialised and armed
+    __syncthreads();  // every MMA is done: nothing reads the K/V stages or Q any more
+  }
+  if (smx) {
+    __half* dst;
+    if (ns == 1) {
+      dst = a.out + ((size_t)(j * a.B + tok) * a.nq + g * grp + hh) * D;
+    } else {
+      const int own = ((rho + 1) * ns - 1) / rows;
+      dst = sst + (size_t)(own * maxr + rho - (own * rows) / ns) * RSH;
+    }
+#pragma unroll
+    for (int c = 0; c < D; c += 32) {
+      uint32_t v[32];
+      if (ntile > 0) {
+        tmem_ld32_wait(tmem + lanes + mb * D + c, v);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = 0u;
+      }
+      if (rho < rows) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint4 u;
+          uint32_t* w = reinterpret_cast<uint32_t*>(&u);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            __half2 h = __floats2half2_rn(__uint_as_float(v[8 * q + 2 * e]) * inv,
+                                          __uint_as_float(v[8 * q + 2 * e + 1]) * inv);
+            w[e] = *reinterpret_cast<uint32_t*>(&h);
+          }
+          *reinterpret_cast<uint4*>(dst + c + 8 * q) = u;
+        }
+      }
+    }
+    if (ns > 1 && rho < rows) *reinterpret_cast<float*>(dst + D) = lse;
+  }
+  if (ns > 1) fence_proxy_async_shared();  // each writer: the staged rows are visible to the bulk copies
+  // every tensor-memory read is done (or abandoned after a timeout)
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kTcMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, ncols);
+  }
+  if (ns == 1) return;
+  merge_splits<D>(a, rO, sst, rbar, rows, grp, ns, sp, maxr, r0, r1, j, g);
 }
 
 }  // namespace
@@ -532,78 +942,112 @@ static int max_smem_optin() {
   return cached[dev];
 }
 
+// The tensor-memory kernel runs query tiles of 129-256 rows (two 128-row MMA
+// blocks) whose splits get at least this many 64-key tiles; below that its
+// fixed per-split work (tensor-memory allocation, the copy of Q, the
+// hand-offs of the first tile) outweighs its faster tiles.  Draft pass of the
+// 27B-class drafter (5 layers, 160 query rows per kv head), us, warp-level /
+// tensor-memory kernel: 674 / 676 at 1024 context rows (2 tiles per split),
+// 688 / 694 at 2048 (4 tiles), 727 / 714 at 4096 (6 tiles); at 64 and 128
+// rows (Qwen3-4B / 8B shapes, one MMA block) it was slower at every length.
+constexpr int kTcMinTiles = 5;
+
 cudaError_t attention(const AttnArgs& a0, cudaStream_t st, bool pdl) {
   AttnArgs a = a0;
   if (a.d != 64 && a.d != 128) return cudaErrorInvalidValue;
   const int rows = a.B * (a.nq / a.nkv);
   const int nw = (rows + 15) / 16;
-  const int rows_pad = nw * 16;
   a.nwc = nw;
-  const int nthr = (2 * nw < 10 ? 2 * nw : (nw > 10 ? nw : 10)) * 32;
-  auto kernel_for = [&](bool kh2, int nst) {
-    if (a.d == 128)
-      return nst == 3 ? (kh2 ? (const void*)attn_kernel<128, 2, 3> : (const void*)attn_kernel<128, 1, 3>)
-                      : (kh2 ? (const void*)attn_kernel<128, 2, 2> : (const void*)attn_kernel<128, 1, 2>);
-    return nst == 3 ? (kh2 ? (const void*)attn_kernel<64, 2, 3> : (const void*)attn_kernel<64, 1, 3>)
-                    : (kh2 ? (const void*)attn_kernel<64, 2, 2> : (const void*)attn_kernel<64, 1, 2>);
-  };
-  auto smem_for = [&](int n, int nst) {
-    // 1 KB alignment slack, K/V stages, Q, barriers, then the
-    // merge's receive area (and its staging area, unless that fits in the
-    // K/V stages and Q)
-    const size_t alias = (size_t)2 * nst * kKT * a.d * 2 + (size_t)rows_pad * a.d * 2;
-    size_t b = 1024 + alias + 64;
-    if (n > 1) {
-      const size_t maxr = (rows + n - 1) / n;
-      const size_t need = (size_t)n * maxr * (a.d + 8) * 2;
-      b += need;                     // receive area
-      if (need > alias) b += need;   // staging area of its own
-    }
-    return b;
-  };
-  // three stages where they fit (two tiles in flight behind the one being
-  // consumed), else two
-  auto stages_for = [&](int n) { return smem_for(n, 3) <= (size_t)max_smem_optin() ? 3 : 2; };
-  // Split count: the longest possible context (capacity plus the block) is
-  // cut into ns chunks of whole 64-key tiles, one CTA each, the ns CTAs of a
-  // (sequence, kv head) forming one cluster.  Cost model: waves of resident
-  // clusters times tiles per split (the pass is latency-bound, each tile a
-  // serial step), the fewest splits among equal costs; splits that would be
-  // left empty by the tile rounding are not launched.  Measured on 8 ragged
-  // sequences (256 to 8192 context rows): 2 / 3 / 4 / 6 / 8 splits gave a
-  // draft pass of 1178 / 1058 / 996 / 1031 / 1086 us, the fractional-wave
-  // cost's order.
   const int total = a.cap + a.B;
   const int ntiles = (total + kKT - 1) / kKT;
   const int need = a.b * a.nkv;  // clusters
-  int ns = 0;
-  long best = -1;
-  for (int n = 1; n <= kMaxSplits && n <= ntiles; ++n) {
-    const int per = (ntiles + n - 1) / n;       // tiles per split
-    const int used = (ntiles + per - 1) / per;  // splits that get keys
-    if (used != n) continue;
-    const int nst = stages_for(n);
-    const int fit = attn_max_clusters(kernel_for(false, nst), n, nthr, smem_for(n, nst));
-    if (fit <= 0) continue;
-    // one sequence: every cluster carries the same keys, so a partial wave
-    // costs a whole one; several (lengths unknown here, typically ragged):
-    // clusters of short sequences finish early and free their SMs, so waves
-    // count fractionally
-    const long cost = a.b > 1 ? (long)(1000.0 * (need > fit ? (double)need / fit : 1.0) * per)
-                              : 1000l * ((need + fit - 1) / fit) * per;
-    if (best < 0 || cost < best) {
-      best = cost;
-      ns = n;
+  struct Plan {
+    bool tc;
+    int nthr, ns, nst, tiles;
+    size_t smem;
+    const void* fn;
+  };
+  // the launch of one kernel family: split count, stages, shared memory
+  auto plan = [&](bool tc) {
+    Plan p{tc, 0, 0, 0, 0, 0, nullptr};
+    // tensor-memory kernel: two 128-row blocks, else one warp per 16 rows
+    const int rows_pad = tc ? 256 : nw * 16;
+    p.nthr = tc ? kTcThreads : (2 * nw < 10 ? 2 * nw : (nw > 10 ? nw : 10)) * 32;
+    auto kernel_for = [&](bool kh2, int nst) {
+      if (tc) {
+        if (a.d == 128) return nst == 3 ? (const void*)attn_tc_kernel<128, 3> : (const void*)attn_tc_kernel<128, 2>;
+        return nst == 3 ? (const void*)attn_tc_kernel<64, 3> : (const void*)attn_tc_kernel<64, 2>;
+      }
+      if (a.d == 128)
+        return nst == 3 ? (kh2 ? (const void*)attn_kernel<128, 2, 3> : (const void*)attn_kernel<128, 1, 3>)
+                        : (kh2 ? (const void*)attn_kernel<128, 2, 2> : (const void*)attn_kernel<128, 1, 2>);
+      return nst == 3 ? (kh2 ? (const void*)attn_kernel<64, 2, 3> : (const void*)attn_kernel<64, 1, 3>)
+                      : (kh2 ? (const void*)attn_kernel<64, 2, 2> : (const void*)attn_kernel<64, 1, 2>);
+    };
+    auto smem_for = [&](int n, int nst) {
+      // 1 KB alignment slack, K/V stages, Q, barriers (64 bytes; 128 with
+      // the tensor-memory kernel's), then the merge's receive area (and its
+      // staging area, unless that fits in the K/V stages and Q)
+      const size_t alias = (size_t)2 * nst * kKT * a.d * 2 + (size_t)rows_pad * a.d * 2;
+      size_t b = 1024 + alias + (tc ? 128 : 64);
+      if (n > 1) {
+        const size_t maxr = (rows + n - 1) / n;
+        const size_t need = (size_t)n * maxr * (a.d + 8) * 2;
+        b += need;                     // receive area
+        if (need > alias) b += need;   // staging area of its own
+      }
+      return b;
+    };
+    // three stages where they fit (two tiles in flight behind the one being
+    // consumed), else two
+    auto stages_for = [&](int n) { return smem_for(n, 3) <= (size_t)max_smem_optin() ? 3 : 2; };
+    // Split count: the longest possible context (capacity plus the block) is
+    // cut into ns chunks of whole 64-key tiles, one CTA each, the ns CTAs of
+    // a (sequence, kv head) forming one cluster.  Cost model: waves of
+    // resident clusters times tiles per split (the pass is latency-bound,
+    // each tile a serial step), the fewest splits among equal costs; splits
+    // that would be left empty by the tile rounding are not launched.
+    // Measured on 8 ragged sequences (256 to 8192 context rows): 2 / 3 / 4 /
+    // 6 / 8 splits gave a draft pass of 1178 / 1058 / 996 / 1031 / 1086 us,
+    // the fractional-wave cost's order.
+    long best = -1;
+    for (int n = 1; n <= kMaxSplits && n <= ntiles; ++n) {
+      const int per = (ntiles + n - 1) / n;       // tiles per split
+      const int used = (ntiles + per - 1) / per;  // splits that get keys
+      if (used != n) continue;
+      const int nst = stages_for(n);
+      const int fit = attn_max_clusters(kernel_for(false, nst), n, p.nthr, smem_for(n, nst));
+      if (fit <= 0) continue;
+      // one sequence: every cluster carries the same keys, so a partial wave
+      // costs a whole one; several (lengths unknown here, typically ragged):
+      // clusters of short sequences finish early and free their SMs, so
+      // waves count fractionally
+      const long cost = a.b > 1 ? (long)(1000.0 * (need > fit ? (double)need / fit : 1.0) * per)
+                                : 1000l * ((need + fit - 1) / fit) * per;
+      if (best < 0 || cost < best) {
+        best = cost;
+        p.ns = n;
+      }
     }
-  }
-  if (ns == 0) return cudaErrorInvalidConfiguration;  // no split count fits in shared memory
-  const int nst = stages_for(ns);
-  const int tiles = (ntiles + ns - 1) / ns;
-  const size_t smem = smem_for(ns, nst);
-  // helper warps take the second key half of every tile when a split has
-  // several tiles (one tile: the extra merge costs more than it saves)
-  const bool kh2 = nthr >= 2 * nw * 32 && tiles >= 2;
-  const void* fn = kernel_for(kh2, nst);
+    if (p.ns == 0) return p;  // no split count fits in shared memory
+    p.nst = stages_for(p.ns);
+    p.tiles = (ntiles + p.ns - 1) / p.ns;
+    p.smem = smem_for(p.ns, p.nst);
+    // warp-level kernel: helper warps take the second key half of every tile
+    // when a split has several tiles (one tile: the extra merge costs more
+    // than it saves)
+    const bool kh2 = !tc && p.nthr >= 2 * nw * 32 && p.tiles >= 2;
+    p.fn = kernel_for(kh2, p.nst);
+    return p;
+  };
+  Plan pl{false, 0, 0, 0, 0, 0, nullptr};
+  if (rows > 128 && rows <= 256) pl = plan(true);
+  if (pl.ns == 0 || pl.tiles < kTcMinTiles) pl = plan(false);
+  if (pl.ns == 0) return cudaErrorInvalidConfiguration;  // no split count fits in shared memory
+  const int ns = pl.ns;
+  const size_t smem = pl.smem;
+  const void* fn = pl.fn;
+  const int nthr = pl.nthr;
   cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (ns > kPortable) cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   // the layer's K and V caches as [b nkv cap] rows of d fp16, read in 64 x 64

@@ -625,23 +625,19 @@ constexpr int64_t kTcMinWeightBytes = 40ll << 20;
 // made the 272-CTA gate|up launch run in two waves), so CTAs that fit two to
 // an SM in shared memory take half the columns.
 
-// NSTV ring stages; the 128-row chunk also comes in a two-stage, 256-column
-// form for launches without split-K (its partial tile alone must fit in the
-// ring), which two CTAs can share an SM with.
-template <int MT, int NSTV = (MT == 16 ? 4 : 3)>
+template <int MT>
 struct TcGeo {
   static constexpr int MCH = MT * 8;  // activation rows per chunk = MMA N
   static_assert(MCH % 16 == 0 && MCH <= 128, "MMA N: a multiple of 16 up to 128");
-  static constexpr int NST = NSTV;                                     // ring stages
-  static constexpr uint32_t TCOLS = MT == 16 && NST > 2 ? 512 : 256;  // tensor-memory columns of a CTA
+  static constexpr int NST = MT == 16 ? 4 : 3;                // ring stages
+  static constexpr uint32_t TCOLS = MT == 16 ? 512 : 256;  // tensor-memory columns of a CTA
   static constexpr int ABYTES = 2 * MCH * 128;  // two [MCH][64] fp16 halves
   static constexpr int WBYTES = kTileBytes;      // int8 tile
   static constexpr int STAGE = WBYTES + ABYTES;  // both 1 KB multiples
   static constexpr int TX = WBYTES + ABYTES;
   static constexpr int TBYTES = (MCH * kTStride * 4 + 1023) / 1024 * 1024;
-  // the partial tile, and for split-K also the reduced tile, in the idle ring
-  static constexpr bool kSplitK = 2 * TBYTES <= NST * STAGE;
-  static_assert(TBYTES <= NST * STAGE, "epilogue tile must fit in the ring");
+  // the partial tile and, for split-K, the reduced tile, in the idle ring
+  static_assert(2 * TBYTES <= NST * STAGE, "epilogue tiles must fit in the ring");
   // tensor memory: accumulator in columns [0, MCH), then one A buffer of 64
   // columns (one k-tile of fp16 pairs) per ring stage from column TA, so one
   // MMA completion releases a stage's A buffer and its activations together
@@ -658,16 +654,12 @@ struct TcGeo {
 // Named barrier over the converter warps and the MMA warp.
 __device__ __forceinline__ void tc_bar() { asm volatile("bar.sync 1, %0;" ::"n"((kTcConv + 1) * 32) : "memory"); }
 
-template <int MT, int NSTV = (MT == 16 ? 4 : 3)>
+template <int MT>
 __global__ void __launch_bounds__(kTcThreads, 1) w8_gemm_kernel(const __grid_constant__ CUtensorMap xmap,
                                                                  const W8Args a) {
-  using G = TcGeo<MT, NSTV>;
+  using G = TcGeo<MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  if (!G::kSplitK && a.splits > 1) {  // the host never launches this; refuse rather than overrun the ring
-    if (threadIdx.x == 0 && a.status) atomicOr(a.status, kDevWaitTimeout);
-    return;
-  }
   // A ring stage holds a weight tile and the activation tile it meets; the
   // two halves are filled and released separately: the weights as soon as
   // the converter group has read them, the activations when the MMAs that
@@ -1140,12 +1132,6 @@ cudaError_t w8_gemm(const W8Args& a0, const __half* x, cudaStream_t st, bool pdl
   a.splits = w8_pick_splits(units, a.K / kTile);
   // keep the whole grid resident in one wave
   while (a.splits > 1 && units > occ * max_active_clusters(fn, threads, smem, a.splits)) --a.splits;
-  if (fn == (const void*)w8_gemm_kernel<16> && a.splits == 1) {
-    // no split-K: the two-stage, 256-column form fits two CTAs on an SM
-    fn = (const void*)w8_gemm_kernel<16, 2>;
-    smem = TcGeo<16, 2>::SMEM;
-    cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  }
   CUtensorMap map;
   if (!encode_tmap_2d(&map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, x, (uint64_t)a.K, (uint64_t)a.M,
                       (uint64_t)a.K * 2, 64, (uint32_t)mch, CU_TENSOR_MAP_SWIZZLE_128B))

@@ -102,6 +102,20 @@ def test_tiny_long_context_multi_tile_splits():
     _check_draft(cfg, W, model, kv, ws, hids, ctx)
 
 
+@pytest.mark.parametrize("lens", [(4000,), (4000, 100)])
+def test_tiny_two_block_query_tile_long_context(lens):
+    """The attention shape of the 27B-class drafter (40 query heads over 8 kv
+    heads, d 128, block 32: 160 query rows per kv head, two 128-row MMA
+    blocks) over a long context, where each split gets six 64-key tiles: the
+    launch that runs the tensor-memory attention.  With a 100-row second
+    sequence most of that sequence's splits hold no keys at all."""
+    import dataclasses
+    cfg = dataclasses.replace(TINY, nq=40, nkv=8, d=128, B=32, D=None, b=len(lens), ctx=lens,
+                              seed=1200 + len(lens))
+    W, model, ctx, kv, ws, hids = _setup(cfg, 256)
+    _check_draft(cfg, W, model, kv, ws, hids, ctx)
+
+
 def test_tiny_prefill_chunk_sizes_agree():
     # the same context committed 5 rows or 64 rows at a time gives one cache
     cfg = TINY.with_ctx((37,))
