@@ -51,9 +51,9 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     # DRAM read + write over algorithmic bytes of four captured launches of
     # each kernel on the 27B-class step (32 rows)
-    "w8_gemm_kernel": {"ratio": 543.048 / 533.504, "src": "c9550cad434bcfaa",
+    "w8_gemm_kernel": {"ratio": 534.574 / 533.504, "src": "db60a83621a45e58",
                        "capture": "profiles/w8_gemm_kernel_27b-class.md"},
-    "wmma_gemm_kernel": {"ratio": 377.436 / 374.928, "src": "c9550cad434bcfaa",
+    "wmma_gemm_kernel": {"ratio": 211.481 / 216.351, "src": "db60a83621a45e58",
                          "capture": "profiles/wmma_gemm_kernel_27b-class.md"},
     "lmhead_kernel": {"ratio": 781.06 / 777.99, "src": "01ee840985b7ff35",
                       "capture": "profiles/lmhead_kernel_qwen3-4b.md"},
@@ -492,6 +492,30 @@ def run_ours(args, rank, world, local_rank):
             g_step.replay()
             copies_out()
 
+        # the same calls and copies captured once into a CUDA graph whose side
+        # branch copies the target logits and hidden rows while the draft pass
+        # runs: every replay moves that step's inputs in and its results out
+        def overlapped_body():
+            cur = torch.cuda.current_stream()
+            side.wait_stream(cur)
+            with torch.cuda.stream(side):
+                logits.copy_(h_lg, non_blocking=True)
+                blk.copy_(h_blk, non_blocking=True)
+            t0.copy_(h_t0, non_blocking=True)
+            kv.len.copy_(len0)
+            api.dflash_draft_block(model, kv, t0, draft, ws)
+            cur.wait_stream(side)
+            api.dflash_verify_accept(logits, draft, n_out, corr, emitted, nxt, vws)
+            api.dflash_kv_commit(model, kv, blk, n_out, ws)
+            copies_out()
+
+        g_ov, g_ov_err = None, None
+        try:
+            g_ov = capture(torch, overlapped_body)
+        except Exception as exc:  # a runtime that cannot capture the pinned copies
+            g_ov_err = f"{type(exc).__name__}: {exc}"[:200]
+            torch.cuda.synchronize()
+
         def timed_host(fn):
             for _ in range(Wm):
                 fn()
@@ -511,6 +535,12 @@ def run_ours(args, rank, world, local_rank):
         assert np.array_equal(o_n.numpy(), np.asarray(nacc, dtype=np.int32)), "overlapped end-to-end step"
         e2e_serial_ms = timed_host(e2e_eager)
         e2e_graph_ms = timed_host(e2e_graph)
+        e2e_gov_ms = None
+        if g_ov is not None:
+            o_n.zero_()
+            e2e_gov_ms = timed_host(g_ov.replay)
+            assert np.array_equal(o_n.numpy(), np.asarray(nacc, dtype=np.int32)), "graph-overlapped end-to-end step"
+            del g_ov
         assert api.dflash_get_status() == 0, "device status flagged during the API timing"
         del g_step
 
@@ -597,15 +627,26 @@ def run_ours(args, rank, world, local_rank):
                             "avg_launch_us": statistics.mean(lm_ms) * 1e3},
         "clocks": clocks,
         "gpu_launches": K * launches_per_step(cfg),
-        "e2e": {"value": whole_job_rate(world, b, K, e2e_ms), "unit": "blocks/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
-                "path": "pinned host buffers in, dflash_draft_block + dflash_verify_accept + dflash_kv_commit "
-                        "called every step, results back to pinned host buffers; the target logits and hidden "
-                        "rows are copied on a second stream while the draft pass runs (verify waits for them)"},
+        "e2e": ({"value": whole_job_rate(world, b, K, e2e_gov_ms), "unit": "blocks/s", "h2d_bytes_per_step": h2d,
+                 "d2h_bytes_per_step": d2h,
+                 "path": "pinned host buffers in, dflash_draft_block + dflash_verify_accept + dflash_kv_commit, "
+                         "results back to pinned host buffers, all captured once into a CUDA graph replayed "
+                         "every step; the target logits and hidden rows are copied on a side branch of the "
+                         "graph while the draft pass runs (verify waits for them)"}
+                if e2e_gov_ms is not None else
+                {"value": whole_job_rate(world, b, K, e2e_ms), "unit": "blocks/s", "h2d_bytes_per_step": h2d,
+                 "d2h_bytes_per_step": d2h, "graph_capture_error": g_ov_err,
+                 "path": "pinned host buffers in, dflash_draft_block + dflash_verify_accept + dflash_kv_commit "
+                         "called every step, results back to pinned host buffers; the target logits and hidden "
+                         "rows are copied on a second stream while the draft pass runs (verify waits for them)"}),
+        "e2e_eager_overlapped": {"value": whole_job_rate(world, b, K, e2e_ms), "unit": "blocks/s",
+                                 "path": "the calls issued eagerly every step, the target logits and hidden rows "
+                                         "copied on a second stream while the draft pass runs"},
         "e2e_serial": {"value": whole_job_rate(world, b, K, e2e_serial_ms), "unit": "blocks/s",
-                       "path": "the same with every copy on the step's stream, before and after the calls"},
+                       "path": "the calls issued eagerly with every copy on the step's stream, before and after "
+                               "the calls"},
         "e2e_graph": {"value": whole_job_rate(world, b, K, e2e_graph_ms), "unit": "blocks/s",
-                      "path": "the same copies around a replay of the captured step"},
+                      "path": "every copy on the step's stream around a replay of the captured step"},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         C = int(ctx[0])
