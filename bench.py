@@ -325,7 +325,15 @@ def run_ours(args, rank, world, local_rank):
     kv.len.copy_(len0)
 
     t0 = torch.from_numpy(synth.tokens(cfg.seed, "t0", b, cfg.V)).to(dev)
-    draft = torch.empty((b, B - 1), dtype=torch.int32, device=dev)
+    # the step's outputs (drafts, accept count, correction token, next token,
+    # emitted tokens) are views of one device buffer, each 16-byte aligned, so
+    # the end-to-end loop brings them back with a single copy
+    al4 = lambda n: (n + 3) // 4 * 4
+    o_sz = [b * (B - 1), b, b, b, b * cfg.R]
+    o_off = np.cumsum([0] + [al4(n) for n in o_sz])
+    outbuf = torch.zeros(int(o_off[-1]), dtype=torch.int32, device=dev)
+    draft, n_out, corr, nxt, emitted = (outbuf[int(o_off[i]):int(o_off[i]) + o_sz[i]] for i in range(5))
+    draft, emitted = draft.view(b, B - 1), emitted.view(b, cfg.R)
     api.dflash_draft_block(model, kv, t0, draft, ws)
     torch.cuda.synchronize()
     nacc = synth.accept_lengths(cfg.seed, "acc", b, B - 1, cfg.accept_mean)
@@ -333,10 +341,6 @@ def run_ours(args, rank, world, local_rank):
     logits = torch.from_numpy(lg_host).to(dev)
     blk_host = np.stack([synth.target_hidden(cfg.seed, f"blk{j}", B, cfg.k * cfg.H) for j in range(b)])
     blk = torch.from_numpy(blk_host).to(dev)
-    n_out = torch.empty(b, dtype=torch.int32, device=dev)
-    corr = torch.empty(b, dtype=torch.int32, device=dev)
-    emitted = torch.empty((b, cfg.R), dtype=torch.int32, device=dev)
-    nxt = torch.empty(b, dtype=torch.int32, device=dev)
     vws = torch.zeros(api.dflash_verify_workspace_size(b, cfg.R, cfg.V), dtype=torch.uint8, device=dev)
 
     def step():
@@ -438,12 +442,10 @@ def run_ours(args, rank, world, local_rank):
         # of the drafts and accept outputs
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
         h_t0, h_lg, h_blk = pin(t0.cpu().numpy()), pin(lg_host), pin(blk_host)
-        o_draft = torch.empty_like(draft, device="cpu").pin_memory()
-        o_n = torch.empty_like(n_out, device="cpu").pin_memory()
-        o_em = torch.empty_like(emitted, device="cpu").pin_memory()
-        o_nx = torch.empty_like(nxt, device="cpu").pin_memory()
+        o_all = torch.empty_like(outbuf, device="cpu").pin_memory()
+        o_n = o_all[int(o_off[1]):int(o_off[1]) + b]
         h2d = h_t0.numel() * 4 + h_lg.numel() * 4 + h_blk.numel() * 2
-        d2h = (o_draft.numel() + o_n.numel() + o_em.numel() + o_nx.numel()) * 4
+        d2h = o_all.numel() * 4
 
         def copies_in():
             t0.copy_(h_t0, non_blocking=True)
@@ -451,10 +453,7 @@ def run_ours(args, rank, world, local_rank):
             blk.copy_(h_blk, non_blocking=True)
 
         def copies_out():
-            o_draft.copy_(draft, non_blocking=True)
-            o_n.copy_(n_out, non_blocking=True)
-            o_em.copy_(emitted, non_blocking=True)
-            o_nx.copy_(nxt, non_blocking=True)
+            o_all.copy_(outbuf, non_blocking=True)  # drafts, accept outputs, emitted tokens
 
         def e2e_eager():
             copies_in()

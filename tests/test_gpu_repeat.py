@@ -5,7 +5,9 @@ cluster shared memory, the attention merge in split order, no float atomics),
 so repeated passes over the same cache must give identical bits.  A pass that
 drifts between runs has a race even when each run stays within the oracle
 tolerance.  Eight sequences of the batched Qwen3-8B shape give 128 block rows,
-the launches of the 128-row projection kernel; one layer keeps it short.
+the launches of the 128-row projection kernel; the 27B-class shape at 4096
+context rows gives the 32-row tensor-memory projections (two CTAs per SM)
+and the tensor-memory attention.  One layer keeps both short.
 """
 import dataclasses
 
@@ -23,9 +25,18 @@ if gpu_available():
     DEV = torch.device("cuda:0")
 
 
-@pytest.mark.parametrize("mode", ["early", "stream"])
-def test_batched_draft_pass_repeats_bitwise(mode):
-    cfg = dataclasses.replace(configs.BATCHED_8B, L=1, ctx=(2048,), ctx_range=None)
+CASES = [("b8-qwen3-8b", "early"), ("b8-qwen3-8b", "stream"), ("27b-class-ctx4096", "early")]
+
+
+def _cfg(name):
+    if name == "b8-qwen3-8b":
+        return dataclasses.replace(configs.BATCHED_8B, L=1, ctx=(2048,), ctx_range=None)
+    return dataclasses.replace(configs.DENSE_27B, L=1, ctx=(4096,))
+
+
+@pytest.mark.parametrize("shape,mode", CASES)
+def test_draft_pass_repeats_bitwise(shape, mode):
+    cfg = _cfg(shape)
     with api.launch_mode(api.LAUNCH_EARLY if mode == "early" else api.LAUNCH_STREAM_ORDER):
         W = synth.drafter_weights(cfg)
         model = api.DeviceDrafter(cfg, synth.FloatWeights(W), DEV)
