@@ -39,10 +39,10 @@ constexpr int kMaxSplits = 16;  // one (non-portable) cluster of splits
 constexpr int kPortable = 8;    // largest cluster every sm_90+ part accepts
 constexpr int kKT = 64;         // keys per tile
 
-// keys [k0, k1) of split sp out of ns equal, kt-aligned chunks of `total`
-__device__ __forceinline__ void split_range(int total, int sp, int ns, int kt, int& k0, int& k1) {
+// keys [k0, k1) of split sp out of ns equal, 64-aligned chunks of `total`
+__device__ __forceinline__ void split_range(int total, int sp, int ns, int& k0, int& k1) {
   int chunk = (total + ns - 1) / ns;
-  chunk = (chunk + kt - 1) / kt * kt;
+  chunk = (chunk + kKT - 1) / kKT * kKT;
   k0 = min(total, sp * chunk);
   k1 = min(total, k0 + chunk);
 }
@@ -53,26 +53,24 @@ __device__ __forceinline__ float ex2(float x) {  // 2^x, hardware approximation;
   return y;
 }
 
-// Byte offset of 16-byte chunk ch (of D / 8) of row r in a K or V stage of
-// KT rows: [D / 64 column halves][KT rows][128 bytes], chunk c of a row at
-// c ^ (r % 8) (the layout a 64-column x KT-row fp16 tensor-map box with
-// 128-byte swizzle writes).
-template <int KT = kKT>
+// Byte offset of 16-byte chunk ch (of D / 8) of row r in a K or V stage:
+// [D / 64 column halves][64 rows][128 bytes], chunk c of a row at c ^ (r % 8)
+// (the layout a 64 x 64 fp16 tensor-map box with 128-byte swizzle writes).
 __device__ __forceinline__ int kv_off(int r, int ch) {
-  return (ch >> 3) * (KT * 128) + (r << 7) + (((ch & 7) ^ (r & 7)) << 4);
+  return ((ch >> 3) << 13) + (r << 7) + (((ch & 7) ^ (r & 7)) << 4);
 }
 
-// Gathers keys [t0, t0 + KT) of (sequence j, kv head g) row by row with
+// Gathers keys [t0, t0 + 64) of (sequence j, kv head g) row by row with
 // cp.async (threads tid of nthr) into K/V stage stg, in the swizzled layout of a tensor-map tile:
 // part 0 = committed context rows t < Lold only, 1 = the rest (rows a folded
 // commit appends, the block's keys, zero fill past k1), 2 = all.  Cache row
 // t < L of the head is row row0 + t of kc / vc; block key t - L is row
 // (j B + t - L) of kblk / vblk.
-template <int D, int KT = kKT>
+template <int D>
 __device__ __forceinline__ void gather_tile(const AttnArgs& a, uint8_t* sK, uint8_t* sV, int stg, int t0, int part,
                                             int k1, int Lold, int L, int row0, int j, int g, int tid, int nthr) {
-  constexpr int KVB = KT * D * 2;
-  for (int c = tid; c < KT * (D / 8); c += nthr) {
+  constexpr int KVB = kKT * D * 2;
+  for (int c = tid; c < kKT * (D / 8); c += nthr) {
     const int r = c / (D / 8), ch = c % (D / 8);
     const int t = t0 + r;
     const bool ok = t < k1;
@@ -92,7 +90,7 @@ __device__ __forceinline__ void gather_tile(const AttnArgs& a, uint8_t* sK, uint
         vs = a.vblk + off;
       }
     }
-    const int so = stg * KVB + kv_off<KT>(r, ch);
+    const int so = stg * KVB + kv_off(r, ch);
     cp_async16(sK + so, ks, ok);
     cp_async16(sV + so, vs, ok);
   }
@@ -194,7 +192,7 @@ __global__ void __launch_bounds__(320, 1)
   if (a.nacc) L += commit_count(a.len[j], a.nacc[j], a.rps, a.cap);
   const int total = L + a.B;
   int k0, k1;
-  split_range(total, sp, ns, kKT, k0, k1);
+  split_range(total, sp, ns, k0, k1);
   const int ntile = (k1 - k0 + kKT - 1) / kKT;
   const int row0 = (j * a.nkv + g) * a.cap;  // this head's first cache row in the tensor maps
   // tile i is a whole tile of committed context (one tensor-map box per 64
@@ -582,7 +580,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (a.nacc) L += commit_count(a.len[j], a.nacc[j], a.rps, a.cap);
   const int total = L + a.B;
   int k0, k1;
-  split_range(total, sp, ns, kKT, k0, k1);
+  split_range(total, sp, ns, k0, k1);
   const int ntile = (k1 - k0 + kKT - 1) / kKT;
   const int row0 = (j * a.nkv + g) * a.cap;
   auto is_tma = [&](int i) { return k0 + (i + 1) * kKT <= min(k1, Lold); };
