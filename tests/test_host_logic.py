@@ -129,3 +129,58 @@ def test_float_weights_view_reads_grid_times_scale():
     w4 = synth.FloatWeights(W4)["down0"]
     assert w4[r, 130] == np.float32(q4[r, 130]) * np.float32(s4[r, 1])
     assert w4[r, 127] == np.float32(q4[r, 127]) * np.float32(s4[r, 0])
+
+
+def _tiled_attention(s, v, tile=64, thresh=8.0):
+    """The tensor-memory attention's per-split loop in float64: scores s
+    [rows][keys] in log2 units, a reference maximum raised only when a tile's
+    maximum exceeds it by more than `thresh`, O and the sum rescaled only
+    then.  Returns the split's normalised output, its log2 log-sum-exp and
+    the largest p it formed."""
+    rows, keys = s.shape
+    mref = np.full(rows, -np.inf)
+    lsum = np.zeros(rows)
+    o = np.zeros((rows, v.shape[1]))
+    pmax = 0.0
+    for t0 in range(0, keys, tile):
+        st = s[:, t0:t0 + tile]
+        mnew = np.maximum(mref, st.max(axis=1))
+        resc = np.isfinite(mref) & (mnew - mref > thresh)
+        corr = np.where(resc, np.exp2(np.where(resc, mref - mnew, 0.0)), 1.0)
+        mref = np.where(~np.isfinite(mref) | resc, mnew, mref)
+        o *= corr[:, None]
+        lsum *= corr
+        p = np.exp2(st - mref[:, None])
+        pmax = max(pmax, float(p.max()))
+        o += p @ v[t0:t0 + tile]
+        lsum += p.sum(axis=1)
+    return o / lsum[:, None], mref + np.log2(lsum), pmax
+
+
+def test_conditional_rescale_softmax_is_softmax():
+    """A reference maximum that lags the running maximum by up to 8 (log2
+    units) leaves every p <= 2^8 and gives the same normalised attention as
+    softmax by definition; the split merge by log-sum-exp weights does too."""
+    rng = np.random.default_rng(7)
+    rows, keys, d = 40, 6 * 64 + 17, 32
+    v = rng.standard_normal((keys, d))
+    # scores that climb slowly (the reference stays stale) and then jump
+    # (the reference is raised and O rescaled)
+    ramp = np.linspace(0.0, 6.0, keys)[None, :]
+    jump = np.where(np.arange(keys) >= 4 * 64, 20.0, 0.0)[None, :]
+    s = rng.standard_normal((rows, keys)) * 2.0 + ramp + jump
+    ref = np.exp2(s - s.max(axis=1, keepdims=True))
+    ref = (ref / ref.sum(axis=1, keepdims=True)) @ v
+    out, _, pmax = _tiled_attention(s, v)
+    assert np.abs(out - ref).max() <= 1e-12 * np.abs(ref).max()
+    assert pmax <= 2.0 ** 8
+    # without the jump the reference never moves after the first tile
+    _, _, pmax2 = _tiled_attention(s - jump, v)
+    assert 1.0 < pmax2 <= 2.0 ** 8
+    # split the keys in 3 and merge: weights 2^(lse - max lse)
+    bounds = [0, 192, 320, keys]
+    parts = [_tiled_attention(s[:, a:b], v[a:b]) for a, b in zip(bounds[:-1], bounds[1:])]
+    lse = np.stack([p[1] for p in parts])
+    w = np.exp2(lse - lse.max(axis=0))
+    merged = sum(w[i][:, None] * parts[i][0] for i in range(len(parts))) / w.sum(axis=0)[:, None]
+    assert np.abs(merged - ref).max() <= 1e-12 * np.abs(ref).max()
