@@ -26,10 +26,14 @@ if gpu_available():
     from block_diffusion_speculative_draft_gb300 import api
     DEV = torch.device("cuda:0")
 
-CASES = [TINY, dataclasses.replace(TINY, b=3, ctx=(), ctx_range=(20, 90), seed=1200), QWEN3_4B]
+# the last case has the 27B-class attention shape (160 query rows per kv
+# head) over 4000 context rows: the tensor-memory attention, with the rows
+# the folded commit appends gathered after its dependency wait
+CASES = [TINY, dataclasses.replace(TINY, b=3, ctx=(), ctx_range=(20, 90), seed=1200), QWEN3_4B,
+         dataclasses.replace(TINY, nq=40, nkv=8, d=128, B=32, D=None, ctx=(4000,), seed=1210)]
 
 
-@pytest.mark.parametrize("cfg", CASES, ids=["tiny", "tiny-b3-ragged", "qwen3-4b"])
+@pytest.mark.parametrize("cfg", CASES, ids=["tiny", "tiny-b3-ragged", "qwen3-4b", "tiny-two-block-ctx4000"])
 def test_commit_draft_matches_commit_then_draft(cfg):
     b, B = cfg.b, cfg.B
     rps = B
